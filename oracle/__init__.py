@@ -1,0 +1,125 @@
+"""CPU oracle for exact softmax attention -- test infrastructure only.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
+legs of ``bench.py`` may import this package.  The product path (the CUDA
+library and its Python binding) never imports it and shares no code with it.
+
+``attention_rows`` / ``attention_fwd`` call the plain fp64 C implementation in
+``attention_oracle.c`` (the definition S = scale*QK^T, P = softmax_row(S),
+O = PV, L = m + ln sum exp(S - m), from the Flash Attention 2 page "Standard
+Attention" and FlashAttention V2 in depth section 6.1).  ``tiled_reference``
+restates the tiled online-softmax algorithm of FlashAttention V2 in depth
+section 6.1 in numpy; tests use it to check that tiling is exact.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attention_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+FP16 = 0
+BF16 = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle into ``oracle/liboracle.so`` (gcc, OpenMP)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + ".tmp%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        p16 = ctypes.POINTER(ctypes.c_uint16)
+        pd = ctypes.POINTER(ctypes.c_double)
+        pi64 = ctypes.POINTER(ctypes.c_int64)
+        i64 = ctypes.c_int64
+        lib.oracle_attention_rows.argtypes = [p16, p16, p16, ctypes.c_int, i64, i64, i64, i64,
+                                              ctypes.c_double, ctypes.c_int, pi64, pi64, i64, pd, pd,
+                                              ctypes.c_int]
+        lib.oracle_attention_rows.restype = ctypes.c_int
+        lib.oracle_attention_fwd.argtypes = [p16, p16, p16, ctypes.c_int, i64, i64, i64, i64,
+                                             ctypes.c_double, ctypes.c_int, pd, pd, ctypes.c_int]
+        lib.oracle_attention_fwd.restype = ctypes.c_int
+        lib.oracle_widen.argtypes = [p16, ctypes.c_int, i64, pd]
+        lib.oracle_widen.restype = ctypes.c_int
+        lib.oracle_max_threads.argtypes = []
+        lib.oracle_max_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _bits(a: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("oracle inputs are 16-bit bit patterns (uint16), got %s" % a.dtype)
+    return a
+
+
+def _ptr(a, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def max_threads() -> int:
+    """OpenMP threads the oracle uses by default."""
+    return int(_load().oracle_max_threads())
+
+
+def widen(bits: np.ndarray, dtype: int) -> np.ndarray:
+    """Exact fp16/bf16 -> float64 widening done by the oracle's own decoder."""
+    bits = _bits(bits)
+    out = np.empty(bits.shape, dtype=np.float64)
+    rc = _load().oracle_widen(_ptr(bits, ctypes.c_uint16), int(dtype), bits.size, _ptr(out, ctypes.c_double))
+    if rc:
+        raise ValueError("oracle_widen failed (%d)" % rc)
+    return out
+
+
+def attention_fwd(q, k, v, dtype: int, scale: float, causal: bool, threads: int = 0):
+    """Full O [B,H,N,d] and L [B,H,N] in float64 from 16-bit bit patterns [B,H,N,d]."""
+    q, k, v = _bits(q), _bits(k), _bits(v)
+    if q.ndim != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must share one [B,H,N,d] shape")
+    B, H, N, d = q.shape
+    o = np.empty((B, H, N, d), dtype=np.float64)
+    lse = np.empty((B, H, N), dtype=np.float64)
+    rc = _load().oracle_attention_fwd(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
+                                      _ptr(v, ctypes.c_uint16), int(dtype), B, H, N, d, float(scale),
+                                      int(bool(causal)), _ptr(o, ctypes.c_double),
+                                      _ptr(lse, ctypes.c_double), int(threads))
+    if rc:
+        raise ValueError("oracle_attention_fwd failed (%d)" % rc)
+    return o, lse
+
+
+def attention_rows(q, k, v, dtype: int, scale: float, causal: bool, bh_idx, row_idx, threads: int = 0):
+    """O rows [count, d] and L [count] for the (bh, row) samples, float64."""
+    q, k, v = _bits(q), _bits(k), _bits(v)
+    B, H, N, d = q.shape
+    bh_idx = np.ascontiguousarray(bh_idx, dtype=np.int64)
+    row_idx = np.ascontiguousarray(row_idx, dtype=np.int64)
+    count = bh_idx.size
+    o = np.empty((count, d), dtype=np.float64)
+    lse = np.empty((count,), dtype=np.float64)
+    rc = _load().oracle_attention_rows(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
+                                       _ptr(v, ctypes.c_uint16), int(dtype), B, H, N, d, float(scale),
+                                       int(bool(causal)), _ptr(bh_idx, ctypes.c_int64),
+                                       _ptr(row_idx, ctypes.c_int64), count, _ptr(o, ctypes.c_double),
+                                       _ptr(lse, ctypes.c_double), int(threads))
+    if rc:
+        raise ValueError("oracle_attention_rows failed (%d)" % rc)
+    return o, lse

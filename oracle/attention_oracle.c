@@ -1,0 +1,224 @@
+/*
+ * Plain CPU oracle for exact softmax attention (test infrastructure only).
+ *
+ * Only the tests, the package's smoke check and the benchmark's CPU-baseline
+ * leg may load this library.  The product path never calls it and shares no
+ * code with it.
+ *
+ * What it computes, per (batch b, head h), with every 16-bit input widened
+ * exactly to double first:
+ *
+ *   s_ij = scale * sum_k q_ik k_jk        "Standard Attention": S = QK^T
+ *                                         (Flash Attention 2 page, Standard
+ *                                         Attention; the scale 1/sqrt(d) is the
+ *                                         one of FlashAttention V2 in depth
+ *                                         section 6.1 and of Lesson 6.6
+ *                                         "A quick recap of standard attention")
+ *   causal: key j is visible to query i only when j <= i
+ *                                         (Flash Attention 2 page, Causal
+ *                                         masking, the mask M; FlashAttention
+ *                                         V2 in depth section 5.1)
+ *   m_i  = max over visible j of s_ij
+ *   p_ij = exp(s_ij - m_i) / sum_j exp(s_ij - m_i)     row softmax
+ *   o_i  = sum_j p_ij v_j                              O = PV
+ *   L_i  = m_i + ln sum_j exp(s_ij - m_i)              the logsumexp that
+ *                                         FlashAttention V2 in depth sections
+ *                                         6.1 and 7.1 store for the backward
+ *
+ * It is the plain definition: one full row of S is formed, then the full row
+ * of P, then the row of O.  There is no tiling, no online softmax and no
+ * reordering beyond the row-by-row evaluation; masked keys (exp(-inf) = 0)
+ * are left out of the sums, which adds nothing to them.
+ *
+ * Parity: pinned by the tests against the worked example of the Flash
+ * Attention 2 page, the one-row practice of Lesson 6.6, closed forms and
+ * invariants (row sums, identical keys, single key, constant values, causal
+ * row 0) and a high-precision brute force on tiny inputs.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORACLE_FP16 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_OK = 0, ORACLE_ERR_ARG = 1, ORACLE_ERR_NOMEM = 2 };
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+static double half_bits_to_double(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double mag;
+    if (e == 0) {
+        mag = ldexp((double)f, -24);               /* subnormal: f * 2^-14 * 2^-10 */
+    } else if (e == 31) {
+        mag = f ? NAN : INFINITY;
+    } else {
+        mag = ldexp((double)(1024 + f), e - 25);   /* (1 + f/1024) * 2^(e-15) */
+    }
+    return sign ? -mag : mag;
+}
+
+/* bfloat16: the upper 16 bits of an IEEE 754 binary32
+ * (1 sign bit, 8 exponent bits with bias 127, 7 fraction bits). */
+static double bfloat_bits_to_double(uint16_t b) {
+    int sign = (b >> 15) & 1;
+    int e = (b >> 7) & 0xff;
+    int f = b & 0x7f;
+    double mag;
+    if (e == 0) {
+        mag = ldexp((double)f, -133);              /* f * 2^-126 * 2^-7 */
+    } else if (e == 255) {
+        mag = f ? NAN : INFINITY;
+    } else {
+        mag = ldexp((double)(128 + f), e - 134);   /* (1 + f/128) * 2^(e-127) */
+    }
+    return sign ? -mag : mag;
+}
+
+static double widen(uint16_t bits, int dtype) {
+    return dtype == ORACLE_BF16 ? bfloat_bits_to_double(bits) : half_bits_to_double(bits);
+}
+
+/* Exact widening of n 16-bit values, exported so tests can check it against a
+ * library conversion. */
+int oracle_widen(const uint16_t* src, int dtype, int64_t n, double* dst) {
+    if (!src || !dst || n < 0 || (dtype != ORACLE_FP16 && dtype != ORACLE_BF16)) return ORACLE_ERR_ARG;
+    for (int64_t i = 0; i < n; ++i) dst[i] = widen(src[i], dtype);
+    return ORACLE_OK;
+}
+
+/* One query row i of one (b, h) slice, by the definition above.
+ * qrow: d doubles; kmat, vmat: N x d doubles (row-major); srow: N doubles of
+ * scratch for the materialised S row (then P row). */
+static void attention_row(const double* qrow, const double* kmat, const double* vmat,
+                          int64_t N, int64_t d, double scale, int causal, int64_t i,
+                          double* srow, double* orow, double* lse) {
+    int64_t nvis = causal ? (i + 1 < N ? i + 1 : N) : N;
+    /* S row: s_ij = scale * q_i . k_j */
+    double m = -INFINITY;
+    for (int64_t j = 0; j < nvis; ++j) {
+        const double* kj = kmat + j * d;
+        double acc = 0.0;
+        for (int64_t c = 0; c < d; ++c) acc += qrow[c] * kj[c];
+        srow[j] = scale * acc;
+        if (srow[j] > m) m = srow[j];
+    }
+    /* P row: exp(s - m) / sum */
+    double sum = 0.0;
+    for (int64_t j = 0; j < nvis; ++j) {
+        srow[j] = exp(srow[j] - m);
+        sum += srow[j];
+    }
+    for (int64_t j = 0; j < nvis; ++j) srow[j] /= sum;
+    /* O row: sum_j p_ij v_j */
+    for (int64_t c = 0; c < d; ++c) orow[c] = 0.0;
+    for (int64_t j = 0; j < nvis; ++j) {
+        const double* vj = vmat + j * d;
+        double p = srow[j];
+        for (int64_t c = 0; c < d; ++c) orow[c] += p * vj[c];
+    }
+    *lse = m + log(sum);
+}
+
+static int check_args(const void* q, const void* k, const void* v, int dtype, int64_t B, int64_t H,
+                      int64_t N, int64_t d, double scale) {
+    if (!q || !k || !v) return ORACLE_ERR_ARG;
+    if (dtype != ORACLE_FP16 && dtype != ORACLE_BF16) return ORACLE_ERR_ARG;
+    if (B < 1 || H < 1 || N < 1 || d < 1) return ORACLE_ERR_ARG;
+    if (!isfinite(scale)) return ORACLE_ERR_ARG;
+    return ORACLE_OK;
+}
+
+/*
+ * Selected rows.  q, k, v: [B, H, N, d] 16-bit bit patterns (dtype 0 = fp16,
+ * 1 = bf16).  For each sample t, bh_idx[t] in [0, B*H) names the (b, h) slice
+ * (bh = b*H + h) and row_idx[t] in [0, N) the query row; o_out receives
+ * count x d doubles, lse_out count doubles (natural log).  Samples of the same
+ * slice should be adjacent so that slice's K and V are widened once.
+ * threads <= 0 uses the OpenMP default.
+ */
+int oracle_attention_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v, int dtype,
+                          int64_t B, int64_t H, int64_t N, int64_t d, double scale, int causal,
+                          const int64_t* bh_idx, const int64_t* row_idx, int64_t count,
+                          double* o_out, double* lse_out, int threads) {
+    int rc = check_args(q, k, v, dtype, B, H, N, d, scale);
+    if (rc) return rc;
+    if (count < 0 || (count > 0 && (!bh_idx || !row_idx || !o_out || !lse_out))) return ORACLE_ERR_ARG;
+    for (int64_t t = 0; t < count; ++t)
+        if (bh_idx[t] < 0 || bh_idx[t] >= B * H || row_idx[t] < 0 || row_idx[t] >= N) return ORACLE_ERR_ARG;
+#ifdef _OPENMP
+    if (threads > 0) omp_set_num_threads(threads);
+#else
+    (void)threads;
+#endif
+    double* kmat = (double*)malloc(sizeof(double) * (size_t)(N * d));
+    double* vmat = (double*)malloc(sizeof(double) * (size_t)(N * d));
+    if (!kmat || !vmat) { free(kmat); free(vmat); return ORACLE_ERR_NOMEM; }
+    int status = ORACLE_OK;
+    int64_t t0 = 0;
+    while (t0 < count) {
+        int64_t bh = bh_idx[t0];
+        int64_t t1 = t0;
+        while (t1 < count && bh_idx[t1] == bh) ++t1;
+        const uint16_t* ks = k + bh * N * d;
+        const uint16_t* vs = v + bh * N * d;
+        for (int64_t x = 0; x < N * d; ++x) { kmat[x] = widen(ks[x], dtype); vmat[x] = widen(vs[x], dtype); }
+        int nomem = 0;
+#pragma omp parallel reduction(| : nomem)
+        {
+            double* srow = (double*)malloc(sizeof(double) * (size_t)N);
+            double* qrow = (double*)malloc(sizeof(double) * (size_t)d);
+            if (!srow || !qrow) {
+                nomem = 1;
+            } else {
+#pragma omp for schedule(dynamic, 1)
+                for (int64_t t = t0; t < t1; ++t) {
+                    int64_t i = row_idx[t];
+                    const uint16_t* qs = q + (bh * N + i) * d;
+                    for (int64_t c = 0; c < d; ++c) qrow[c] = widen(qs[c], dtype);
+                    attention_row(qrow, kmat, vmat, N, d, scale, causal, i, srow, o_out + t * d, lse_out + t);
+                }
+            }
+            free(srow);
+            free(qrow);
+        }
+        if (nomem) { status = ORACLE_ERR_NOMEM; break; }
+        t0 = t1;
+    }
+    free(kmat);
+    free(vmat);
+    return status;
+}
+
+/* Every row: o_out [B, H, N, d] doubles, lse_out [B, H, N] doubles. */
+int oracle_attention_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, int dtype,
+                         int64_t B, int64_t H, int64_t N, int64_t d, double scale, int causal,
+                         double* o_out, double* lse_out, int threads) {
+    int rc = check_args(q, k, v, dtype, B, H, N, d, scale);
+    if (rc) return rc;
+    if (!o_out || !lse_out) return ORACLE_ERR_ARG;
+    int64_t* bh_idx = (int64_t*)malloc(sizeof(int64_t) * (size_t)N);
+    int64_t* row_idx = (int64_t*)malloc(sizeof(int64_t) * (size_t)N);
+    if (!bh_idx || !row_idx) { free(bh_idx); free(row_idx); return ORACLE_ERR_NOMEM; }
+    for (int64_t bh = 0; bh < B * H && rc == ORACLE_OK; ++bh) {
+        for (int64_t i = 0; i < N; ++i) { bh_idx[i] = bh; row_idx[i] = i; }
+        rc = oracle_attention_rows(q, k, v, dtype, B, H, N, d, scale, causal, bh_idx, row_idx, N,
+                                   o_out + bh * N * d, lse_out + bh * N, threads);
+    }
+    free(bh_idx);
+    free(row_idx);
+    return rc;
+}
+
+/* Threads OpenMP will use (1 without OpenMP); reported by the CPU baseline. */
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
