@@ -1,0 +1,345 @@
+"""Benchmark of the exact tiled attention forward pass on GB300.
+
+One step = one forward pass (S = QK^T, online softmax, O = PV, LSE) over the
+whole workload, i.e. one launch of the forward kernel through the C ABI.
+Default workload: B=1, H=32, N=16384, d=128, bf16, causal -- the
+long-context batch-1 case the throughput target is set on.  Inputs (403 MB)
+exceed the 129 MB L2, so no flush is needed between steps.
+
+Prints one JSON line.  ``value`` is forward TFLOP/s (4*B*H*N^2*d, halved for
+causal) with inputs resident in HBM; ``e2e`` is the same metric through the
+host-buffer entry point with the host<->device copies inside the timed
+region; ``roofline`` relates the kernel's CUDA-event time to the measured
+dense bf16 tensor peak; ``cpu_baseline`` times the plain CPU oracle on a
+bounded sample of rows.  ``--impl reference`` times the oracle alone.
+
+Under torchrun (WORLD_SIZE > 1) every rank runs the same workload on its own
+GPU (independent replicas: the forward pass has no exchange step), timing is
+the max over ranks and ``value`` sums the ranks' work.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from exact_tiled_attention_fa2_gb300 import synthetic as sy  # noqa: E402
+
+METRIC = "forward attention TFLOP/s at 1 GB300 and % of dense FP16/BF16 tensor peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = 4
+KERNEL_SOURCES = ["fa2_fwd_kernel.cuh", "sm103_ptx.cuh", "fa2_internal.h", "fa2_abi.cu"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "exact_tiled_attention_fa2_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "of measured (bf16 burst, MEASURED_PEAKS.json)"
+    except Exception:
+        return 1900.0, "of fallback (1.9 PFLOP/s bf16)"
+
+
+def recorded_traffic(workload: int):
+    """DRAM bytes per launch from the committed ncu summary, if it matches this kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic_per_launch.txt")
+    if not os.path.exists(path):
+        return None
+    src = kernel_source_hash()
+    with open(path) as f:
+        for line in f:
+            parts = dict(p.split("=", 1) for p in line.split() if "=" in p)
+            if parts.get("kernel_sha") == src and parts.get("workload") == str(workload):
+                try:
+                    return float(parts["bytes_per_launch"])
+                except (KeyError, ValueError):
+                    return None
+    return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sms.append(float(f[1]))
+                maxes.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+def oracle_sample(w: sy.Workload, q, k, v, target_s: float, rng, threads: int = 0):
+    """Run the CPU oracle on random rows until ~target_s seconds; return (flops, seconds, rows)."""
+    import oracle
+
+    BH = w.B * w.H
+    done_flops, done_s, done_rows = 0.0, 0.0, 0
+    batch = 8
+    while done_s < target_s:
+        bh = np.sort(rng.integers(0, BH, size=batch))
+        rows = rng.integers(0, w.N, size=batch)
+        t0 = time.perf_counter()
+        oracle.attention_rows(q, k, v, w.dtype, w.scale, w.causal, bh, rows, threads=threads)
+        dt = time.perf_counter() - t0
+        keys = (rows + 1) if w.causal else np.full(batch, w.N)
+        done_flops += float(4.0 * w.d * keys.sum())
+        done_s += dt
+        done_rows += batch
+        if dt < target_s / 20:
+            batch *= 2
+    return done_flops, done_s, done_rows
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+
+    q, k, v = w.inputs()
+    rng = np.random.default_rng(12345)
+    per_step = max(0.5, min(4.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, q, k, v, per_step / 4, rng)
+    flops, secs, rows = 0.0, 0.0, 0
+    for _ in range(args.steps):
+        f, s, r = oracle_sample(w, q, k, v, per_step, rng)
+        flops, secs, rows = flops + f, secs + s, rows + r
+    value = flops / secs / 1e12
+    cores = oracle.max_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w, args.gpus),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "%d random (head,row) rows of the workload, each step ~%.1f s of CPU work; "
+                                   "flops counted 4*d per visible key" % (rows, per_step)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w: sy.Workload, n_gpus: int):
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+            "dtype": "bf16" if w.dtype == sy.BF16 else "fp16", "causal": w.causal,
+            "scale": "1/sqrt(d)", "q_scale": w.q_scale,
+            "l2": "inputs (%.0f MB) larger than the 129 MB L2; no flush" % (3 * w.B * w.H * w.N * w.d * 2 / 1e6),
+            "parallelism": "replicas x%d" % n_gpus, "seed": w.seed(0)}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(sy.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="bounded CPU-oracle sample (s)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = sy.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+
+    import exact_tiled_attention_fa2_gb300 as fa2
+    from exact_tiled_attention_fa2_gb300 import build as fa2_build
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    fa2_build.build() if rank == 0 else None
+    if dist is not None:
+        dist.barrier()
+    fa2.load_library()
+
+    q_bits, k_bits, v_bits = w.inputs()
+    tdt = torch.bfloat16 if w.dtype == sy.BF16 else torch.float16
+    host = [torch.from_numpy(x.view(np.int16)).view(tdt) for x in (q_bits, k_bits, v_bits)]
+    dev = torch.device("cuda", local)
+    q, k, v = (h.to(dev) for h in host)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        fa2.fa2_fwd(q, k, v, o, lse, scale=w.scale, causal=w.causal, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    code, detail = fa2.fa2_get_device_status(stream)
+    if code != fa2.FA2_OK:
+        raise RuntimeError("device status %d (0x%x) after warm-up" % (code, detail))
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for i in range(args.steps):
+                starts[i].record(stream)
+                step()
+                ends[i].record(stream)
+            t1.record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize(dev)
+    elapsed_ms = t0.elapsed_time(t1)
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    code, detail = fa2.fa2_get_device_status(stream)
+    if code != fa2.FA2_OK:
+        raise RuntimeError("device status %d (0x%x) in timed region" % (code, detail))
+    max_ms = elapsed_ms
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        max_ms = float(t.item())
+        dist.barrier()
+
+    flops = w.flops()
+    value = flops * args.steps * ws / (max_ms / 1e3) / 1e12
+    avg_launch_ms = sum(kernel_ms) / len(kernel_ms)
+    achieved = flops / (avg_launch_ms / 1e3) / 1e12
+    peak, peak_note = measured_peak()
+
+    e2e = None
+    cpu = None
+    if rank == 0:
+        # end to end through the host-buffer entry point: H2D of q, k, v and D2H of o, lse each step
+        qh, kh, vh = (h.pin_memory() for h in host)
+        oh = torch.empty(q.shape, dtype=tdt).pin_memory()
+        lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        wsb = torch.empty(fa2.fa2_fwd_host_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
+        fa2.fa2_fwd_host(qh, kh, vh, oh, lh, wsb, scale=w.scale, causal=w.causal, stream=stream)
+        te = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            fa2.fa2_fwd_host(qh, kh, vh, oh, lh, wsb, scale=w.scale, causal=w.causal, stream=stream)
+        e2e_s = time.perf_counter() - te
+        tb = w.B * w.H * w.N * w.d * 2
+        e2e = {"value": flops * args.e2e_steps / e2e_s / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": 3 * tb, "d2h_bytes_per_step": tb + w.B * w.H * w.N * 4,
+               "steps": args.e2e_steps, "ms_per_step": 1e3 * e2e_s / args.e2e_steps,
+               "api": "fa2_fwd_host (pinned host buffers)"}
+        del wsb
+        if ws == 1 and not args.no_cpu_baseline:
+            import oracle
+
+            f, s, rows = oracle_sample(w, q_bits, k_bits, v_bits, args.cpu_seconds, np.random.default_rng(7))
+            cpu = {"value": f / s / 1e12, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                   "sample": "%d random (head,row) rows of the workload in %.1f s (fp64 oracle, OpenMP); "
+                             "flops counted 4*d per visible key" % (rows, s)}
+
+    if rank == 0:
+        clk = clocks.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == sy.BF16 else "fp16",
+            "data": "synthetic", "config": workload_config(w, ws),
+            "pct_of_peak": 100.0 * value / ws / peak,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                         "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
+                         "peak_source": peak_note, "kernel": "fa2_fwd_kernel",
+                         "avg_launch_ms": avg_launch_ms,
+                         "algorithmic_flops_per_launch": flops,
+                         "algorithmic_bytes_per_launch": w.algorithmic_bytes()},
+            "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                       "samples": clk["samples"]},
+            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": args.steps,
+            "kernel_sha": kernel_source_hash(),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

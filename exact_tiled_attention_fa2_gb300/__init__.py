@@ -1,1 +1,152 @@
-"""GB300-native exact tiled attention (FlashAttention-2 forward) for sm_103a."""
+"""GB300-native exact tiled attention: the FlashAttention-2 forward pass on sm_103a.
+
+A thin ctypes binding over the C ABI in ``include/fa2.h`` (library
+``libfa2_gb300.so``, built in-tree by ``exact_tiled_attention_fa2_gb300.build``).
+Every step of the forward pass runs in the CUDA kernels; this module only
+marshals torch tensors (device memory, streams) into pointers and sizes.
+There is no CPU fallback: if the library is missing, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa2_gb300.so")
+
+FA2_FP16 = 0
+FA2_BF16 = 1
+FA2_OK = 0
+FA2_ERR_INVALID_ARG = 1
+FA2_ERR_UNSUPPORTED = 2
+FA2_ERR_MISALIGNED = 3
+FA2_ERR_CUDA = 4
+FA2_ERR_DEVICE_TIMEOUT = 5
+
+_lib = None
+
+
+class Fa2Error(RuntimeError):
+    """A nonzero fa2_status returned through the C ABI."""
+
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s failed: %s (status %d)" % (where, fa2_status_string(code), code))
+
+
+def load_library():
+    """Load libfa2_gb300.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libfa2_gb300.so is not built (run `python -m exact_tiled_attention_fa2_gb300.build` "
+                           "or __graft_entry__.build()); there is no fallback path")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, ci, cf, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa2_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, ci, vp]
+    lib.fa2_fwd.restype = ci
+    lib.fa2_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, sz, ci, ci, ci, ci, cf, ci, ci, vp]
+    lib.fa2_fwd_host.restype = ci
+    lib.fa2_fwd_host_workspace_bytes.argtypes = [ci, ci, ci, ci]
+    lib.fa2_fwd_host_workspace_bytes.restype = sz
+    lib.fa2_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.fa2_get_device_status.restype = ci
+    lib.fa2_status_string.argtypes = [ci]
+    lib.fa2_status_string.restype = ctypes.c_char_p
+    lib.fa2_version.argtypes = []
+    lib.fa2_version.restype = ci
+    _lib = lib
+    return lib
+
+
+def fa2_status_string(code: int) -> str:
+    return load_library().fa2_status_string(int(code)).decode()
+
+
+def fa2_version() -> int:
+    return int(load_library().fa2_version())
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return FA2_FP16
+    if t.dtype == torch.bfloat16:
+        return FA2_BF16
+    raise TypeError("q, k, v must be float16 or bfloat16, got %s" % t.dtype)
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(int(stream.cuda_stream))
+
+
+def fa2_fwd(q, k, v, o=None, lse=None, scale=None, causal=False, stream=None):
+    """Exact attention forward on CUDA tensors [B, H, N, d] (fp16/bf16, contiguous).
+
+    Returns (o, lse): o [B,H,N,d] of q's dtype, lse [B,H,N] float32 (natural
+    log).  ``scale`` defaults to 1/sqrt(d).  Asynchronous on ``stream``
+    (default: torch's current stream).
+    """
+    import torch
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must share one [B, H, N, d] shape")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("fa2_fwd takes CUDA tensors; use fa2_fwd_host for host buffers")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous [B, H, N, d]")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    B, H, N, d = q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / float(d) ** 0.5
+    rc = load_library().fa2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q),
+                                _stream_handle(stream, q.device))
+    if rc:
+        raise Fa2Error(rc, "fa2_fwd")
+    return o, lse
+
+
+def fa2_fwd_host_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load_library().fa2_fwd_host_workspace_bytes(B, H, N, d))
+
+
+def fa2_fwd_host(q, k, v, o, lse, workspace, scale=None, causal=False, dtype=None, stream=None):
+    """End-to-end forward on HOST buffers (torch CPU tensors, ideally pinned).
+
+    Copies q, k, v into ``workspace`` (a CUDA uint8 tensor of at least
+    fa2_fwd_host_workspace_bytes bytes), runs the kernel, copies o and lse back
+    into the given host tensors and synchronises the stream.
+    """
+    import torch
+    B, H, N, d = q.shape
+    code = _dtype_code(q) if dtype is None else int(dtype)
+    if scale is None:
+        scale = 1.0 / float(d) ** 0.5
+    for t in (q, k, v, o, lse):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("fa2_fwd_host takes contiguous host tensors")
+    rc = load_library().fa2_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                     workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                     B, H, N, d, float(scale), int(bool(causal)), code,
+                                     _stream_handle(stream, workspace.device))
+    if rc:
+        raise Fa2Error(rc, "fa2_fwd_host")
+    return o, lse
+
+
+def fa2_get_device_status(stream=None):
+    """Synchronise ``stream``; return (status, raw detail bits) and clear the device status word."""
+    import torch
+    detail = ctypes.c_uint32(0)
+    rc = load_library().fa2_get_device_status(_stream_handle(stream, torch.cuda.current_device()),
+                                              ctypes.byref(detail))
+    return rc, int(detail.value)

@@ -1,0 +1,221 @@
+// fa2_abi.cu -- the C ABI declared in include/fa2.h: argument checks, TMA
+// tensor maps, the per-device status word, kernel dispatch and the
+// host-buffer end-to-end entry point.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa2.h"
+#include "fa2_internal.h"
+
+namespace fa2 {
+
+// Written by kernels when a bounded wait gives up; one per device context.
+__device__ uint32_t g_device_status;
+
+TileGeometry tile_geometry(int d) {
+  TileGeometry g;
+  g.q_rows = 128;
+  g.kv_rows = (d == 256) ? 64 : 128;
+  return g;
+}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  bool supported = false;
+  uint32_t* status = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Per-device set-up: capability check and the status word's device address.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA2_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA2_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& s = g_devices[dev];
+  if (!s.ready) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return FA2_ERR_CUDA;
+    s.supported = (prop.major == 10 && prop.minor == 3);
+    if (s.supported) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return FA2_ERR_CUDA;
+      s.status = static_cast<uint32_t*>(addr);
+      uint32_t zero = 0;
+      if (cudaMemcpy(s.status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA2_ERR_CUDA;
+    }
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return FA2_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    s.ready = true;
+  }
+  if (!s.supported) return FA2_ERR_UNSUPPORTED;
+  *out = &s;
+  return FA2_OK;
+}
+
+// [B*H, N, d] view of a [B,H,N,d] tensor; boxes of 64 columns x `rows` rows,
+// 128-byte swizzle.  Rows past N read as zeros (and are clipped on store).
+int encode_map(CUtensorMap* m, const void* base, int bh, int n, int d, int rows, bool bf16) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)n * (cuuint64_t)d * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA2_OK : FA2_ERR_CUDA;
+}
+
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+  uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+// Checks that need no CUDA call.  Sizes in elements.
+int check_shape(int B, int H, int N, int d, float scale, int causal, int dtype) {
+  if (dtype != FA2_FP16 && dtype != FA2_BF16) return FA2_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1) return FA2_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA2_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA2_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return FA2_ERR_UNSUPPORTED;
+  if ((long long)B * (long long)H > INT_MAX) return FA2_ERR_UNSUPPORTED;
+  if ((N + 127) / 128 > 65535) return FA2_ERR_UNSUPPORTED;  // query tiles map to grid.y
+  return FA2_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+}  // namespace fa2
+
+using namespace fa2;
+
+extern "C" int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                       int d, float scale, int causal, int dtype, void* stream) {
+  int rc = check_shape(B, H, N, d, scale, causal, dtype);
+  if (rc) return rc;
+  if (!q || !k || !v || !o || !lse) return FA2_ERR_INVALID_ARG;
+  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(o) || misaligned(lse)) return FA2_ERR_MISALIGNED;
+  const size_t elems = (size_t)B * H * (size_t)N * d;
+  const size_t tbytes = elems * 2, lbytes = (size_t)B * H * (size_t)N * 4;
+  const void* ins[3] = {q, k, v};
+  for (const void* in : ins) {
+    if (ranges_overlap(o, tbytes, in, tbytes) || ranges_overlap(lse, lbytes, in, tbytes)) return FA2_ERR_INVALID_ARG;
+  }
+  if (ranges_overlap(o, tbytes, lse, lbytes)) return FA2_ERR_INVALID_ARG;
+
+  DeviceState* ds = nullptr;
+  rc = device_state(&ds);
+  if (rc) return rc;
+  const bool bf16 = dtype == FA2_BF16;
+  const TileGeometry g = tile_geometry(d);
+  LaunchArgs a;
+  std::memset(&a, 0, sizeof(a));
+  const int bh = B * H;
+  if (encode_map(&a.tm_q, q, bh, N, d, g.q_rows, bf16) || encode_map(&a.tm_k, k, bh, N, d, g.kv_rows, bf16) ||
+      encode_map(&a.tm_v, v, bh, N, d, g.kv_rows, bf16))
+    return FA2_ERR_CUDA;
+  a.p.o = o;
+  a.p.lse = lse;
+  a.p.status = ds->status;
+  a.p.n = N;
+  a.p.num_q_tiles = (N + g.q_rows - 1) / g.q_rows;
+  a.p.bh = bh;
+  a.p.scale_log2 = scale * 1.4426950408889634f;
+  a.bf16 = bf16;
+  a.causal = causal != 0;
+  a.stream = static_cast<cudaStream_t>(stream);
+  int e = 0;
+  switch (d) {
+    case 64: e = launch_fwd_d64(a); break;
+    case 128: e = launch_fwd_d128(a); break;
+    default: e = launch_fwd_d256(a); break;
+  }
+  return e == 0 ? FA2_OK : FA2_ERR_CUDA;
+}
+
+extern "C" size_t fa2_fwd_host_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+  const size_t elems = (size_t)B * H * (size_t)N * d;
+  return 4 * align256(elems * 2) + align256((size_t)B * H * (size_t)N * 4);
+}
+
+extern "C" int fa2_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host,
+                            float* lse_host, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                            float scale, int causal, int dtype, void* stream) {
+  int rc = check_shape(B, H, N, d, scale, causal, dtype);
+  if (rc) return rc;
+  if (!q_host || !k_host || !v_host || !o_host || !lse_host || !workspace) return FA2_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA2_ERR_MISALIGNED;
+  if (workspace_bytes < fa2_fwd_host_workspace_bytes(B, H, N, d)) return FA2_ERR_INVALID_ARG;
+  const size_t elems = (size_t)B * H * (size_t)N * d;
+  const size_t tb = elems * 2, lb = (size_t)B * H * (size_t)N * 4;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  void* qd = w;
+  void* kd = w + align256(tb);
+  void* vd = w + 2 * align256(tb);
+  void* od = w + 3 * align256(tb);
+  float* ld = reinterpret_cast<float*>(w + 4 * align256(tb));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(qd, q_host, tb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(kd, k_host, tb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(vd, v_host, tb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return FA2_ERR_CUDA;
+  rc = fa2_fwd(qd, kd, vd, od, ld, B, H, N, d, scale, causal, dtype, stream);
+  if (rc) return rc;
+  if (cudaMemcpyAsync(o_host, od, tb, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyAsync(lse_host, ld, lb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return FA2_ERR_CUDA;
+  return fa2_get_device_status(stream, nullptr);
+}
+
+extern "C" int fa2_get_device_status(void* stream, uint32_t* detail) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA2_ERR_CUDA;
+  DeviceState* ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc) return rc;
+  uint32_t word = 0, zero = 0;
+  if (cudaMemcpy(&word, ds->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return FA2_ERR_CUDA;
+  if (word && cudaMemcpy(ds->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return FA2_ERR_CUDA;
+  if (detail) *detail = word;
+  return word ? FA2_ERR_DEVICE_TIMEOUT : FA2_OK;
+}
+
+extern "C" const char* fa2_status_string(int status) {
+  switch (status) {
+    case FA2_OK: return "ok";
+    case FA2_ERR_INVALID_ARG: return "invalid argument (size, dtype, scale, null pointer or overlapping buffers)";
+    case FA2_ERR_UNSUPPORTED: return "unsupported (head dim not 64/128/256, size limit, or not an sm_103 device)";
+    case FA2_ERR_MISALIGNED: return "pointer not 16-byte aligned (workspace: 256-byte)";
+    case FA2_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case FA2_ERR_DEVICE_TIMEOUT: return "a kernel wait timed out; the tile was abandoned";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int fa2_version(void) { return 100; }

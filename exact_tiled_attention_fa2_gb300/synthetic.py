@@ -18,6 +18,8 @@ value is then rounded to nearest-even into fp16 or bf16.
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass
 
 import numpy as np
@@ -45,17 +47,30 @@ def splitmix64(seed: int, counters: np.ndarray) -> np.ndarray:
         return _mix(z)
 
 
+def _normals_chunk(seed: int, first: int, out: np.ndarray) -> None:
+    e = np.arange(first, first + out.size, dtype=np.uint64)
+    r1 = splitmix64(seed, e * np.uint64(2))
+    r2 = splitmix64(seed, e * np.uint64(2) + np.uint64(1))
+    u1 = ((r1 >> np.uint64(40)).astype(np.float64) + 1.0) * (1.0 / 16777216.0)   # (0, 1]
+    u2 = (r2 >> np.uint64(40)).astype(np.float64) * (1.0 / 16777216.0)           # [0, 1)
+    out[:] = (np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)).astype(np.float32)
+
+
 def normals_f32(seed: int, start: int, count: int) -> np.ndarray:
-    """float32 N(0,1) draws for elements [start, start + count) of the stream."""
+    """float32 N(0,1) draws for elements [start, start + count) of the stream.
+
+    Chunks are independent (counter-based), so they are filled by a thread
+    pool; the result does not depend on the number of threads.
+    """
     out = np.empty(count, dtype=np.float32)
-    for off in range(0, count, _CHUNK):
-        n = min(_CHUNK, count - off)
-        e = np.arange(start + off, start + off + n, dtype=np.uint64)
-        r1 = splitmix64(seed, e * np.uint64(2))
-        r2 = splitmix64(seed, e * np.uint64(2) + np.uint64(1))
-        u1 = ((r1 >> np.uint64(40)).astype(np.float64) + 1.0) * (1.0 / 16777216.0)   # (0, 1]
-        u2 = (r2 >> np.uint64(40)).astype(np.float64) * (1.0 / 16777216.0)           # [0, 1)
-        out[off:off + n] = (np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)).astype(np.float32)
+    offs = list(range(0, count, _CHUNK))
+    if len(offs) <= 1:
+        if count:
+            _normals_chunk(seed, start, out)
+        return out
+    workers = min(len(offs), os.cpu_count() or 1, 32)
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        list(ex.map(lambda off: _normals_chunk(seed, start + off, out[off:off + _CHUNK]), offs))
     return out
 
 

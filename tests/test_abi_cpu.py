@@ -1,0 +1,114 @@
+"""The C-ABI library loads without a GPU, exports every symbol include/*.h
+declares, and rejects bad arguments before making any CUDA call.  CPU only:
+no call here ever reaches a kernel launch (every call carries an invalid
+argument), so the file is also safe on a GPU machine."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import exact_tiled_attention_fa2_gb300 as fa2
+from exact_tiled_attention_fa2_gb300 import build as fa2_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa2_build.build()
+    return fa2.load_library()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(fa2_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_entry_points():
+    names = _declared_functions()
+    for required in ("fa2_fwd", "fa2_fwd_host", "fa2_fwd_host_workspace_bytes", "fa2_get_device_status",
+                     "fa2_status_string", "fa2_version"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = fa2.fa2_status_string(code)
+        assert isinstance(s, str) and s
+    assert fa2.fa2_status_string(0) == "ok"
+    assert "unknown" in fa2.fa2_status_string(99)
+    assert fa2.fa2_version() >= 100
+
+
+# Pointer values below are never dereferenced: each call fails argument checks first.
+A = 0x10000  # 16-byte aligned stand-ins
+GOOD = dict(B=1, H=2, N=64, d=64, scale=0.125, causal=0, dtype=0)
+
+
+def _call(lib, q=A, k=2 * A, v=3 * A, o=4 * A, lse=5 * A, **kw):
+    a = dict(GOOD)
+    a.update(kw)
+    return lib.fa2_fwd(q, k, v, o, lse, a["B"], a["H"], a["N"], a["d"], a["scale"], a["causal"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=2), fa2.FA2_ERR_INVALID_ARG),
+    (dict(dtype=-1), fa2.FA2_ERR_INVALID_ARG),
+    (dict(B=0), fa2.FA2_ERR_INVALID_ARG),
+    (dict(H=-3), fa2.FA2_ERR_INVALID_ARG),
+    (dict(N=0), fa2.FA2_ERR_INVALID_ARG),
+    (dict(causal=2), fa2.FA2_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa2.FA2_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa2.FA2_ERR_INVALID_ARG),
+    (dict(scale=0.0), fa2.FA2_ERR_INVALID_ARG),
+    (dict(scale=-0.125), fa2.FA2_ERR_INVALID_ARG),
+    (dict(d=32), fa2.FA2_ERR_UNSUPPORTED),
+    (dict(d=96), fa2.FA2_ERR_UNSUPPORTED),
+    (dict(d=512), fa2.FA2_ERR_UNSUPPORTED),
+    (dict(N=65535 * 128 + 1), fa2.FA2_ERR_UNSUPPORTED),
+])
+def test_bad_sizes_rejected(lib, kw, code):
+    assert _call(lib, **kw) == code
+
+
+@pytest.mark.parametrize("which", ["q", "k", "v", "o", "lse"])
+def test_null_pointers_rejected(lib, which):
+    assert _call(lib, **{which: 0}) == fa2.FA2_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("which", ["q", "k", "v", "o", "lse"])
+def test_misaligned_pointers_rejected(lib, which):
+    base = {"q": A, "k": 2 * A, "v": 3 * A, "o": 4 * A, "lse": 5 * A}[which]
+    assert _call(lib, **{which: base + 8}) == fa2.FA2_ERR_MISALIGNED
+
+
+def test_overlapping_outputs_rejected(lib):
+    # o overlapping k, lse overlapping q, o overlapping lse
+    assert _call(lib, o=2 * A + 1024) == fa2.FA2_ERR_INVALID_ARG
+    assert _call(lib, lse=A + 4096) == fa2.FA2_ERR_INVALID_ARG
+    assert _call(lib, lse=4 * A + 16) == fa2.FA2_ERR_INVALID_ARG
+
+
+def test_host_entry_point_checks(lib):
+    ws = fa2.fa2_fwd_host_workspace_bytes(1, 2, 64, 64)
+    assert ws == 4 * 16384 + 512
+    assert fa2.fa2_fwd_host_workspace_bytes(0, 2, 64, 64) == 0
+    f = lib.fa2_fwd_host
+    # workspace too small, misaligned workspace, null host pointer, bad dtype
+    assert f(A, A, A, A, A, 6 * A, ws - 1, 1, 2, 64, 64, 0.125, 0, 0, None) == fa2.FA2_ERR_INVALID_ARG
+    assert f(A, A, A, A, A, 6 * A + 16, ws, 1, 2, 64, 64, 0.125, 0, 0, None) == fa2.FA2_ERR_MISALIGNED
+    assert f(0, A, A, A, A, 6 * A, ws, 1, 2, 64, 64, 0.125, 0, 0, None) == fa2.FA2_ERR_INVALID_ARG
+    assert f(A, A, A, A, A, 6 * A, ws, 1, 2, 64, 64, 0.125, 0, 5, None) == fa2.FA2_ERR_INVALID_ARG
