@@ -22,6 +22,8 @@ FA2_ERR_UNSUPPORTED = 2
 FA2_ERR_MISALIGNED = 3
 FA2_ERR_CUDA = 4
 FA2_ERR_DEVICE_TIMEOUT = 5
+FA2_ERR_SCRATCH_LIMIT = 6
+FA2_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _lib = None
 
@@ -50,6 +52,8 @@ def load_library():
     lib.fa2_fwd_host.restype = ci
     lib.fa2_fwd_host_workspace_bytes.argtypes = [ci, ci, ci, ci]
     lib.fa2_fwd_host_workspace_bytes.restype = sz
+    lib.fa2_fwd_host_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, ci, vp]
+    lib.fa2_fwd_host_noalloc.restype = ci
     lib.fa2_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.fa2_get_device_status.restype = ci
     lib.fa2_status_string.argtypes = [ci]
@@ -140,6 +144,32 @@ def fa2_fwd_host(q, k, v, o, lse, workspace, scale=None, causal=False, dtype=Non
                                      _stream_handle(stream, workspace.device))
     if rc:
         raise Fa2Error(rc, "fa2_fwd_host")
+    return o, lse
+
+
+def fa2_fwd_host_noalloc(q, k, v, o, lse, scale=None, causal=False, dtype=None, stream=None):
+    """fa2_fwd_host without a caller-provided workspace, for callers that cannot allocate device memory.
+
+    The device copies live in the library's static device array of
+    FA2_NOALLOC_SCRATCH_BYTES bytes (held by every GPU that loads the library),
+    so this call allocates nothing on the device.  Problems whose
+    fa2_fwd_host_workspace_bytes exceed that size raise Fa2Error with
+    FA2_ERR_SCRATCH_LIMIT.  Calls share the array: calls that overlap on the GPU
+    race.  The first call on a device looks up the array's address there.
+    """
+    import torch
+    B, H, N, d = q.shape
+    code = _dtype_code(q) if dtype is None else int(dtype)
+    if scale is None:
+        scale = 1.0 / float(d) ** 0.5
+    for t in (q, k, v, o, lse):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("fa2_fwd_host_noalloc takes contiguous host tensors")
+    rc = load_library().fa2_fwd_host_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                             lse.data_ptr(), B, H, N, d, float(scale), int(bool(causal)), code,
+                                             _stream_handle(stream, torch.cuda.current_device()))
+    if rc:
+        raise Fa2Error(rc, "fa2_fwd_host_noalloc")
     return o, lse
 
 

@@ -193,6 +193,52 @@ extern "C" int fa2_fwd_host(const void* q_host, const void* k_host, const void* 
   return fa2_get_device_status(stream, nullptr);
 }
 
+namespace fa2 {
+
+// Device staging area of fa2_fwd_host_noalloc: a fixed-size array in the
+// module's global memory, so that entry point never allocates.  Host code
+// must not use the symbol as an address; it looks up the device address once
+// per device.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[FA2_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_address[kMaxDevices];
+
+// Device address of g_noalloc_scratch on the current device (looked up on
+// first use, with that device current).
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA2_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA2_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_address[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return FA2_ERR_CUDA;
+    g_noalloc_address[dev] = p;
+  }
+  *out = g_noalloc_address[dev];
+  return FA2_OK;
+}
+
+}  // namespace
+}  // namespace fa2
+
+extern "C" int fa2_fwd_host_noalloc(const void* q_host, const void* k_host, const void* v_host, void* o_host,
+                                    float* lse_host, int B, int H, int N, int d, float scale, int causal,
+                                    int dtype, void* stream) {
+  int rc = check_shape(B, H, N, d, scale, causal, dtype);
+  if (rc) return rc;
+  if (!q_host || !k_host || !v_host || !o_host || !lse_host) return FA2_ERR_INVALID_ARG;
+  if (fa2_fwd_host_workspace_bytes(B, H, N, d) > FA2_NOALLOC_SCRATCH_BYTES) return FA2_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  rc = noalloc_scratch(&scratch);
+  if (rc) return rc;
+  return fa2_fwd_host(q_host, k_host, v_host, o_host, lse_host, scratch, FA2_NOALLOC_SCRATCH_BYTES, B, H, N, d,
+                      scale, causal, dtype, stream);
+}
+
 extern "C" int fa2_get_device_status(void* stream, uint32_t* detail) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA2_ERR_CUDA;
   DeviceState* ds = nullptr;
@@ -214,6 +260,7 @@ extern "C" const char* fa2_status_string(int status) {
     case FA2_ERR_MISALIGNED: return "pointer not 16-byte aligned (workspace: 256-byte)";
     case FA2_ERR_CUDA: return "CUDA runtime or driver call failed";
     case FA2_ERR_DEVICE_TIMEOUT: return "a kernel wait timed out; the tile was abandoned";
+    case FA2_ERR_SCRATCH_LIMIT: return "problem exceeds the static device scratch of fa2_fwd_host_noalloc";
     default: return "unknown status";
   }
 }

@@ -44,7 +44,8 @@ typedef enum {
   FA2_ERR_UNSUPPORTED = 2,    /* head dim not in {64, 128, 256}, or no sm_103 device */
   FA2_ERR_MISALIGNED = 3,     /* a pointer is not 16-byte aligned */
   FA2_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed */
-  FA2_ERR_DEVICE_TIMEOUT = 5  /* a kernel wait ran out of time (fa2_get_device_status) */
+  FA2_ERR_DEVICE_TIMEOUT = 5, /* a kernel wait ran out of time (fa2_get_device_status) */
+  FA2_ERR_SCRATCH_LIMIT = 6   /* problem too large for fa2_fwd_host_noalloc's static scratch */
 } fa2_status;
 
 /*
@@ -86,6 +87,39 @@ int fa2_fwd_host(const void* q_host, const void* k_host, const void* v_host, voi
 
 /* Device workspace fa2_fwd_host needs: q, k, v, o and lse, each 256-byte aligned. */
 size_t fa2_fwd_host_workspace_bytes(int B, int H, int N, int d);
+
+/* Bytes of the library's static device scratch used by fa2_fwd_host_noalloc. */
+#define FA2_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * fa2_fwd_host_noalloc -- fa2_fwd_host for callers that cannot allocate
+ * device memory.  The pages have no counterpart: it exists for callers that
+ * hold only host buffers and are not allowed to call cudaMalloc -- e.g. a
+ * process whose device memory is wholly reserved by another allocator, so a
+ * raw cudaMalloc would fail, or a latency-bound loop that must not call an
+ * allocator that may synchronise the device.
+ *
+ * Same arguments and results as fa2_fwd_host, without the workspace: the
+ * device staging copies of q, k, v, o and lse live in one static device
+ * array of FA2_NOALLOC_SCRATCH_BYTES bytes that the library defines, which
+ * every GPU that loads the library holds until the process exits.  The call
+ * allocates nothing (no cudaMalloc or cudaFree, no allocating library call).
+ *
+ *   Limit: fa2_fwd_host_workspace_bytes(B, H, N, d) must not exceed
+ *   FA2_NOALLOC_SCRATCH_BYTES; larger problems return FA2_ERR_SCRATCH_LIMIT
+ *   before any CUDA call.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (with it current); make that first call before any stream capture.
+ * All calls on a device share the one array: calls whose work overlaps on
+ * the GPU (other streams, other host threads) race and must be serialised by
+ * the caller.  Nothing in the array needs to start at zero -- every byte a
+ * call reads was written earlier in that same call.  The call synchronises
+ * `stream` before returning.
+ */
+int fa2_fwd_host_noalloc(const void* q_host, const void* k_host, const void* v_host, void* o_host,
+                         float* lse_host, int B, int H, int N, int d, float scale, int causal, int dtype,
+                         void* stream);
 
 /*
  * fa2_get_device_status -- synchronises `stream`, then returns and clears the

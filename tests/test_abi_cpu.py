@@ -45,7 +45,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(6):
+    for code in range(7):
         s = fa2.fa2_status_string(code)
         assert isinstance(s, str) and s
     assert fa2.fa2_status_string(0) == "ok"
