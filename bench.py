@@ -210,10 +210,15 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="bounded CPU-oracle sample (s)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="override H (a smaller case of the same kernel, e.g. for an ncu capture)")
+    ap.add_argument("--kernel-only", action="store_true", help="skip the end-to-end and CPU-baseline legs")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = sy.WORKLOADS[args.workload]
+    if args.heads > 0:
+        w = sy.Workload(w.index, w.B, args.heads, w.N, w.d, w.dtype, w.causal, w.q_scale)
     if args.impl == "reference":
         return run_reference(args, w)
 
@@ -290,7 +295,7 @@ def main():
 
     e2e = None
     cpu = None
-    if rank == 0:
+    if rank == 0 and not args.kernel_only:
         # end to end through the host-buffer entry point: H2D of q, k, v and D2H of o, lse each step
         qh, kh, vh = (h.pin_memory() for h in host)
         oh = torch.empty(q.shape, dtype=tdt).pin_memory()
