@@ -1,0 +1,448 @@
+// fa2_fwd_pingpong.cuh -- forward kernel for head dims 64 and 128: two query
+// tiles per CTA whose softmax work alternates with the other tile's MMAs.
+//
+// A CTA owns 256 consecutive query rows of one (batch, head) as two 128-row
+// tiles A and B that share every streamed K_j / V_j tile (so K/V are read
+// from L2 once per 256 rows).  Tensor memory holds S_A, S_B (fp32, 128
+// columns each; P overwrites them as packed 16-bit pairs) and O~_A, O~_B.
+// The MMA-issuing thread runs, per key/value tile j,
+//
+//     O~_A += P_A(j) V_j,   S_A(j+1) = Q_A K_{j+1}^T,
+//     O~_B += P_B(j) V_j,   S_B(j+1) = Q_B K_{j+1}^T
+//
+// so while softmax warpgroup A turns S_A(j+1) into P_A(j+1), the tensor pipe
+// works on tile B, and the other way round.  tcgen05 MMAs issued by one
+// thread execute in order, which is what lets S_t(j+1) be issued into the
+// columns P_t(j) is read from right after O~_t += P_t(j) V_j.
+//
+// The running maximum is only raised when a tile's maximum exceeds it by
+// more than kRescaleLog2 (2^8): otherwise P = 2^(s - m) may reach 2^8, which
+// 16-bit P and fp32 l and O~ hold exactly as well, and O~ need not be
+// rescaled.  The result is the same exact softmax: every term and l use the
+// same m, and LSE = (m + log2 l) ln 2.  (Deferred normalisation taken one
+// step further than FlashAttention V2 in depth, section 3.2.)
+//
+// Warp roles (384 threads = 3 warpgroups): warps 0-3 softmax + epilogue of
+// tile A, warps 4-7 of tile B (one thread per row = TMEM lane), warp 8 TMEM
+// owner and MMA issuer, warp 9 TMA producer, warps 10-11 idle.  The third
+// warpgroup gives registers to the two softmax warpgroups (setmaxnreg):
+// 2 x 128 x 208 + 128 x 80 <= 384 x 168 registers at launch.
+#pragma once
+
+#include "fa2_fwd_kernel.cuh"
+
+namespace fa2 {
+
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int D_>
+struct PingPongConfig {
+  static constexpr int D = D_;
+  static constexpr int BR = 128;   // rows per query tile (MMA M, TMEM lanes)
+  static constexpr int BC = 128;   // keys per streamed tile
+  static constexpr int NQ = 2;     // query tiles per CTA
+  static constexpr int STAGES = (D == 64) ? 3 : 2;
+  static constexpr int THREADS = 384;
+  static constexpr int MMA_WARP = 8;
+  static constexpr int TMA_WARP = 9;
+  static constexpr uint32_t REGS_AT_LAUNCH = 168;   // 65536 / 384, rounded down to a multiple of 8
+  static constexpr uint32_t REGS_SOFTMAX = 208;
+  static constexpr uint32_t REGS_OTHER = 80;
+  static_assert(2 * 128 * REGS_SOFTMAX + 128 * REGS_OTHER <= THREADS * REGS_AT_LAUNCH, "register split");
+  static constexpr uint32_t Q_BYTES = BR * D * 2;
+  static constexpr uint32_t KV_BYTES = BC * D * 2;
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = OFF_Q + NQ * Q_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;
+  static constexpr uint32_t NUM_BARS = 32;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
+  static constexpr uint32_t TMEM_S = 0;     // + 128 * tile
+  static constexpr uint32_t TMEM_O = 256;   // + D * tile
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(D == 64 || D == 128, "ping-pong kernel: head dim 64 or 128");
+  static_assert(TMEM_O + NQ * D <= TMEM_COLS, "tensor memory");
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+};
+
+enum : int {
+  PB_Q = 0,         // + tile
+  PB_KFULL = 2,     // + stage (<= 4 stages)
+  PB_VFULL = 6,     // + stage
+  PB_KVEMPTY = 10,  // + stage
+  PB_S = 14,        // + tile
+  PB_P = 16,        // + tile
+  PB_O = 18,        // + tile
+  PB_EXIT = 20,
+};
+
+struct PairCtx {
+  uint32_t bar0, sQ, sK, sV, tmem;
+  volatile int* abort_flag;
+  uint32_t* status;
+  int bh, n;
+  int q0[2];    // first query row of each tile
+  int nkv[2];   // key/value tiles each tile visits (0: tile lies past N)
+  int nkv_max;
+  __device__ __forceinline__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
+};
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+template <class C>
+__device__ __forceinline__ void pp_producer(const PairCtx& t, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                                            const CUtensorMap* tm_v) {
+  for (int q = 0; q < C::NQ; ++q) {
+    if (t.nkv[q] == 0) continue;
+    mbar_arrive_expect_tx(t.bar(PB_Q + q), C::Q_BYTES);
+    for (int kb = 0; kb < C::D / 64; ++kb)
+      tma_load_3d(t.sQ + q * C::Q_BYTES + kb * (C::BR * 128), tm_q, kb * 64, t.q0[q], t.bh, t.bar(PB_Q + q));
+  }
+  int last_use[C::STAGES];
+  for (int s = 0; s < C::STAGES; ++s) last_use[s] = -1;
+  for (int j = 0; j < t.nkv_max; ++j) {
+    const int s = j % C::STAGES;
+    const int u = j / C::STAGES;
+    if (u > 0 && !wait_or_abort(t.bar(PB_KVEMPTY + s), (u - 1) & 1, t.abort_flag, t.status, kSiteProducerEmpty))
+      break;
+    mbar_arrive_expect_tx(t.bar(PB_KFULL + s), C::KV_BYTES);
+    for (int kb = 0; kb < C::D / 64; ++kb)
+      tma_load_3d(t.sK + s * C::KV_BYTES + kb * (C::BC * 128), tm_k, kb * 64, j * C::BC, t.bh,
+                  t.bar(PB_KFULL + s));
+    mbar_arrive_expect_tx(t.bar(PB_VFULL + s), C::KV_BYTES);
+    for (int kb = 0; kb < C::D / 64; ++kb)
+      tma_load_3d(t.sV + s * C::KV_BYTES + kb * (C::BC * 128), tm_v, kb * 64, j * C::BC, t.bh,
+                  t.bar(PB_VFULL + s));
+    last_use[s] = u;
+  }
+  for (int q = 0; q < C::NQ; ++q)
+    if (t.nkv[q] > 0) wait_drain(t.bar(PB_Q + q), 0, t.status);
+  for (int s = 0; s < C::STAGES; ++s) {
+    if (last_use[s] >= 0) {
+      wait_drain(t.bar(PB_KFULL + s), last_use[s] & 1, t.status);
+      wait_drain(t.bar(PB_VFULL + s), last_use[s] & 1, t.status);
+    }
+  }
+}
+
+template <class C, bool BF16, bool CAUSAL>
+__device__ __forceinline__ void pp_mma(const PairCtx& t) {
+  constexpr uint32_t idesc_qk = make_idesc_f16(C::BR, C::BC, BF16, false, false);
+  constexpr uint32_t idesc_pv = make_idesc_f16(C::BR, C::D, BF16, false, true);
+  bool ok = true;
+  auto issue_s = [&](int q, int j) {
+    const uint32_t k_base = t.sK + (j % C::STAGES) * C::KV_BYTES;
+    const uint32_t q_base = t.sQ + q * C::Q_BYTES;
+    const uint32_t tS = t.tmem + C::TMEM_S + 128 * q;
+#pragma unroll
+    for (int k = 0; k < C::D / 16; ++k) {
+      const uint64_t a = make_sdesc_sw128(q_base + (k >> 2) * (C::BR * 128) + (k & 3) * 32, 16, 1024);
+      const uint64_t b = make_sdesc_sw128(k_base + (k >> 2) * (C::BC * 128) + (k & 3) * 32, 16, 1024);
+      umma_ss(tS, a, b, idesc_qk, k > 0 ? 1u : 0u);
+    }
+    umma_commit(t.bar(PB_S + q));
+  };
+  auto issue_pv = [&](int q, int j) {
+    const uint32_t v_base = t.sV + (j % C::STAGES) * C::KV_BYTES;
+    const uint32_t tS = t.tmem + C::TMEM_S + 128 * q;
+    const uint32_t tO = t.tmem + C::TMEM_O + C::D * q;
+    const bool split = split_tile<C, BF16, CAUSAL>(j, t.q0[q], t.n);
+#pragma unroll
+    for (int k = 0; k < C::BC / 16; ++k) {
+      const uint64_t b = make_sdesc_sw128(v_base + k * (16 * 128), C::BC * 128, 1024);
+      umma_ts(tO, tS + k * 8, b, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+      if (split) umma_ts(tO, tS + C::BC / 2 + k * 8, b, idesc_pv, 1u);
+    }
+    umma_commit(t.bar(PB_O + q));
+  };
+  auto wait_k = [&](int j) {
+    return wait_or_abort(t.bar(PB_KFULL + j % C::STAGES), (uint32_t)(j / C::STAGES) & 1, t.abort_flag, t.status,
+                         kSiteMmaK);
+  };
+#pragma unroll
+  for (int q = 0; q < C::NQ; ++q)
+    if (ok && t.nkv[q] > 0) ok = wait_or_abort(t.bar(PB_Q + q), 0, t.abort_flag, t.status, kSiteMmaQ);
+  if (ok) ok = wait_k(0);
+  if (ok) {
+    tc_fence_after();
+#pragma unroll
+    for (int q = 0; q < C::NQ; ++q)
+      if (t.nkv[q] > 0) issue_s(q, 0);
+    for (int j = 0; j < t.nkv_max && ok; ++j) {
+      const int s = j % C::STAGES;
+#pragma unroll
+      for (int q = 0; q < C::NQ; ++q) {
+        if (!ok || j >= t.nkv[q]) continue;
+        if (!wait_or_abort(t.bar(PB_P + q), (uint32_t)j & 1, t.abort_flag, t.status, kSiteMmaP) ||
+            !wait_or_abort(t.bar(PB_VFULL + s), (uint32_t)(j / C::STAGES) & 1, t.abort_flag, t.status,
+                           kSiteMmaV)) {
+          ok = false;
+          continue;
+        }
+        tc_fence_after();
+        issue_pv(q, j);
+        if (j + 1 < t.nkv[q]) {
+          if (!wait_k(j + 1)) {
+            ok = false;
+            continue;
+          }
+          tc_fence_after();
+          issue_s(q, j + 1);
+        }
+      }
+      if (ok) umma_commit(t.bar(PB_KVEMPTY + s));
+    }
+  }
+  umma_commit(t.bar(PB_EXIT));
+  wait_drain(t.bar(PB_EXIT), 0, t.status);
+}
+
+template <class C, bool BF16, bool CAUSAL>
+__device__ __forceinline__ void pp_softmax(const PairCtx& t, const KernelParams& p, int q, int warp, int lane) {
+  const int nkv = q ? t.nkv[1] : t.nkv[0];   // selects, not a runtime-indexed local array
+  const int q0 = q ? t.q0[1] : t.q0[0];
+  if (nkv == 0) return;
+  const int quad = warp & 3;
+  const int r = quad * 32 + lane;
+  const int row = q0 + r;
+  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+  const uint32_t tS = t.tmem + lane_off + C::TMEM_S + 128 * q;
+  const uint32_t tO = t.tmem + lane_off + C::TMEM_O + C::D * q;
+  const float sl2 = p.scale_log2;
+  float m_run = -INFINITY;  // the maximum the exponentials are taken against (exp2 domain)
+  float l_run = 0.f;
+  bool ok = true;
+  for (int j = 0; j < nkv; ++j) {
+    ok = wait_or_abort(t.bar(PB_S + q), (uint32_t)j & 1, t.abort_flag, t.status, kSiteSoftmaxS);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    tc_fence_after();
+    uint32_t sr[C::BC];
+#pragma unroll
+    for (int c = 0; c < C::BC; c += 32) tmem_ld_32x32b_x32(tS + c, sr + c);
+#pragma unroll
+    for (int c = 0; c < C::BC; c += 32) tmem_ld_wait_x32(sr + c);
+    const int k0 = j * C::BC;
+    const bool masked = (k0 + C::BC > t.n) || (CAUSAL && (k0 + C::BC - 1 > q0));
+    if (masked) {
+#pragma unroll
+      for (int c = 0; c < C::BC; ++c) {
+        const int key = k0 + c;
+        if (key >= t.n || (CAUSAL && key > row)) sr[c] = __float_as_uint(-INFINITY);
+      }
+    }
+    float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < C::BC; c += 8) {
+      mx0 = fmax3(mx0, __uint_as_float(sr[c + 0]), __uint_as_float(sr[c + 1]));
+      mx1 = fmax3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+      mx2 = fmax3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+      mx3 = fmax3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+    }
+    const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+    const bool raise = m_tile > m_run + kRescaleLog2;   // false when both are -inf
+    const float m_new = raise ? m_tile : m_run;
+    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+    const float alpha = raise ? ex2_approx(m_run - m_use) : 1.f;
+    const bool split = split_tile<C, BF16, CAUSAL>(j, q0, t.n);
+    const float2 scale2 = make_float2(sl2, sl2);
+    const float2 neg_m2 = make_float2(-m_use, -m_use);
+    float2 sum0 = make_float2(0.f, 0.f), sum1 = make_float2(0.f, 0.f);
+    // P in 32-column chunks: exponentiate, pack to 16-bit pairs, store to the
+    // chunk's TMEM columns (S is already in registers, so overwriting is safe)
+#pragma unroll
+    for (int ch = 0; ch < C::BC / 32; ++ch) {
+      uint32_t ph[16];
+      uint32_t pl[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int col = ch * 32 + 2 * c;
+        float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), scale2, neg_m2);
+        x.x = ex2_approx(x.x);
+        x.y = ex2_approx(x.y);
+        if (c & 1)
+          sum1 = __fadd2_rn(sum1, x);
+        else
+          sum0 = __fadd2_rn(sum0, x);
+        ph[c] = pack2<BF16>(x.x, x.y);
+        if (split) {
+          const float2 h = unpack2<BF16>(ph[c]);
+          pl[c] = pack2<BF16>(x.x - h.x, x.y - h.y);
+        }
+      }
+      tmem_st_32x32b_x16(tS + ch * 16, ph);
+      if (split) tmem_st_32x32b_x16(tS + C::BC / 2 + ch * 16, pl);
+    }
+    const float2 sum2 = __fadd2_rn(sum0, sum1);
+    l_run = l_run * alpha + (sum2.x + sum2.y);
+    if (j > 0) {
+      // O~ holds every product up to PV(j-1) once this phase has completed
+      bool ok2 = wait_or_abort(t.bar(PB_O + q), (uint32_t)(j - 1) & 1, t.abort_flag, t.status, kSiteSoftmaxO);
+      ok2 = __all_sync(0xffffffffu, ok2);
+      if (!ok2) {
+        ok = false;
+        break;
+      }
+      if (__any_sync(0xffffffffu, raise)) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < C::D; c += 32) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(tO + c, o);
+          tmem_ld_wait_x32(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st_32x32b_x32(tO + c, o);
+        }
+      }
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(t.bar(PB_P + q));
+    m_run = m_new;
+  }
+  if (ok) {
+    ok = wait_or_abort(t.bar(PB_O + q), (uint32_t)(nkv - 1) & 1, t.abort_flag, t.status, kSiteEpilogueO);
+    ok = __all_sync(0xffffffffu, ok);
+  }
+  if (!ok) return;
+  tc_fence_after();
+  const float inv_l = 1.f / l_run;
+  uint8_t* o_row = reinterpret_cast<uint8_t*>(p.o) + ((size_t)t.bh * (size_t)t.n + (size_t)row) * (C::D * 2);
+#pragma unroll 1
+  for (int c = 0; c < C::D; c += 32) {
+    uint32_t o[32];
+    tmem_ld_32x32b_x32(tO + c, o);
+    tmem_ld_wait_x32(o);
+    uint32_t packed[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      packed[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+    if (row < t.n) {
+      uint4* dst = reinterpret_cast<uint4*>(o_row + c * 2);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+    }
+  }
+  if (row < t.n) p.lse[(size_t)t.bh * (size_t)t.n + (size_t)row] = (m_run + log2f(l_run)) * 0.6931471805599453f;
+}
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(384, 1)
+    fa2_fwd_pingpong_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v, const KernelParams p) {
+  using C = PingPongConfig<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  const int warp = (int)(threadIdx.x >> 5);
+  const int lane = (int)(threadIdx.x & 31);
+
+  PairCtx t;
+  t.bar0 = sbase + C::OFF_BAR;
+  t.sQ = sbase + C::OFF_Q;
+  t.sK = sbase + C::OFF_K;
+  t.sV = sbase + C::OFF_V;
+  t.abort_flag = abort_flag;
+  t.status = p.status;
+  t.n = p.n;
+  t.bh = (int)blockIdx.x;
+  // causal: the pairs with the most key tiles (highest rows) start first
+  const int pair = CAUSAL ? (int)(gridDim.y - 1 - blockIdx.y) : (int)blockIdx.y;
+  t.nkv_max = 0;
+  for (int q = 0; q < C::NQ; ++q) {
+    t.q0[q] = pair * (C::NQ * C::BR) + q * C::BR;
+    if (t.q0[q] >= t.n) {
+      t.nkv[q] = 0;
+    } else {
+      const int kv_end = CAUSAL ? min(t.n, t.q0[q] + C::BR) : t.n;
+      t.nkv[q] = (kv_end + C::BC - 1) / C::BC;
+    }
+    t.nkv_max = max(t.nkv_max, t.nkv[q]);
+  }
+
+  if (threadIdx.x == 0) {
+    for (int q = 0; q < C::NQ; ++q) {
+      mbar_init(t.bar(PB_Q + q), 1);
+      mbar_init(t.bar(PB_S + q), 1);
+      mbar_init(t.bar(PB_P + q), 4);  // one arrival per softmax warp of the tile
+      mbar_init(t.bar(PB_O + q), 1);
+    }
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(t.bar(PB_KFULL + s), 1);
+      mbar_init(t.bar(PB_VFULL + s), 1);
+      mbar_init(t.bar(PB_KVEMPTY + s), 1);
+    }
+    mbar_init(t.bar(PB_EXIT), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::TMA_WARP && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  t.tmem = *tmem_slot;
+
+  if (warp >= 8) {
+    regs_decrease<C::REGS_OTHER>();
+    if (warp == C::TMA_WARP) {
+      if (lane == 0) pp_producer<C>(t, &tm_q, &tm_k, &tm_v);
+    } else if (warp == C::MMA_WARP) {
+      if (lane == 0) pp_mma<C, BF16, CAUSAL>(t);
+      __syncwarp();
+    }
+  } else {
+    regs_increase<C::REGS_SOFTMAX>();
+    pp_softmax<C, BF16, CAUSAL>(t, p, warp >> 2, warp, lane);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(t.tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D, bool BF16, bool CAUSAL>
+int launch_fwd_pingpong(const LaunchArgs& a) {
+  using C = PingPongConfig<D>;
+  auto kern = fa2_fwd_pingpong_kernel<D, BF16, CAUSAL>;
+  // The softmax warpgroups' setmaxnreg.inc only completes if the block was
+  // launched with the registers the split assumes: refuse to launch otherwise.
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+  if (e != cudaSuccess) return (int)e;
+  if ((uint32_t)attr.numRegs != C::REGS_AT_LAUNCH) return (int)cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
+  if (e != cudaSuccess) return (int)e;
+  const int pairs = (a.p.n + C::NQ * C::BR - 1) / (C::NQ * C::BR);
+  dim3 grid((unsigned)a.p.bh, (unsigned)pairs);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.p);
+  return (int)cudaGetLastError();
+}
+
+template <int D>
+int launch_fwd_pingpong_dispatch(const LaunchArgs& a) {
+  if (a.bf16) return a.causal ? launch_fwd_pingpong<D, true, true>(a) : launch_fwd_pingpong<D, true, false>(a);
+  return a.causal ? launch_fwd_pingpong<D, false, true>(a) : launch_fwd_pingpong<D, false, false>(a);
+}
+
+}  // namespace fa2
