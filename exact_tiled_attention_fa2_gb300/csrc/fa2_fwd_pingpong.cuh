@@ -26,7 +26,7 @@
 // tile A, warps 4-7 of tile B (one thread per row = TMEM lane), warp 8 TMEM
 // owner and MMA issuer, warp 9 TMA producer, warps 10-11 idle.  The third
 // warpgroup gives registers to the two softmax warpgroups (setmaxnreg):
-// 2 x 128 x 208 + 128 x 80 <= 384 x 168 registers at launch.
+// 2 x 128 x 200 + 128 x 104 = 384 x 168 registers at launch.
 #pragma once
 
 #include "fa2_fwd_kernel.cuh"
@@ -46,8 +46,8 @@ struct PingPongConfig {
   static constexpr int MMA_WARP = 8;
   static constexpr int TMA_WARP = 9;
   static constexpr uint32_t REGS_AT_LAUNCH = 168;   // 65536 / 384, rounded down to a multiple of 8
-  static constexpr uint32_t REGS_SOFTMAX = 208;
-  static constexpr uint32_t REGS_OTHER = 80;
+  static constexpr uint32_t REGS_SOFTMAX = 200;
+  static constexpr uint32_t REGS_OTHER = 104;
   static_assert(2 * 128 * REGS_SOFTMAX + 128 * REGS_OTHER <= THREADS * REGS_AT_LAUNCH, "register split");
   static constexpr uint32_t Q_BYTES = BR * D * 2;
   static constexpr uint32_t KV_BYTES = BC * D * 2;
@@ -130,44 +130,53 @@ __device__ __forceinline__ void pp_producer(const PairCtx& t, const CUtensorMap*
   }
 }
 
+// Descriptors are built once and advanced by adding (byte offset >> 4) to the
+// start-address field: every tile sits below 256 KB of shared memory, so the
+// 14-bit field never carries into the next one.
+template <class C>
+__device__ __forceinline__ constexpr uint64_t kmajor_step(int k, int rows) {
+  return (uint64_t)(((k >> 2) * (rows * 128) + (k & 3) * 32) >> 4);
+}
+
 template <class C, bool BF16, bool CAUSAL>
 __device__ __forceinline__ void pp_mma(const PairCtx& t) {
   constexpr uint32_t idesc_qk = make_idesc_f16(C::BR, C::BC, BF16, false, false);
   constexpr uint32_t idesc_pv = make_idesc_f16(C::BR, C::D, BF16, false, true);
+  const uint64_t dq0 = make_sdesc_sw128(t.sQ, 16, 1024);
+  const uint64_t dk0 = make_sdesc_sw128(t.sK, 16, 1024);
+  const uint64_t dv0 = make_sdesc_sw128(t.sV, C::BC * 128, 1024);
   bool ok = true;
   auto issue_s = [&](int q, int j) {
-    const uint32_t k_base = t.sK + (j % C::STAGES) * C::KV_BYTES;
-    const uint32_t q_base = t.sQ + q * C::Q_BYTES;
+    const uint64_t a0 = dq0 + (uint64_t)((q * C::Q_BYTES) >> 4);
+    const uint64_t b0 = dk0 + (uint64_t)(((j % C::STAGES) * C::KV_BYTES) >> 4);
     const uint32_t tS = t.tmem + C::TMEM_S + 128 * q;
 #pragma unroll
-    for (int k = 0; k < C::D / 16; ++k) {
-      const uint64_t a = make_sdesc_sw128(q_base + (k >> 2) * (C::BR * 128) + (k & 3) * 32, 16, 1024);
-      const uint64_t b = make_sdesc_sw128(k_base + (k >> 2) * (C::BC * 128) + (k & 3) * 32, 16, 1024);
-      umma_ss(tS, a, b, idesc_qk, k > 0 ? 1u : 0u);
-    }
+    for (int k = 0; k < C::D / 16; ++k)
+      umma_ss(tS, a0 + kmajor_step<C>(k, C::BR), b0 + kmajor_step<C>(k, C::BC), idesc_qk, k > 0 ? 1u : 0u);
     umma_commit(t.bar(PB_S + q));
   };
   auto issue_pv = [&](int q, int j) {
-    const uint32_t v_base = t.sV + (j % C::STAGES) * C::KV_BYTES;
+    const uint64_t b0 = dv0 + (uint64_t)(((j % C::STAGES) * C::KV_BYTES) >> 4);
     const uint32_t tS = t.tmem + C::TMEM_S + 128 * q;
     const uint32_t tO = t.tmem + C::TMEM_O + C::D * q;
-    const bool split = split_tile<C, BF16, CAUSAL>(j, t.q0[q], t.n);
+    if (split_tile<C, BF16, CAUSAL>(j, t.q0[q], t.n)) {
 #pragma unroll
-    for (int k = 0; k < C::BC / 16; ++k) {
-      const uint64_t b = make_sdesc_sw128(v_base + k * (16 * 128), C::BC * 128, 1024);
-      umma_ts(tO, tS + k * 8, b, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
-      if (split) umma_ts(tO, tS + C::BC / 2 + k * 8, b, idesc_pv, 1u);
+      for (int k = 0; k < C::BC / 16; ++k) {
+        const uint64_t b = b0 + (uint64_t)((k * 16 * 128) >> 4);
+        umma_ts(tO, tS + k * 8, b, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+        umma_ts(tO, tS + C::BC / 2 + k * 8, b, idesc_pv, 1u);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < C::BC / 16; ++k)
+        umma_ts(tO, tS + k * 8, b0 + (uint64_t)((k * 16 * 128) >> 4), idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
     }
     umma_commit(t.bar(PB_O + q));
-  };
-  auto wait_k = [&](int j) {
-    return wait_or_abort(t.bar(PB_KFULL + j % C::STAGES), (uint32_t)(j / C::STAGES) & 1, t.abort_flag, t.status,
-                         kSiteMmaK);
   };
 #pragma unroll
   for (int q = 0; q < C::NQ; ++q)
     if (ok && t.nkv[q] > 0) ok = wait_or_abort(t.bar(PB_Q + q), 0, t.abort_flag, t.status, kSiteMmaQ);
-  if (ok) ok = wait_k(0);
+  if (ok) ok = wait_or_abort(t.bar(PB_KFULL), 0, t.abort_flag, t.status, kSiteMmaK);
   if (ok) {
     tc_fence_after();
 #pragma unroll
@@ -175,23 +184,27 @@ __device__ __forceinline__ void pp_mma(const PairCtx& t) {
       if (t.nkv[q] > 0) issue_s(q, 0);
     for (int j = 0; j < t.nkv_max && ok; ++j) {
       const int s = j % C::STAGES;
+      const int s1 = (j + 1) % C::STAGES;
+      bool have_v = false, have_k = false;
 #pragma unroll
       for (int q = 0; q < C::NQ; ++q) {
         if (!ok || j >= t.nkv[q]) continue;
-        if (!wait_or_abort(t.bar(PB_P + q), (uint32_t)j & 1, t.abort_flag, t.status, kSiteMmaP) ||
-            !wait_or_abort(t.bar(PB_VFULL + s), (uint32_t)(j / C::STAGES) & 1, t.abort_flag, t.status,
-                           kSiteMmaV)) {
-          ok = false;
-          continue;
+        ok = wait_or_abort(t.bar(PB_P + q), (uint32_t)j & 1, t.abort_flag, t.status, kSiteMmaP);
+        if (ok && !have_v) {
+          ok = wait_or_abort(t.bar(PB_VFULL + s), (uint32_t)(j / C::STAGES) & 1, t.abort_flag, t.status, kSiteMmaV);
+          have_v = true;
         }
+        if (!ok) continue;
         tc_fence_after();
         issue_pv(q, j);
         if (j + 1 < t.nkv[q]) {
-          if (!wait_k(j + 1)) {
-            ok = false;
-            continue;
+          if (!have_k) {
+            ok = wait_or_abort(t.bar(PB_KFULL + s1), (uint32_t)((j + 1) / C::STAGES) & 1, t.abort_flag, t.status,
+                               kSiteMmaK);
+            have_k = true;
+            if (!ok) continue;
+            tc_fence_after();
           }
-          tc_fence_after();
           issue_s(q, j + 1);
         }
       }
@@ -200,6 +213,33 @@ __device__ __forceinline__ void pp_mma(const PairCtx& t) {
   }
   umma_commit(t.bar(PB_EXIT));
   wait_drain(t.bar(PB_EXIT), 0, t.status);
+}
+
+// Exponentiate one 32-column chunk of S into packed 16-bit P (and, when
+// SPLIT, its low part P - P_hi) and store it to the chunk's TMEM columns.
+template <class C, bool BF16, bool SPLIT>
+__device__ __forceinline__ void pp_p_chunk(const uint32_t* sr, int ch, uint32_t tS, float2 scale2, float2 neg_m2,
+                                           float2& sum0, float2& sum1) {
+  uint32_t ph[16];
+  uint32_t pl[16];
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const int col = ch * 32 + 2 * c;
+    float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), scale2, neg_m2);
+    x.x = ex2_approx(x.x);
+    x.y = ex2_approx(x.y);
+    if (c & 1)
+      sum1 = __fadd2_rn(sum1, x);
+    else
+      sum0 = __fadd2_rn(sum0, x);
+    ph[c] = pack2<BF16>(x.x, x.y);
+    if constexpr (SPLIT) {
+      const float2 h = unpack2<BF16>(ph[c]);
+      pl[c] = pack2<BF16>(x.x - h.x, x.y - h.y);
+    }
+  }
+  tmem_st_32x32b_x16(tS + ch * 16, ph);
+  if constexpr (SPLIT) tmem_st_32x32b_x16(tS + C::BC / 2 + ch * 16, pl);
 }
 
 template <class C, bool BF16, bool CAUSAL>
@@ -253,52 +293,28 @@ __device__ __forceinline__ void pp_softmax(const PairCtx& t, const KernelParams&
     const float2 scale2 = make_float2(sl2, sl2);
     const float2 neg_m2 = make_float2(-m_use, -m_use);
     float2 sum0 = make_float2(0.f, 0.f), sum1 = make_float2(0.f, 0.f);
-    // P in 32-column chunks: exponentiate, pack to 16-bit pairs, store to the
-    // chunk's TMEM columns (S is already in registers, so overwriting is safe)
+    // P in 32-column chunks (S is already in registers, so overwriting it is safe)
+    if (split) {
 #pragma unroll
-    for (int ch = 0; ch < C::BC / 32; ++ch) {
-      uint32_t ph[16];
-      uint32_t pl[16];
+      for (int ch = 0; ch < C::BC / 32; ++ch) pp_p_chunk<C, BF16, true>(sr, ch, tS, scale2, neg_m2, sum0, sum1);
+    } else {
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int col = ch * 32 + 2 * c;
-        float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), scale2, neg_m2);
-        x.x = ex2_approx(x.x);
-        x.y = ex2_approx(x.y);
-        if (c & 1)
-          sum1 = __fadd2_rn(sum1, x);
-        else
-          sum0 = __fadd2_rn(sum0, x);
-        ph[c] = pack2<BF16>(x.x, x.y);
-        if (split) {
-          const float2 h = unpack2<BF16>(ph[c]);
-          pl[c] = pack2<BF16>(x.x - h.x, x.y - h.y);
-        }
-      }
-      tmem_st_32x32b_x16(tS + ch * 16, ph);
-      if (split) tmem_st_32x32b_x16(tS + C::BC / 2 + ch * 16, pl);
+      for (int ch = 0; ch < C::BC / 32; ++ch) pp_p_chunk<C, BF16, false>(sr, ch, tS, scale2, neg_m2, sum0, sum1);
     }
     const float2 sum2 = __fadd2_rn(sum0, sum1);
     l_run = l_run * alpha + (sum2.x + sum2.y);
-    if (j > 0) {
-      // O~ holds every product up to PV(j-1) once this phase has completed
-      bool ok2 = wait_or_abort(t.bar(PB_O + q), (uint32_t)(j - 1) & 1, t.abort_flag, t.status, kSiteSoftmaxO);
-      ok2 = __all_sync(0xffffffffu, ok2);
-      if (!ok2) {
-        ok = false;
-        break;
-      }
-      if (__any_sync(0xffffffffu, raise)) {
-        tc_fence_after();
+    // O~ <- alpha O~ when the maximum moved.  O~ already holds PV(j-1): the
+    // S(j) commit this thread waited on was issued after it, and a commit
+    // completes only when every earlier MMA of its issuing thread has.
+    if (j > 0 && __any_sync(0xffffffffu, raise)) {
 #pragma unroll 1
-        for (int c = 0; c < C::D; c += 32) {
-          uint32_t o[32];
-          tmem_ld_32x32b_x32(tO + c, o);
-          tmem_ld_wait_x32(o);
+      for (int c = 0; c < C::D; c += 32) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(tO + c, o);
+        tmem_ld_wait_x32(o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st_32x32b_x32(tO + c, o);
-        }
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        tmem_st_32x32b_x32(tO + c, o);
       }
     }
     tmem_st_wait();
