@@ -39,7 +39,7 @@ from exact_tiled_attention_fa2_gb300 import synthetic as sy  # noqa: E402
 METRIC = "forward attention TFLOP/s at 1 GB300 and % of dense FP16/BF16 tensor peak"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = 4
-KERNEL_SOURCES = ["fa2_fwd_kernel.cuh", "fa2_fwd_pingpong.cuh", "sm103_ptx.cuh", "fa2_internal.h", "fa2_abi.cu"]
+KERNEL_SOURCES = ["fa2_common.cuh", "fa2_fwd_pingpong.cuh", "fa2_fwd_dbuf.cuh", "sm103_ptx.cuh", "fa2_internal.h", "fa2_abi.cu"]
 
 
 def kernel_source_hash() -> str:
@@ -330,7 +330,7 @@ def main():
             "pct_of_peak": 100.0 * value / ws / peak,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                          "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
-                         "peak_source": peak_note, "kernel": "fa2_fwd_pingpong_kernel" if w.d <= 128 else "fa2_fwd_kernel",
+                         "peak_source": peak_note, "kernel": "fa2_fwd_pingpong_kernel" if w.d <= 128 else "fa2_fwd_dbuf_kernel",
                          "avg_launch_ms": avg_launch_ms,
                          "algorithmic_flops_per_launch": flops,
                          "algorithmic_bytes_per_launch": w.algorithmic_bytes()},

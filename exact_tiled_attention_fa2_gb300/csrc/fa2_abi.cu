@@ -88,6 +88,44 @@ int encode_map(CUtensorMap* m, const void* base, int bh, int n, int d, int rows,
   return r == CUDA_SUCCESS ? FA2_OK : FA2_ERR_CUDA;
 }
 
+// The tensor maps of the last call on this host thread: repeated calls on the
+// same buffers and sizes (the usual case in a loop) skip re-encoding them.
+struct MapCache {
+  bool valid = false;
+  int dev = -1, bh = 0, n = 0, d = 0, dtype = -1;
+  const void *q = nullptr, *k = nullptr, *v = nullptr;
+  CUtensorMap tm_q, tm_k, tm_v;
+};
+thread_local MapCache t_maps;
+
+int cached_maps(LaunchArgs& a, const void* q, const void* k, const void* v, int bh, int n, int d, int dtype) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA2_ERR_CUDA;
+  MapCache& c = t_maps;
+  if (!(c.valid && c.dev == dev && c.q == q && c.k == k && c.v == v && c.bh == bh && c.n == n && c.d == d &&
+        c.dtype == dtype)) {
+    const bool bf16 = dtype == FA2_BF16;
+    const TileGeometry g = tile_geometry(d);
+    c.valid = false;
+    if (encode_map(&c.tm_q, q, bh, n, d, g.q_rows, bf16) || encode_map(&c.tm_k, k, bh, n, d, g.kv_rows, bf16) ||
+        encode_map(&c.tm_v, v, bh, n, d, g.kv_rows, bf16))
+      return FA2_ERR_CUDA;
+    c.dev = dev;
+    c.q = q;
+    c.k = k;
+    c.v = v;
+    c.bh = bh;
+    c.n = n;
+    c.d = d;
+    c.dtype = dtype;
+    c.valid = true;
+  }
+  a.tm_q = c.tm_q;
+  a.tm_k = c.tm_k;
+  a.tm_v = c.tm_v;
+  return FA2_OK;
+}
+
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
   uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + nb && y < x + na;
@@ -136,9 +174,8 @@ extern "C" int fa2_fwd(const void* q, const void* k, const void* v, void* o, flo
   LaunchArgs a;
   std::memset(&a, 0, sizeof(a));
   const int bh = B * H;
-  if (encode_map(&a.tm_q, q, bh, N, d, g.q_rows, bf16) || encode_map(&a.tm_k, k, bh, N, d, g.kv_rows, bf16) ||
-      encode_map(&a.tm_v, v, bh, N, d, g.kv_rows, bf16))
-    return FA2_ERR_CUDA;
+  rc = cached_maps(a, q, k, v, bh, N, d, dtype);
+  if (rc) return rc;
   a.p.o = o;
   a.p.lse = lse;
   a.p.status = ds->status;

@@ -1,0 +1,400 @@
+// fa2_fwd_dbuf.cuh -- forward kernel for head dim 256: one 128-row query tile
+// per CTA with two S buffers in tensor memory.
+//
+// At d = 256 the accumulator O~ alone takes 256 TMEM columns and a query tile
+// 64 KB of shared memory, so a CTA holds one query tile.  Key/value tiles of
+// B_c = 64 rows stream through separate 2-stage K and V rings (Q 64 KB +
+// 4 x 32 KB).  S alternates between two 64-column TMEM buffers, and the
+// MMA-issuing thread runs, per key tile j,
+//
+//     O~ += P(j) V_j,   S(j+2) = Q K_{j+2}^T   (into the buffer P(j) came from)
+//
+// so the softmax of tile j+1 overlaps those two products.  The PV products
+// have N = d = 256, the MMA shape that keeps the tensor pipe busiest.  A K
+// stage is released as soon as its S product completes and a V stage after
+// its PV product, so the next K tile loads while the current PV runs.
+// Online softmax as in the two-tile kernel: running max raised only past a
+// 2^8 margin, O~ rescaled in place when it is.
+//
+// Warp roles (192 threads): warps 0-3 softmax + epilogue (one thread per
+// query row = TMEM lane), warp 4 TMEM owner and MMA issuer, warp 5 TMA.
+#pragma once
+
+#include "fa2_fwd_pingpong.cuh"
+
+namespace fa2 {
+
+template <int D_>
+struct DbufConfig {
+  static constexpr int D = D_;
+  static constexpr int BR = 128;
+  static constexpr int BC = 64;
+  static constexpr int KSTAGES = 2;
+  static constexpr int VSTAGES = 2;
+  static constexpr int THREADS = 192;
+  static constexpr int MMA_WARP = 4;
+  static constexpr int TMA_WARP = 5;
+  static constexpr uint32_t Q_BYTES = BR * D * 2;
+  static constexpr uint32_t KV_BYTES = BC * D * 2;
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + KSTAGES * KV_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_V + VSTAGES * KV_BYTES;
+  static constexpr uint32_t NUM_BARS = 24;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
+  static constexpr uint32_t TMEM_S = 0;     // + 64 * buffer
+  static constexpr uint32_t TMEM_O = 128;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(D == 256, "double-buffered-S kernel: head dim 256");
+  static_assert(TMEM_O + D <= TMEM_COLS, "tensor memory");
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+};
+
+enum : int {
+  DB_Q = 0,
+  DB_KFULL = 1,    // + stage
+  DB_KEMPTY = 3,   // + stage
+  DB_VFULL = 5,    // + stage
+  DB_VEMPTY = 7,   // + stage
+  DB_S = 9,        // + buffer
+  DB_O = 12,       // after every PV product (waited only before a rare O~ rescale)
+  DB_EXIT = 13,
+  DB_OLAST = 14,   // once, after the last PV product: the epilogue's single-phase wait
+  DB_P = 15,       // + buffer.  One per S buffer: S(j+1) is issued before the MMA
+                   // thread waits for P(j), so the softmax may finish P(j) and
+                   // P(j+1) first; on a single barrier that would put it two
+                   // phases ahead of the parity the MMA thread waits for.
+};
+
+// K_j is needed two products before V_j, so the K and V streams are issued
+// independently: whichever ring has a free slot gets the next load.
+template <class C>
+__device__ __forceinline__ void db_producer(const TileCtx& t, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                                            const CUtensorMap* tm_v) {
+  mbar_arrive_expect_tx(t.bar(DB_Q), C::Q_BYTES);
+  for (int kb = 0; kb < C::D / 64; ++kb)
+    tma_load_3d(t.sQ + kb * (C::BR * 128), tm_q, kb * 64, t.q0, t.bh, t.bar(DB_Q));
+  int jk = 0, jv = 0;
+  uint64_t idle_since = 0;
+  while (jk < t.nkv || jv < t.nkv) {
+    bool progressed = false;
+    if (jk < t.nkv) {
+      const int s = jk % C::KSTAGES, u = jk / C::KSTAGES;
+      if (u == 0 || mbar_try_wait(t.bar(DB_KEMPTY + s), (u - 1) & 1)) {
+        mbar_arrive_expect_tx(t.bar(DB_KFULL + s), C::KV_BYTES);
+        for (int kb = 0; kb < C::D / 64; ++kb)
+          tma_load_3d(t.sK + s * C::KV_BYTES + kb * (C::BC * 128), tm_k, kb * 64, jk * C::BC, t.bh,
+                      t.bar(DB_KFULL + s));
+        ++jk;
+        progressed = true;
+      }
+    }
+    if (jv < t.nkv) {
+      const int s = jv % C::VSTAGES, u = jv / C::VSTAGES;
+      if (u == 0 || mbar_try_wait(t.bar(DB_VEMPTY + s), (u - 1) & 1)) {
+        mbar_arrive_expect_tx(t.bar(DB_VFULL + s), C::KV_BYTES);
+        for (int kb = 0; kb < C::D / 64; ++kb)
+          tma_load_3d(t.sV + s * C::KV_BYTES + kb * (C::BC * 128), tm_v, kb * 64, jv * C::BC, t.bh,
+                      t.bar(DB_VFULL + s));
+        ++jv;
+        progressed = true;
+      }
+    }
+    if (progressed) {
+      idle_since = 0;
+    } else {
+      const uint64_t now = global_timer_ns();
+      if (idle_since == 0) {
+        idle_since = now;
+      } else if (*t.abort_flag) {
+        break;
+      } else if (now - idle_since > kWaitLimitNs) {
+        *t.abort_flag = 1;
+        atomicOr(t.status, kStatusTimeout | (1u << (8 + kSiteProducerEmpty)));
+        break;
+      }
+    }
+  }
+  // Own copies in flight land before the CTA may exit.
+  wait_drain(t.bar(DB_Q), 0, t.status);
+  for (int s = 0; s < C::KSTAGES; ++s) {
+    const int last = jk - 1 - ((jk - 1 - s) % C::KSTAGES + C::KSTAGES) % C::KSTAGES;  // last K tile in stage s
+    if (last >= 0) wait_drain(t.bar(DB_KFULL + s), (uint32_t)(last / C::KSTAGES) & 1, t.status);
+  }
+  for (int s = 0; s < C::VSTAGES; ++s) {
+    const int last = jv - 1 - ((jv - 1 - s) % C::VSTAGES + C::VSTAGES) % C::VSTAGES;
+    if (last >= 0) wait_drain(t.bar(DB_VFULL + s), (uint32_t)(last / C::VSTAGES) & 1, t.status);
+  }
+}
+
+template <class C, bool BF16, bool CAUSAL>
+__device__ __forceinline__ void db_mma(const TileCtx& t) {
+  constexpr uint32_t idesc_qk = make_idesc_f16(C::BR, C::BC, BF16, false, false);
+  constexpr uint32_t idesc_pv = make_idesc_f16(C::BR, C::D, BF16, false, true);
+  const uint64_t dq0 = make_sdesc_sw128(t.sQ, 16, 1024);
+  const uint64_t dk0 = make_sdesc_sw128(t.sK, 16, 1024);
+  const uint64_t dv0 = make_sdesc_sw128(t.sV, C::BC * 128, 1024);
+  bool ok = true;
+  auto issue_s = [&](int j) -> bool {
+    const int sk = j % C::KSTAGES;
+    if (!wait_or_abort(t.bar(DB_KFULL + sk), (uint32_t)(j / C::KSTAGES) & 1, t.abort_flag, t.status, kSiteMmaK))
+      return false;
+    tc_fence_after();
+    const uint64_t b0 = dk0 + (uint64_t)((sk * C::KV_BYTES) >> 4);
+    const uint32_t tS = t.tmem + C::TMEM_S + 64 * (j & 1);
+#pragma unroll
+    for (int k = 0; k < C::D / 16; ++k)
+      umma_ss(tS, dq0 + kmajor_step<C>(k, C::BR), b0 + kmajor_step<C>(k, C::BC), idesc_qk, k > 0 ? 1u : 0u);
+    umma_commit(t.bar(DB_S + (j & 1)));
+    umma_commit(t.bar(DB_KEMPTY + sk));
+    return true;
+  };
+  if (wait_or_abort(t.bar(DB_Q), 0, t.abort_flag, t.status, kSiteMmaQ)) {
+    tc_fence_after();
+    ok = issue_s(0);
+    if (ok && t.nkv > 1) ok = issue_s(1);
+    for (int j = 0; j < t.nkv && ok; ++j) {
+      const int sv = j % C::VSTAGES;
+      ok = wait_or_abort(t.bar(DB_P + (j & 1)), (uint32_t)(j >> 1) & 1, t.abort_flag, t.status, kSiteMmaP) &&
+           wait_or_abort(t.bar(DB_VFULL + sv), (uint32_t)(j / C::VSTAGES) & 1, t.abort_flag, t.status, kSiteMmaV);
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t b0 = dv0 + (uint64_t)((sv * C::KV_BYTES) >> 4);
+      const uint32_t tS = t.tmem + C::TMEM_S + 64 * (j & 1);
+      const uint32_t tO = t.tmem + C::TMEM_O;
+      if (split_tile<C, BF16, CAUSAL>(j, t.q0, t.n)) {
+#pragma unroll
+        for (int k = 0; k < C::BC / 16; ++k) {
+          const uint64_t b = b0 + (uint64_t)((k * 16 * 128) >> 4);
+          umma_ts(tO, tS + k * 8, b, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+          umma_ts(tO, tS + C::BC / 2 + k * 8, b, idesc_pv, 1u);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < C::BC / 16; ++k)
+          umma_ts(tO, tS + k * 8, b0 + (uint64_t)((k * 16 * 128) >> 4), idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+      }
+      umma_commit(t.bar(DB_O));
+      umma_commit(t.bar(DB_VEMPTY + sv));
+      if (j + 1 == t.nkv) umma_commit(t.bar(DB_OLAST));
+      // S(j+2) reuses the columns P(j) is read from: in-order MMA execution
+      // lets it follow the product above directly
+      if (j + 2 < t.nkv) ok = issue_s(j + 2);
+    }
+  }
+  umma_commit(t.bar(DB_EXIT));
+  wait_drain(t.bar(DB_EXIT), 0, t.status);
+}
+
+template <class C, bool BF16, bool CAUSAL>
+__device__ __forceinline__ void db_softmax(const TileCtx& t, const KernelParams& p, int warp, int lane) {
+  const int quad = warp & 3;
+  const int r = quad * 32 + lane;
+  const int row = t.q0 + r;
+  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+  const uint32_t tO = t.tmem + lane_off + C::TMEM_O;
+  const float sl2 = p.scale_log2;
+  float m_run = -INFINITY;
+  float l_run = 0.f;
+  bool ok = true;
+  for (int j = 0; j < t.nkv; ++j) {
+    const uint32_t tS = t.tmem + lane_off + C::TMEM_S + 64 * (j & 1);
+    ok = wait_or_abort(t.bar(DB_S + (j & 1)), (uint32_t)(j >> 1) & 1, t.abort_flag, t.status, kSiteSoftmaxS);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    tc_fence_after();
+    uint32_t sr[C::BC];
+#pragma unroll
+    for (int c = 0; c < C::BC; c += 32) tmem_ld_32x32b_x32(tS + c, sr + c);
+#pragma unroll
+    for (int c = 0; c < C::BC; c += 32) tmem_ld_wait_x32(sr + c);
+    const int k0 = j * C::BC;
+    const bool masked = (k0 + C::BC > t.n) || (CAUSAL && (k0 + C::BC - 1 > t.q0));
+    if (masked) {
+#pragma unroll
+      for (int c = 0; c < C::BC; ++c) {
+        const int key = k0 + c;
+        if (key >= t.n || (CAUSAL && key > row)) sr[c] = __float_as_uint(-INFINITY);
+      }
+    }
+    float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < C::BC; c += 8) {
+      mx0 = fmax3(mx0, __uint_as_float(sr[c + 0]), __uint_as_float(sr[c + 1]));
+      mx1 = fmax3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+      mx2 = fmax3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+      mx3 = fmax3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+    }
+    const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+    const bool raise = m_tile > m_run + kRescaleLog2;
+    const float m_new = raise ? m_tile : m_run;
+    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+    const float alpha = raise ? ex2_approx(m_run - m_use) : 1.f;
+    const float2 scale2 = make_float2(sl2, sl2);
+    const float2 neg_m2 = make_float2(-m_use, -m_use);
+    float2 sum0 = make_float2(0.f, 0.f), sum1 = make_float2(0.f, 0.f);
+    if (split_tile<C, BF16, CAUSAL>(j, t.q0, t.n)) {
+#pragma unroll
+      for (int ch = 0; ch < C::BC / 32; ++ch) pp_p_chunk<C, BF16, true>(sr, ch, tS, scale2, neg_m2, sum0, sum1);
+    } else {
+#pragma unroll
+      for (int ch = 0; ch < C::BC / 32; ++ch) pp_p_chunk<C, BF16, false>(sr, ch, tS, scale2, neg_m2, sum0, sum1);
+    }
+    const float2 sum2 = __fadd2_rn(sum0, sum1);
+    l_run = l_run * alpha + (sum2.x + sum2.y);
+    if (j > 0 && __any_sync(0xffffffffu, raise)) {
+      // S(j) was issued before PV(j-1): wait for that product before rescaling
+      // O~.  S(j) completing implies PV(j-2) did, so this barrier is at phase
+      // j-1 or j and the parity wait is unambiguous.
+      bool ok2 = wait_or_abort(t.bar(DB_O), (uint32_t)(j - 1) & 1, t.abort_flag, t.status, kSiteSoftmaxO);
+      ok2 = __all_sync(0xffffffffu, ok2);
+      if (!ok2) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < C::D; c += 32) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(tO + c, o);
+        tmem_ld_wait_x32(o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        tmem_st_32x32b_x32(tO + c, o);
+      }
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(t.bar(DB_P + (j & 1)));
+    m_run = m_new;
+  }
+  if (ok) {
+    // Not the every-product barrier: S(j+1) is issued before PV(j), so it can
+    // still be two phases behind here, where a parity wait would pass early.
+    ok = wait_or_abort(t.bar(DB_OLAST), 0, t.abort_flag, t.status, kSiteEpilogueO);
+    ok = __all_sync(0xffffffffu, ok);
+  }
+  if (!ok) return;
+  tc_fence_after();
+  const float inv_l = 1.f / l_run;
+  uint8_t* o_row = reinterpret_cast<uint8_t*>(p.o) + ((size_t)t.bh * (size_t)t.n + (size_t)row) * (C::D * 2);
+#pragma unroll 1
+  for (int c = 0; c < C::D; c += 32) {
+    uint32_t o[32];
+    tmem_ld_32x32b_x32(tO + c, o);
+    tmem_ld_wait_x32(o);
+    uint32_t packed[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      packed[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+    if (row < t.n) {
+      uint4* dst = reinterpret_cast<uint4*>(o_row + c * 2);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+    }
+  }
+  if (row < t.n) p.lse[(size_t)t.bh * (size_t)t.n + (size_t)row] = (m_run + log2f(l_run)) * 0.6931471805599453f;
+}
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(192, 1)
+    fa2_fwd_dbuf_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const KernelParams p) {
+  using C = DbufConfig<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  const int warp = (int)(threadIdx.x >> 5);
+  const int lane = (int)(threadIdx.x & 31);
+
+  TileCtx t;
+  t.bar0 = sbase + C::OFF_BAR;
+  t.sQ = sbase + C::OFF_Q;
+  t.sK = sbase + C::OFF_K;
+  t.sV = sbase + C::OFF_V;
+  t.abort_flag = abort_flag;
+  t.status = p.status;
+  t.n = p.n;
+  t.bh = (int)blockIdx.x;
+  const int q_tile = CAUSAL ? (int)(gridDim.y - 1 - blockIdx.y) : (int)blockIdx.y;
+  t.q0 = q_tile * C::BR;
+  const int kv_end = CAUSAL ? min(t.n, t.q0 + C::BR) : t.n;
+  t.nkv = (kv_end + C::BC - 1) / C::BC;
+
+  if (threadIdx.x == 0) {
+    mbar_init(t.bar(DB_Q), 1);
+    for (int s = 0; s < C::KSTAGES; ++s) {
+      mbar_init(t.bar(DB_KFULL + s), 1);
+      mbar_init(t.bar(DB_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < C::VSTAGES; ++s) {
+      mbar_init(t.bar(DB_VFULL + s), 1);
+      mbar_init(t.bar(DB_VEMPTY + s), 1);
+    }
+    mbar_init(t.bar(DB_S), 1);
+    mbar_init(t.bar(DB_S + 1), 1);
+    mbar_init(t.bar(DB_P), 4);       // one arrival per softmax warp
+    mbar_init(t.bar(DB_P + 1), 4);
+    mbar_init(t.bar(DB_O), 1);
+    mbar_init(t.bar(DB_OLAST), 1);
+    mbar_init(t.bar(DB_EXIT), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::TMA_WARP && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  t.tmem = *tmem_slot;
+
+  if (warp == C::TMA_WARP) {
+    if (lane == 0) db_producer<C>(t, &tm_q, &tm_k, &tm_v);
+  } else if (warp == C::MMA_WARP) {
+    if (lane == 0) db_mma<C, BF16, CAUSAL>(t);
+    __syncwarp();
+  } else {
+    db_softmax<C, BF16, CAUSAL>(t, p, warp, lane);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(t.tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D, bool BF16, bool CAUSAL>
+int launch_fwd_dbuf(const LaunchArgs& a) {
+  using C = DbufConfig<D>;
+  auto kern = fa2_fwd_dbuf_kernel<D, BF16, CAUSAL>;
+  static std::atomic<unsigned long long> configured{0};
+  const int e = once_per_device(configured, [&]() -> int {
+    return (int)cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
+  });
+  if (e != 0) return e;
+  dim3 grid((unsigned)a.p.bh, (unsigned)a.p.num_q_tiles);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.p);
+  return (int)cudaGetLastError();
+}
+
+template <int D>
+int launch_fwd_dbuf_dispatch(const LaunchArgs& a) {
+  if (a.bf16) return a.causal ? launch_fwd_dbuf<D, true, true>(a) : launch_fwd_dbuf<D, true, false>(a);
+  return a.causal ? launch_fwd_dbuf<D, false, true>(a) : launch_fwd_dbuf<D, false, false>(a);
+}
+
+}  // namespace fa2

@@ -29,7 +29,7 @@
 // 2 x 128 x 200 + 128 x 104 = 384 x 168 registers at launch.
 #pragma once
 
-#include "fa2_fwd_kernel.cuh"
+#include "fa2_common.cuh"
 
 namespace fa2 {
 
@@ -73,7 +73,7 @@ enum : int {
   PB_KVEMPTY = 10,  // + stage
   PB_S = 14,        // + tile
   PB_P = 16,        // + tile
-  PB_O = 18,        // + tile
+  PB_O = 18,        // + tile: once, after the tile's last PV product
   PB_EXIT = 20,
 };
 
@@ -171,7 +171,7 @@ __device__ __forceinline__ void pp_mma(const PairCtx& t) {
       for (int k = 0; k < C::BC / 16; ++k)
         umma_ts(tO, tS + k * 8, b0 + (uint64_t)((k * 16 * 128) >> 4), idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
     }
-    umma_commit(t.bar(PB_O + q));
+    if (j + 1 == t.nkv[q]) umma_commit(t.bar(PB_O + q));
   };
 #pragma unroll
   for (int q = 0; q < C::NQ; ++q)
@@ -324,7 +324,7 @@ __device__ __forceinline__ void pp_softmax(const PairCtx& t, const KernelParams&
     m_run = m_new;
   }
   if (ok) {
-    ok = wait_or_abort(t.bar(PB_O + q), (uint32_t)(nkv - 1) & 1, t.abort_flag, t.status, kSiteEpilogueO);
+    ok = wait_or_abort(t.bar(PB_O + q), 0, t.abort_flag, t.status, kSiteEpilogueO);
     ok = __all_sync(0xffffffffu, ok);
   }
   if (!ok) return;
@@ -441,14 +441,17 @@ template <int D, bool BF16, bool CAUSAL>
 int launch_fwd_pingpong(const LaunchArgs& a) {
   using C = PingPongConfig<D>;
   auto kern = fa2_fwd_pingpong_kernel<D, BF16, CAUSAL>;
-  // The softmax warpgroups' setmaxnreg.inc only completes if the block was
-  // launched with the registers the split assumes: refuse to launch otherwise.
-  cudaFuncAttributes attr;
-  cudaError_t e = cudaFuncGetAttributes(&attr, kern);
-  if (e != cudaSuccess) return (int)e;
-  if ((uint32_t)attr.numRegs != C::REGS_AT_LAUNCH) return (int)cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
-  if (e != cudaSuccess) return (int)e;
+  static std::atomic<unsigned long long> configured{0};
+  const int e = once_per_device(configured, [&]() -> int {
+    // The softmax warpgroups' setmaxnreg.inc only completes if the block was
+    // launched with the registers the split assumes: refuse to launch otherwise.
+    cudaFuncAttributes attr;
+    cudaError_t r = cudaFuncGetAttributes(&attr, kern);
+    if (r != cudaSuccess) return (int)r;
+    if ((uint32_t)attr.numRegs != C::REGS_AT_LAUNCH) return (int)cudaErrorInvalidConfiguration;
+    return (int)cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
+  });
+  if (e != 0) return e;
   const int pairs = (a.p.n + C::NQ * C::BR - 1) / (C::NQ * C::BR);
   dim3 grid((unsigned)a.p.bh, (unsigned)pairs);
   kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.p);

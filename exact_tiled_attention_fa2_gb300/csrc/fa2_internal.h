@@ -6,11 +6,13 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace fa2 {
 
 // Status bits a kernel ORs into the device status word when a bounded wait
-// gives up: bit 0 = some wait timed out; bits 8..15 = wait site (role and
-// barrier, see the kernel's WaitSite); the host maps any nonzero word to
+// gives up: bit 0 = some wait timed out; bit 8 + s for each wait site s that
+// gave up (see WaitSite); the host maps any nonzero word to
 // FA2_ERR_DEVICE_TIMEOUT.
 constexpr uint32_t kStatusTimeout = 1u;
 
@@ -40,6 +42,20 @@ struct TileGeometry {
 };
 
 TileGeometry tile_geometry(int d);
+
+// One-time per-device set-up of a kernel instantiation (attributes, checks):
+// `setup` runs until it succeeds once on a device; devices >= 64 run it on
+// every call.
+template <class F>
+inline int once_per_device(std::atomic<unsigned long long>& done, F&& setup) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return (int)cudaErrorNoDevice;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return 0;
+  const int e = setup();
+  if (e == 0 && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // Each launches the forward kernel for one head dim; returns a cudaError_t.
 int launch_fwd_d64(const LaunchArgs& a);

@@ -228,3 +228,23 @@ def test_invalid_device_arguments_launch_nothing():
     rc = lib.fa2_fwd(base, base, base, base, lse.data_ptr(), 1, 1, 64, 64, 0.125, 0, 0, None)
     assert rc == fa2.FA2_ERR_INVALID_ARG           # o aliases q
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("d,dtype,causal,N", [(256, sy.FP16, False, 3000), (256, sy.BF16, True, 1000),
+                                              (128, sy.BF16, True, 2048), (64, sy.FP16, False, 1024)])
+def test_repeated_launches_identical(d, dtype, causal, N):
+    """Many back-to-back launches: every one bit-identical and no wait ever timing out.
+
+    Pipeline races (a barrier running a phase ahead of its waiter) show up as
+    rare timeouts or wrong tiles under varying timing, not on a single run."""
+    B, H = 1, 16
+    q, k, v = (to_dev(x, dtype) for x in sy.make_qkv(B, H, N, d, dtype, seed=7200 + d + N))
+    o0, l0 = fa2.fa2_fwd(q, k, v, causal=causal)
+    o, lse = torch.empty_like(o0), torch.empty_like(l0)
+    for i in range(60):
+        fa2.fa2_fwd(q, k, v, o, lse, causal=causal)
+        if i % 10 == 9:
+            torch.cuda.synchronize()
+            assert torch.equal(o, o0) and torch.equal(lse, l0), "launch %d differs" % i
+    code, detail = fa2.fa2_get_device_status()
+    assert code == fa2.FA2_OK, "a wait timed out (0x%x)" % detail
