@@ -140,8 +140,8 @@ int check_shape(int B, int H, int N, int d, float scale, int causal, int dtype) 
   if (causal != 0 && causal != 1) return FA2_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA2_ERR_INVALID_ARG;
   if (d != 64 && d != 128 && d != 256) return FA2_ERR_UNSUPPORTED;
-  if ((long long)B * (long long)H > INT_MAX) return FA2_ERR_UNSUPPORTED;
-  if ((N + 127) / 128 > 65535) return FA2_ERR_UNSUPPORTED;  // query tiles map to grid.y
+  // one block per (head, query tile) in a 1-D grid
+  if ((long long)B * (long long)H * (long long)((N + 127) / 128) > INT_MAX) return FA2_ERR_UNSUPPORTED;
   return FA2_OK;
 }
 

@@ -92,6 +92,31 @@ __device__ __forceinline__ bool split_tile(int j, int q0, int n) {
   }
 }
 
+// Order of work units over a 1-D grid of (B*H) x units blocks.  Heads go in
+// groups of kHeadGroup; inside a group the units run from the last (the one
+// with the most key tiles under a causal mask) to the first, heads
+// interleaved.  So the CTAs resident at a time share the K/V of about
+// kHeadGroup heads in L2, and causal work is launched longest first within
+// each group, whose short tail overlaps the next group's long units.
+constexpr int kHeadGroup = 8;
+
+__device__ __forceinline__ void unit_of_block(int block, int bh_total, int units, int& bh, int& unit) {
+  const int full_groups = bh_total / kHeadGroup;
+  const int per_group = kHeadGroup * units;
+  int g, size, r;
+  if (block < full_groups * per_group) {
+    g = block / per_group;
+    r = block - g * per_group;
+    size = kHeadGroup;
+  } else {
+    g = full_groups;
+    r = block - full_groups * per_group;
+    size = bh_total - full_groups * kHeadGroup;
+  }
+  bh = g * kHeadGroup + r % size;
+  unit = units - 1 - r / size;
+}
+
 // Addresses and sizes of one query tile's work, shared by its warp roles.
 struct TileCtx {
   uint32_t bar0;       // shared address of barrier 0

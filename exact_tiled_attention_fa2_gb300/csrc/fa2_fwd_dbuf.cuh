@@ -321,8 +321,8 @@ __global__ void __launch_bounds__(192, 1)
   t.abort_flag = abort_flag;
   t.status = p.status;
   t.n = p.n;
-  t.bh = (int)blockIdx.x;
-  const int q_tile = CAUSAL ? (int)(gridDim.y - 1 - blockIdx.y) : (int)blockIdx.y;
+  int q_tile;
+  unit_of_block((int)blockIdx.x, p.bh, p.num_q_tiles, t.bh, q_tile);
   t.q0 = q_tile * C::BR;
   const int kv_end = CAUSAL ? min(t.n, t.q0 + C::BR) : t.n;
   t.nkv = (kv_end + C::BC - 1) / C::BC;
@@ -386,7 +386,7 @@ int launch_fwd_dbuf(const LaunchArgs& a) {
     return (int)cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
   });
   if (e != 0) return e;
-  dim3 grid((unsigned)a.p.bh, (unsigned)a.p.num_q_tiles);
+  dim3 grid((unsigned)(a.p.bh * a.p.num_q_tiles));
   kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.p);
   return (int)cudaGetLastError();
 }

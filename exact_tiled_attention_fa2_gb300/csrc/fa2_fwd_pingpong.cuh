@@ -372,9 +372,9 @@ __global__ void __launch_bounds__(384, 1)
   t.abort_flag = abort_flag;
   t.status = p.status;
   t.n = p.n;
-  t.bh = (int)blockIdx.x;
-  // causal: the pairs with the most key tiles (highest rows) start first
-  const int pair = CAUSAL ? (int)(gridDim.y - 1 - blockIdx.y) : (int)blockIdx.y;
+  const int pairs = (t.n + C::NQ * C::BR - 1) / (C::NQ * C::BR);
+  int pair;
+  unit_of_block((int)blockIdx.x, p.bh, pairs, t.bh, pair);
   t.nkv_max = 0;
   for (int q = 0; q < C::NQ; ++q) {
     t.q0[q] = pair * (C::NQ * C::BR) + q * C::BR;
@@ -453,7 +453,7 @@ int launch_fwd_pingpong(const LaunchArgs& a) {
   });
   if (e != 0) return e;
   const int pairs = (a.p.n + C::NQ * C::BR - 1) / (C::NQ * C::BR);
-  dim3 grid((unsigned)a.p.bh, (unsigned)pairs);
+  dim3 grid((unsigned)(a.p.bh * pairs));
   kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.p);
   return (int)cudaGetLastError();
 }

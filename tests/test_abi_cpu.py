@@ -78,7 +78,7 @@ def _call(lib, q=A, k=2 * A, v=3 * A, o=4 * A, lse=5 * A, **kw):
     (dict(d=32), fa2.FA2_ERR_UNSUPPORTED),
     (dict(d=96), fa2.FA2_ERR_UNSUPPORTED),
     (dict(d=512), fa2.FA2_ERR_UNSUPPORTED),
-    (dict(N=65535 * 128 + 1), fa2.FA2_ERR_UNSUPPORTED),
+    (dict(N=2 ** 30, H=2 ** 10), fa2.FA2_ERR_UNSUPPORTED),
 ])
 def test_bad_sizes_rejected(lib, kw, code):
     assert _call(lib, **kw) == code
