@@ -132,26 +132,46 @@ class ClockSampler:
                 "samples": len(sms)}
 
 
+ORACLE_ROWS_PER_BATCH = 64
+
+
 def oracle_sample(w: sy.Workload, q, k, v, target_s: float, rng, threads: int = 0):
-    """Run the CPU oracle on random rows until ~target_s seconds; return (flops, seconds, rows)."""
+    """Run the CPU oracle on random rows until ~target_s seconds; return (flops, seconds, rows).
+
+    Each batch is ORACLE_ROWS_PER_BATCH uniformly random rows of one uniformly
+    random (batch, head) slice -- an unbiased sample of the workload's rows
+    that lets the oracle widen that slice's K and V once per batch."""
     import oracle
 
     BH = w.B * w.H
     done_flops, done_s, done_rows = 0.0, 0.0, 0
-    batch = 8
     while done_s < target_s:
-        bh = np.sort(rng.integers(0, BH, size=batch))
-        rows = rng.integers(0, w.N, size=batch)
+        bh = np.full(ORACLE_ROWS_PER_BATCH, int(rng.integers(0, BH)))
+        rows = rng.integers(0, w.N, size=ORACLE_ROWS_PER_BATCH)
         t0 = time.perf_counter()
         oracle.attention_rows(q, k, v, w.dtype, w.scale, w.causal, bh, rows, threads=threads)
-        dt = time.perf_counter() - t0
-        keys = (rows + 1) if w.causal else np.full(batch, w.N)
+        done_s += time.perf_counter() - t0
+        keys = (rows + 1) if w.causal else np.full(rows.size, w.N)
         done_flops += float(4.0 * w.d * keys.sum())
-        done_s += dt
-        done_rows += batch
-        if dt < target_s / 20:
-            batch *= 2
+        done_rows += rows.size
     return done_flops, done_s, done_rows
+
+
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The maximum of `value` over every rank of the default process group
+    (the value itself when there is no group)."""
+    if dist is None or not dist.is_initialized():
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step: float, steps: int, world_size: int, max_ms: float) -> float:
+    """Whole-job TFLOP/s: every rank's steps, over the slowest rank's time."""
+    return flops_per_step * steps * world_size / (max_ms / 1e3) / 1e12
 
 
 def dist_env():
@@ -301,15 +321,12 @@ def main():
     code, detail = fa2.fa2_get_device_status(stream)
     if code != fa2.FA2_OK:
         raise RuntimeError("device status %d (0x%x) in timed region" % (code, detail))
-    max_ms = elapsed_ms
+    max_ms = max_over_ranks(elapsed_ms, dist, dev)
     if dist is not None:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        max_ms = float(t.item())
         dist.barrier()
 
     flops = w.flops()
-    value = flops * args.steps * ws / (max_ms / 1e3) / 1e12
+    value = job_throughput(flops, args.steps, ws, max_ms)
     avg_launch_ms = sum(kernel_ms) / len(kernel_ms)
     achieved = flops / (avg_launch_ms / 1e3) / 1e12
     peak, peak_note = measured_peak()

@@ -54,6 +54,8 @@ def load_library():
     lib.fa2_fwd_host_workspace_bytes.restype = sz
     lib.fa2_fwd_host_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, ci, vp]
     lib.fa2_fwd_host_noalloc.restype = ci
+    lib.fa2_selftest_wait_timeout.argtypes = [ci, vp]
+    lib.fa2_selftest_wait_timeout.restype = ci
     lib.fa2_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.fa2_get_device_status.restype = ci
     lib.fa2_status_string.argtypes = [ci]
@@ -171,6 +173,14 @@ def fa2_fwd_host_noalloc(q, k, v, o, lse, scale=None, causal=False, dtype=None, 
     if rc:
         raise Fa2Error(rc, "fa2_fwd_host_noalloc")
     return o, lse
+
+
+def fa2_selftest_wait_timeout(limit_us: int = 2000, stream=None) -> None:
+    """Launch the bounded-wait self-test (a wait that must expire after limit_us)."""
+    import torch
+    rc = load_library().fa2_selftest_wait_timeout(int(limit_us), _stream_handle(stream, torch.cuda.current_device()))
+    if rc:
+        raise Fa2Error(rc, "fa2_selftest_wait_timeout")
 
 
 def fa2_get_device_status(stream=None):

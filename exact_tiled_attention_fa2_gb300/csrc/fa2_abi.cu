@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "../../include/fa2.h"
+#include "fa2_common.cuh"
 #include "fa2_internal.h"
 
 namespace fa2 {
@@ -274,6 +275,34 @@ extern "C" int fa2_fwd_host_noalloc(const void* q_host, const void* k_host, cons
   if (rc) return rc;
   return fa2_fwd_host(q_host, k_host, v_host, o_host, lse_host, scratch, FA2_NOALLOC_SCRATCH_BYTES, B, H, N, d,
                       scale, causal, dtype, stream);
+}
+
+namespace fa2 {
+
+// One thread waits, through the kernels' bounded-wait helper, on an mbarrier
+// that nothing ever arrives on; the wait expires after limit_ns and records
+// kSiteSelfTest in the status word, and the kernel returns normally.
+__global__ void selftest_wait_timeout_kernel(uint32_t* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_mbar_init();
+  wait_or_abort_for(b, 0, &abort_flag, status, kSiteSelfTest, limit_ns);
+}
+
+}  // namespace fa2
+
+extern "C" int fa2_selftest_wait_timeout(int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return FA2_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc) return rc;
+  selftest_wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(ds->status,
+                                                                                (uint64_t)limit_us * 1000ull);
+  return cudaGetLastError() == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
 }
 
 extern "C" int fa2_get_device_status(void* stream, uint32_t* detail) {

@@ -24,23 +24,33 @@ enum WaitSite : uint32_t {
   kSiteSoftmaxO = 8,
   kSiteEpilogueO = 9,
   kSiteDrain = 10,
+  kSiteSelfTest = 11,
 };
 
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                              uint32_t* status, uint32_t site) {
+// Wait for the phase of `bar` with the given parity for at most `limit_ns`;
+// give up early if another role of the CTA has already given up.  On
+// expiry: raise the CTA's abort flag, record the site in the device status
+// word and return false (the caller then abandons its work and returns).
+__device__ __forceinline__ bool wait_or_abort_for(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                  uint32_t* status, uint32_t site, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 31u) == 0) {
       if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicOr(status, kStatusTimeout | (1u << (8 + site)));
         return false;
       }
     }
   }
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              uint32_t* status, uint32_t site) {
+  return wait_or_abort_for(bar, parity, abort_flag, status, site, kWaitLimitNs);
 }
 
 // Bounded wait that ignores the abort flag: used to let this CTA's own copies

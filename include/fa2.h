@@ -130,6 +130,20 @@ int fa2_fwd_host_noalloc(const void* q_host, const void* k_host, const void* v_h
  */
 int fa2_get_device_status(void* stream, uint32_t* detail);
 
+/*
+ * fa2_selftest_wait_timeout -- exercises the kernels' failure path without a
+ * GPU fault: launches one CTA whose single wait, made through the same
+ * bounded-wait routine every forward-kernel wait uses, is on an mbarrier that
+ * nothing ever completes.  After `limit_us` microseconds (1 .. 1e6) the wait
+ * gives up, records its site in the device status word and the kernel
+ * returns normally.  Asynchronous on `stream`; a following
+ * fa2_get_device_status returns FA2_ERR_DEVICE_TIMEOUT (detail bit 8 + 11)
+ * and clears the word.  No counterpart on the pages: it tests the library's
+ * own hang protection (FlashAttention V2 in depth describes no failure
+ * handling).
+ */
+int fa2_selftest_wait_timeout(int limit_us, void* stream);
+
 /* Static English description of a status code. */
 const char* fa2_status_string(int status);
 

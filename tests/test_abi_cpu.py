@@ -34,7 +34,7 @@ def _declared_functions():
 def test_header_declares_entry_points():
     names = _declared_functions()
     for required in ("fa2_fwd", "fa2_fwd_host", "fa2_fwd_host_workspace_bytes", "fa2_get_device_status",
-                     "fa2_status_string", "fa2_version"):
+                     "fa2_status_string", "fa2_version", "fa2_selftest_wait_timeout"):
         assert required in names
 
 
@@ -112,3 +112,8 @@ def test_host_entry_point_checks(lib):
     assert f(A, A, A, A, A, 6 * A + 16, ws, 1, 2, 64, 64, 0.125, 0, 0, None) == fa2.FA2_ERR_MISALIGNED
     assert f(0, A, A, A, A, 6 * A, ws, 1, 2, 64, 64, 0.125, 0, 0, None) == fa2.FA2_ERR_INVALID_ARG
     assert f(A, A, A, A, A, 6 * A, ws, 1, 2, 64, 64, 0.125, 0, 5, None) == fa2.FA2_ERR_INVALID_ARG
+
+
+def test_selftest_limit_checked(lib):
+    assert lib.fa2_selftest_wait_timeout(0, None) == fa2.FA2_ERR_INVALID_ARG
+    assert lib.fa2_selftest_wait_timeout(1000001, None) == fa2.FA2_ERR_INVALID_ARG
