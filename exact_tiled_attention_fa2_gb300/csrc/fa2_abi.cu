@@ -202,14 +202,25 @@ extern "C" size_t fa2_fwd_host_workspace_bytes(int B, int H, int N, int d) {
   return 4 * align256(elems * 2) + align256((size_t)B * H * (size_t)N * 4);
 }
 
-extern "C" int fa2_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host,
-                            float* lse_host, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
-                            float scale, int causal, int dtype, void* stream) {
+namespace fa2 {
+namespace {
+
+// Checks shared by the host-buffer entry points.
+int check_host_args(const void* q_host, const void* k_host, const void* v_host, const void* o_host,
+                    const float* lse_host, const void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                    float scale, int causal, int dtype) {
   int rc = check_shape(B, H, N, d, scale, causal, dtype);
   if (rc) return rc;
   if (!q_host || !k_host || !v_host || !o_host || !lse_host || !workspace) return FA2_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA2_ERR_MISALIGNED;
   if (workspace_bytes < fa2_fwd_host_workspace_bytes(B, H, N, d)) return FA2_ERR_INVALID_ARG;
+  return FA2_OK;
+}
+
+// Whole problem in one pass on `stream`: copy in, forward, copy out, synchronise.
+int host_forward_serial(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
+                        void* workspace, int B, int H, int N, int d, float scale, int causal, int dtype,
+                        void* stream) {
   const size_t elems = (size_t)B * H * (size_t)N * d;
   const size_t tb = elems * 2, lb = (size_t)B * H * (size_t)N * 4;
   uint8_t* w = static_cast<uint8_t*>(workspace);
@@ -223,12 +234,127 @@ extern "C" int fa2_fwd_host(const void* q_host, const void* k_host, const void* 
       cudaMemcpyAsync(kd, k_host, tb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(vd, v_host, tb, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return FA2_ERR_CUDA;
-  rc = fa2_fwd(qd, kd, vd, od, ld, B, H, N, d, scale, causal, dtype, stream);
+  int rc = fa2_fwd(qd, kd, vd, od, ld, B, H, N, d, scale, causal, dtype, stream);
   if (rc) return rc;
   if (cudaMemcpyAsync(o_host, od, tb, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaMemcpyAsync(lse_host, ld, lb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return FA2_ERR_CUDA;
   return fa2_get_device_status(stream, nullptr);
+}
+
+// Library-owned copy streams and events of one device for the pipelined host
+// path, created on first use and kept until exit.  The mutex serialises
+// pipelined calls on the device (they share the streams and events).
+constexpr int kMaxChunks = 4;
+constexpr size_t kPipelineMinBytes = (size_t)48 << 20;
+
+struct CopyEngines {
+  bool ready = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t entry = nullptr, in_done[kMaxChunks], fwd_done[kMaxChunks], out_done[kMaxChunks];
+  std::mutex busy;
+};
+CopyEngines g_copy[kMaxDevices];
+
+int copy_engines(CopyEngines** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA2_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA2_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  CopyEngines& c = g_copy[dev];
+  if (!c.ready) {
+    const unsigned f = cudaEventDisableTiming;
+    if (cudaStreamCreateWithFlags(&c.h2d, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&c.d2h, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c.entry, f) != cudaSuccess)
+      return FA2_ERR_CUDA;
+    for (int i = 0; i < kMaxChunks; ++i) {
+      if (cudaEventCreateWithFlags(&c.in_done[i], f) != cudaSuccess ||
+          cudaEventCreateWithFlags(&c.fwd_done[i], f) != cudaSuccess ||
+          cudaEventCreateWithFlags(&c.out_done[i], f) != cudaSuccess)
+        return FA2_ERR_CUDA;
+    }
+    c.ready = true;
+  }
+  *out = &c;
+  return FA2_OK;
+}
+
+// The (b,h) slices are independent, so the problem is cut into up to
+// kMaxChunks groups of heads: the copy-in of group c+1 (one stream) and the
+// copy-out of group c-1 (another) run while the forward pass of group c runs
+// on `stream`.
+int host_forward_pipelined(const void* q_host, const void* k_host, const void* v_host, void* o_host,
+                           float* lse_host, void* workspace, int B, int H, int N, int d, float scale, int causal,
+                           int dtype, void* stream) {
+  const int bh = B * H;
+  const size_t head_elems = (size_t)N * d;
+  const size_t tb = (size_t)bh * head_elems * 2;
+  if (3 * tb < kPipelineMinBytes || bh < 2)
+    return host_forward_serial(q_host, k_host, v_host, o_host, lse_host, workspace, B, H, N, d, scale, causal,
+                               dtype, stream);
+  CopyEngines* ce = nullptr;
+  int rc = copy_engines(&ce);
+  if (rc) return rc;
+  std::lock_guard<std::mutex> busy(ce->busy);
+  const int chunks = bh < kMaxChunks ? bh : kMaxChunks;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  uint8_t* qd = w;
+  uint8_t* kd = w + align256(tb);
+  uint8_t* vd = w + 2 * align256(tb);
+  uint8_t* od = w + 3 * align256(tb);
+  float* ld = reinterpret_cast<float*>(w + 4 * align256(tb));
+  const uint8_t* qh = static_cast<const uint8_t*>(q_host);
+  const uint8_t* kh = static_cast<const uint8_t*>(k_host);
+  const uint8_t* vh = static_cast<const uint8_t*>(v_host);
+  uint8_t* oh = static_cast<uint8_t*>(o_host);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool ok = cudaEventRecord(ce->entry, s) == cudaSuccess &&
+            cudaStreamWaitEvent(ce->h2d, ce->entry, 0) == cudaSuccess;
+  // copy-in of every group, in order, on the copy-in stream
+  for (int c = 0; c < chunks && ok; ++c) {
+    const int h0 = (int)((long long)bh * c / chunks), h1 = (int)((long long)bh * (c + 1) / chunks);
+    const size_t off = (size_t)h0 * head_elems * 2, bytes = (size_t)(h1 - h0) * head_elems * 2;
+    ok = cudaMemcpyAsync(qd + off, qh + off, bytes, cudaMemcpyHostToDevice, ce->h2d) == cudaSuccess &&
+         cudaMemcpyAsync(kd + off, kh + off, bytes, cudaMemcpyHostToDevice, ce->h2d) == cudaSuccess &&
+         cudaMemcpyAsync(vd + off, vh + off, bytes, cudaMemcpyHostToDevice, ce->h2d) == cudaSuccess &&
+         cudaEventRecord(ce->in_done[c], ce->h2d) == cudaSuccess;
+  }
+  // forward of each group once its inputs landed; copy-out once it finished
+  for (int c = 0; c < chunks && ok; ++c) {
+    const int h0 = (int)((long long)bh * c / chunks), h1 = (int)((long long)bh * (c + 1) / chunks);
+    const size_t off = (size_t)h0 * head_elems * 2, bytes = (size_t)(h1 - h0) * head_elems * 2;
+    ok = cudaStreamWaitEvent(s, ce->in_done[c], 0) == cudaSuccess;
+    if (!ok) break;
+    rc = fa2_fwd(qd + off, kd + off, vd + off, od + off, ld + (size_t)h0 * N, 1, h1 - h0, N, d, scale, causal,
+                 dtype, stream);
+    if (rc) break;
+    ok = cudaEventRecord(ce->fwd_done[c], s) == cudaSuccess &&
+         cudaStreamWaitEvent(ce->d2h, ce->fwd_done[c], 0) == cudaSuccess &&
+         cudaMemcpyAsync(oh + off, od + off, bytes, cudaMemcpyDeviceToHost, ce->d2h) == cudaSuccess &&
+         cudaMemcpyAsync(lse_host + (size_t)h0 * N, ld + (size_t)h0 * N, (size_t)(h1 - h0) * N * 4,
+                         cudaMemcpyDeviceToHost, ce->d2h) == cudaSuccess &&
+         cudaEventRecord(ce->out_done[c], ce->d2h) == cudaSuccess;
+  }
+  if (ok && rc == FA2_OK) ok = cudaStreamWaitEvent(s, ce->out_done[chunks - 1], 0) == cudaSuccess;
+  // whatever happened, nothing of this call may still be in flight on return
+  const bool drained = cudaStreamSynchronize(ce->h2d) == cudaSuccess && cudaStreamSynchronize(ce->d2h) == cudaSuccess;
+  if (rc) return rc;
+  if (!ok || !drained) return FA2_ERR_CUDA;
+  return fa2_get_device_status(stream, nullptr);
+}
+
+}  // namespace
+}  // namespace fa2
+
+extern "C" int fa2_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host,
+                            float* lse_host, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                            float scale, int causal, int dtype, void* stream) {
+  int rc = check_host_args(q_host, k_host, v_host, o_host, lse_host, workspace, workspace_bytes, B, H, N, d, scale,
+                           causal, dtype);
+  if (rc) return rc;
+  return host_forward_pipelined(q_host, k_host, v_host, o_host, lse_host, workspace, B, H, N, d, scale, causal,
+                                dtype, stream);
 }
 
 namespace fa2 {
@@ -273,8 +399,8 @@ extern "C" int fa2_fwd_host_noalloc(const void* q_host, const void* k_host, cons
   void* scratch = nullptr;
   rc = noalloc_scratch(&scratch);
   if (rc) return rc;
-  return fa2_fwd_host(q_host, k_host, v_host, o_host, lse_host, scratch, FA2_NOALLOC_SCRATCH_BYTES, B, H, N, d,
-                      scale, causal, dtype, stream);
+  return host_forward_serial(q_host, k_host, v_host, o_host, lse_host, scratch, B, H, N, d, scale, causal, dtype,
+                             stream);
 }
 
 namespace fa2 {

@@ -76,10 +76,17 @@ int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *
  * Copies q, k, v (host, [B,H,N,d] `dtype`; pinned memory gives full copy
  * bandwidth) into the caller's device workspace, runs fa2_fwd on `stream`,
- * copies o and lse back into the host buffers and synchronises `stream`
- * before returning.  `workspace` is a device buffer of at least
+ * copies o and lse back into the host buffers and synchronises before
+ * returning.  `workspace` is a device buffer of at least
  * fa2_fwd_host_workspace_bytes(B,H,N,d) bytes, 256-byte aligned, owned by the
  * caller.  Returns FA2_ERR_DEVICE_TIMEOUT if a kernel wait timed out.
+ *
+ * Problems with at least 48 MB of input are cut into up to 4 groups of
+ * (b,h) slices: the copy-in of the next group and the copy-out of the
+ * previous one run on two copy streams the library creates once per device
+ * while the forward pass of the current group runs on `stream` (which first
+ * waits for work already queued on it).  Such calls on one device are
+ * serialised by the library.  Results are identical to the unsplit pass.
  */
 int fa2_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host,
                  float* lse_host, void* workspace, size_t workspace_bytes,

@@ -204,6 +204,7 @@ def test_outputs_written_in_place_only():
 
 
 def test_side_stream_and_host_entry_point():
+    # small problem: the host path runs copy-in, forward and copy-out in one pass
     B, H, N, d = 2, 2, 333, 64
     q, k, v = sy.make_qkv(B, H, N, d, sy.BF16, 78)
     s = torch.cuda.Stream()
@@ -248,3 +249,20 @@ def test_repeated_launches_identical(d, dtype, causal, N):
             assert torch.equal(o, o0) and torch.equal(lse, l0), "launch %d differs" % i
     code, detail = fa2.fa2_get_device_status()
     assert code == fa2.FA2_OK, "a wait timed out (0x%x)" % detail
+
+
+def test_host_entry_point_pipelined_over_head_groups():
+    # >= 48 MB of input: the host path overlaps copies of one group of heads with the forward of another
+    B, H, N, d = 1, 16, 8192, 64
+    q, k, v = sy.make_qkv(B, H, N, d, sy.FP16, 79)
+    o_d, l_d = fa2.fa2_fwd(to_dev(q, sy.FP16), to_dev(k, sy.FP16), to_dev(v, sy.FP16), causal=True)
+    torch.cuda.synchronize()
+    qh, kh, vh = (torch.from_numpy(x.view(np.int16)).view(torch.float16).pin_memory() for x in (q, k, v))
+    oh = torch.empty((B, H, N, d), dtype=torch.float16).pin_memory()
+    lh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    ws = torch.empty(fa2.fa2_fwd_host_workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        oh.zero_()
+        lh.zero_()
+        fa2.fa2_fwd_host(qh, kh, vh, oh, lh, ws, causal=True)
+        assert torch.equal(oh, o_d.cpu()) and torch.equal(lh, l_d.cpu())
