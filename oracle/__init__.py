@@ -57,6 +57,14 @@ def _load():
         lib.oracle_attention_fwd.restype = ctypes.c_int
         lib.oracle_widen.argtypes = [p16, ctypes.c_int, i64, pd]
         lib.oracle_widen.restype = ctypes.c_int
+        lib.oracle_attention_fwd_f64.argtypes = [pd, pd, pd, i64, i64, i64, i64, ctypes.c_double, ctypes.c_int, pd, pd]
+        lib.oracle_attention_fwd_f64.restype = ctypes.c_int
+        lib.oracle_attention_bwd_f64.argtypes = [pd, pd, pd, pd, i64, i64, i64, i64, ctypes.c_double, ctypes.c_int,
+                                                 pd, pd, pd, pd, ctypes.c_int]
+        lib.oracle_attention_bwd_f64.restype = ctypes.c_int
+        lib.oracle_attention_bwd.argtypes = [p16, p16, p16, p16, ctypes.c_int, i64, i64, i64, i64, ctypes.c_double,
+                                             ctypes.c_int, pd, pd, pd, pd, ctypes.c_int]
+        lib.oracle_attention_bwd.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -123,3 +131,52 @@ def attention_rows(q, k, v, dtype: int, scale: float, causal: bool, bh_idx, row_
     if rc:
         raise ValueError("oracle_attention_rows failed (%d)" % rc)
     return o, lse
+
+
+def _f64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def attention_fwd_f64(q, k, v, scale: float, causal: bool):
+    """Forward on float64 inputs [B,H,N,d]: (O, L) by the same definition."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, N, d = q.shape
+    o = np.empty((B, H, N, d))
+    lse = np.empty((B, H, N))
+    rc = _load().oracle_attention_fwd_f64(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
+                                          _ptr(v, ctypes.c_double), B, H, N, d, float(scale), int(bool(causal)),
+                                          _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double))
+    if rc:
+        raise ValueError("oracle_attention_fwd_f64 failed (%d)" % rc)
+    return o, lse
+
+
+def attention_bwd_f64(q, k, v, dout, scale: float, causal: bool, threads: int = 0):
+    """Gradients (dQ, dK, dV, D) of the forward pass for upstream dO, float64 inputs [B,H,N,d]."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, H, N, d = q.shape
+    dq, dk, dv = (np.empty((B, H, N, d)) for _ in range(3))
+    delta = np.empty((B, H, N))
+    rc = _load().oracle_attention_bwd_f64(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
+                                          _ptr(v, ctypes.c_double), _ptr(dout, ctypes.c_double), B, H, N, d,
+                                          float(scale), int(bool(causal)), _ptr(dq, ctypes.c_double),
+                                          _ptr(dk, ctypes.c_double), _ptr(dv, ctypes.c_double),
+                                          _ptr(delta, ctypes.c_double), int(threads))
+    if rc:
+        raise ValueError("oracle_attention_bwd_f64 failed (%d)" % rc)
+    return dq, dk, dv, delta
+
+
+def attention_bwd(q, k, v, dout, dtype: int, scale: float, causal: bool, threads: int = 0):
+    """Gradients (dQ, dK, dV, D) from 16-bit bit patterns [B,H,N,d], float64 results."""
+    q, k, v, dout = _bits(q), _bits(k), _bits(v), _bits(dout)
+    B, H, N, d = q.shape
+    dq, dk, dv = (np.empty((B, H, N, d)) for _ in range(3))
+    delta = np.empty((B, H, N))
+    rc = _load().oracle_attention_bwd(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16), _ptr(v, ctypes.c_uint16),
+                                      _ptr(dout, ctypes.c_uint16), int(dtype), B, H, N, d, float(scale),
+                                      int(bool(causal)), _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double),
+                                      _ptr(dv, ctypes.c_double), _ptr(delta, ctypes.c_double), int(threads))
+    if rc:
+        raise ValueError("oracle_attention_bwd failed (%d)" % rc)
+    return dq, dk, dv, delta

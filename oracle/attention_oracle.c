@@ -34,6 +34,22 @@
  * Attention 2 page, the one-row practice of Lesson 6.6, closed forms and
  * invariants (row sums, identical keys, single key, constant values, causal
  * row 0) and a high-precision brute force on tiny inputs.
+ *
+ * Backward (the gradients of the forward pass for an upstream gradient dO,
+ * FlashAttention V2 in depth section 7 and Lesson 6.6 "Recomputation in the
+ * backward pass"), per (b, h), by the definition of the softmax Jacobian:
+ *
+ *   P   = softmax_row(S) as above (visible keys only)
+ *   dV  = P^T dO
+ *   dP  = dO V^T
+ *   D_i = sum_j P_ij dP_ij          (section 7.3 shows it equals rowsum(dO o O))
+ *   dS  = P o (dP - D)              (o: elementwise)
+ *   dQ  = scale dS K,   dK = scale dS^T Q
+ *
+ * Rows are done first (P row, dP row, D_i, dQ_i), then keys (dK_j, dV_j
+ * summed over the rows that see key j, with P_ij and dS_ij rebuilt from the
+ * row statistics of the first pass).  Pinned by central finite differences
+ * of the forward definition, the identity of section 7.3 and invariants.
  */
 #include <math.h>
 #include <stdint.h>
@@ -212,6 +228,146 @@ int oracle_attention_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v
     free(bh_idx);
     free(row_idx);
     return rc;
+}
+
+/* ------------------------------------------------------------------ fp64 inputs */
+
+static int check_args_f64(const double* q, const double* k, const double* v, int64_t B, int64_t H, int64_t N,
+                          int64_t d, double scale) {
+  if (!q || !k || !v || B < 1 || H < 1 || N < 1 || d < 1 || !isfinite(scale)) return ORACLE_ERR_ARG;
+  return ORACLE_OK;
+}
+
+/* Forward on fp64 inputs [B,H,N,d] (same definition as oracle_attention_fwd). */
+int oracle_attention_fwd_f64(const double* q, const double* k, const double* v, int64_t B, int64_t H, int64_t N,
+                             int64_t d, double scale, int causal, double* o_out, double* lse_out) {
+  if (check_args_f64(q, k, v, B, H, N, d, scale) || !o_out || !lse_out) return ORACLE_ERR_ARG;
+  double* srow = (double*)malloc(sizeof(double) * (size_t)N);
+  if (!srow) return ORACLE_ERR_NOMEM;
+  for (int64_t bh = 0; bh < B * H; ++bh)
+    for (int64_t i = 0; i < N; ++i)
+      attention_row(q + (bh * N + i) * d, k + bh * N * d, v + bh * N * d, N, d, scale, causal, i, srow,
+                    o_out + (bh * N + i) * d, lse_out + bh * N + i);
+  free(srow);
+  return ORACLE_OK;
+}
+
+/* Backward of one (b,h) slice: q, k, v, dout are N x d; writes dq, dk, dv
+ * (N x d) and delta (N). */
+static int attention_bwd_slice(const double* q, const double* k, const double* v, const double* dout, int64_t N,
+                               int64_t d, double scale, int causal, double* dq, double* dk, double* dv,
+                               double* delta) {
+  double* m = (double*)malloc(sizeof(double) * (size_t)N);
+  double* l = (double*)malloc(sizeof(double) * (size_t)N);
+  if (!m || !l) { free(m); free(l); return ORACLE_ERR_NOMEM; }
+  int nomem = 0;
+  /* rows: P_i, dP_i, D_i, dS_i, dQ_i */
+#pragma omp parallel reduction(| : nomem)
+  {
+    double* p = (double*)malloc(sizeof(double) * (size_t)N);
+    double* dp = (double*)malloc(sizeof(double) * (size_t)N);
+    if (!p || !dp) {
+      nomem = 1;
+    } else {
+#pragma omp for schedule(dynamic, 4)
+      for (int64_t i = 0; i < N; ++i) {
+        const int64_t nvis = causal ? (i + 1 < N ? i + 1 : N) : N;
+        const double* qi = q + i * d;
+        const double* doi = dout + i * d;
+        double mi = -INFINITY;
+        for (int64_t j = 0; j < nvis; ++j) {
+          double acc = 0.0;
+          for (int64_t c = 0; c < d; ++c) acc += qi[c] * k[j * d + c];
+          p[j] = scale * acc;
+          if (p[j] > mi) mi = p[j];
+        }
+        double li = 0.0;
+        for (int64_t j = 0; j < nvis; ++j) { p[j] = exp(p[j] - mi); li += p[j]; }
+        for (int64_t j = 0; j < nvis; ++j) p[j] /= li;
+        double di = 0.0;
+        for (int64_t j = 0; j < nvis; ++j) {
+          double acc = 0.0;
+          for (int64_t c = 0; c < d; ++c) acc += doi[c] * v[j * d + c];
+          dp[j] = acc;
+          di += p[j] * dp[j];
+        }
+        for (int64_t c = 0; c < d; ++c) dq[i * d + c] = 0.0;
+        for (int64_t j = 0; j < nvis; ++j) {
+          const double ds = p[j] * (dp[j] - di);
+          for (int64_t c = 0; c < d; ++c) dq[i * d + c] += scale * ds * k[j * d + c];
+        }
+        m[i] = mi;
+        l[i] = li;
+        delta[i] = di;
+      }
+    }
+    free(p);
+    free(dp);
+  }
+  if (nomem) { free(m); free(l); return ORACLE_ERR_NOMEM; }
+  /* keys: dK_j, dV_j over the rows that see key j */
+#pragma omp parallel for schedule(dynamic, 4)
+  for (int64_t j = 0; j < N; ++j) {
+    for (int64_t c = 0; c < d; ++c) { dk[j * d + c] = 0.0; dv[j * d + c] = 0.0; }
+    for (int64_t i = causal ? j : 0; i < N; ++i) {
+      double s = 0.0, dpij = 0.0;
+      for (int64_t c = 0; c < d; ++c) {
+        s += q[i * d + c] * k[j * d + c];
+        dpij += dout[i * d + c] * v[j * d + c];
+      }
+      const double pij = exp(scale * s - m[i]) / l[i];
+      const double ds = pij * (dpij - delta[i]);
+      for (int64_t c = 0; c < d; ++c) {
+        dv[j * d + c] += pij * dout[i * d + c];
+        dk[j * d + c] += scale * ds * q[i * d + c];
+      }
+    }
+  }
+  free(m);
+  free(l);
+  return ORACLE_OK;
+}
+
+/* Backward on fp64 inputs [B,H,N,d]; outputs dq, dk, dv [B,H,N,d] and
+ * delta [B,H,N] (D_i = sum_j P_ij dP_ij). */
+int oracle_attention_bwd_f64(const double* q, const double* k, const double* v, const double* dout, int64_t B,
+                             int64_t H, int64_t N, int64_t d, double scale, int causal, double* dq, double* dk,
+                             double* dv, double* delta, int threads) {
+  if (check_args_f64(q, k, v, B, H, N, d, scale) || !dout || !dq || !dk || !dv || !delta) return ORACLE_ERR_ARG;
+#ifdef _OPENMP
+  if (threads > 0) omp_set_num_threads(threads);
+#else
+  (void)threads;
+#endif
+  for (int64_t bh = 0; bh < B * H; ++bh) {
+    const int64_t off = bh * N * d;
+    int rc = attention_bwd_slice(q + off, k + off, v + off, dout + off, N, d, scale, causal, dq + off, dk + off,
+                                 dv + off, delta + bh * N);
+    if (rc) return rc;
+  }
+  return ORACLE_OK;
+}
+
+/* Backward on 16-bit inputs (widened exactly first). */
+int oracle_attention_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout, int dtype,
+                         int64_t B, int64_t H, int64_t N, int64_t d, double scale, int causal, double* dq,
+                         double* dk, double* dv, double* delta, int threads) {
+  int rc = check_args(q, k, v, dtype, B, H, N, d, scale);
+  if (rc) return rc;
+  if (!dout) return ORACLE_ERR_ARG;
+  const int64_t n = B * H * N * d;
+  double* buf = (double*)malloc(sizeof(double) * (size_t)(4 * n));
+  if (!buf) return ORACLE_ERR_NOMEM;
+  for (int64_t x = 0; x < n; ++x) {
+    buf[x] = widen(q[x], dtype);
+    buf[n + x] = widen(k[x], dtype);
+    buf[2 * n + x] = widen(v[x], dtype);
+    buf[3 * n + x] = widen(dout[x], dtype);
+  }
+  rc = oracle_attention_bwd_f64(buf, buf + n, buf + 2 * n, buf + 3 * n, B, H, N, d, scale, causal, dq, dk, dv,
+                                delta, threads);
+  free(buf);
+  return rc;
 }
 
 /* Threads OpenMP will use (1 without OpenMP); reported by the CPU baseline. */
