@@ -239,6 +239,8 @@ def main():
     ap.add_argument("--kernel-only", action="store_true", help="skip the end-to-end and CPU-baseline legs")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps one by one instead of replaying them from a CUDA graph")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (fa2_bwd) instead: 2.5x the forward FLOPs (five products)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -275,6 +277,18 @@ def main():
 
     def step():
         fa2.fa2_fwd(q, k, v, o, lse, scale=w.scale, causal=w.causal, stream=stream)
+
+    if args.backward:
+        with torch.cuda.stream(stream):
+            step()
+        stream.synchronize()
+        dout = torch.from_numpy(sy.make_qkv(w.B, w.H, w.N, w.d, w.dtype, w.seed(0) + 500)[0].view(np.int16)).view(
+            tdt).to(dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+        bws = torch.empty(fa2.fa2_bwd_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
+
+        def step():  # noqa: F811 -- the backward pass replaces the forward as the timed step
+            fa2.fa2_bwd(q, k, v, o, lse, dout, dq, dk, dv, bws, scale=w.scale, causal=w.causal, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -325,7 +339,7 @@ def main():
     if dist is not None:
         dist.barrier()
 
-    flops = w.flops()
+    flops = w.flops() * (2.5 if args.backward else 1.0)
     value = job_throughput(flops, args.steps, ws, max_ms)
     avg_launch_ms = sum(kernel_ms) / len(kernel_ms)
     achieved = flops / (avg_launch_ms / 1e3) / 1e12
@@ -333,7 +347,7 @@ def main():
 
     e2e = None
     cpu = None
-    if rank == 0 and not args.kernel_only:
+    if rank == 0 and not args.kernel_only and not args.backward:
         # end to end through the host-buffer entry point: H2D of q, k, v and D2H of o, lse each step
         qh, kh, vh = (h.pin_memory() for h in host)
         oh = torch.empty(q.shape, dtype=tdt).pin_memory()
@@ -361,20 +375,23 @@ def main():
     if rank == 0:
         clk = clocks.summary()
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "metric": METRIC if not args.backward else
+            "backward attention TFLOP/s at 1 GB300 (2.5x the forward FLOPs) and % of dense FP16/BF16 tensor peak",
+            "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == sy.BF16 else "fp16",
             "data": "synthetic", "config": dict(workload_config(w, ws), launch=launch_mode(args)),
             "pct_of_peak": 100.0 * value / ws / peak,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                          "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
-                         "peak_source": peak_note, "kernel": "fa2_fwd_pingpong_kernel" if w.d <= 128 else "fa2_fwd_dbuf_kernel",
+                         "peak_source": peak_note, "kernel": ("fa2_bwd_kernel" if args.backward else
+                                    "fa2_fwd_pingpong_kernel" if w.d <= 128 else "fa2_fwd_dbuf_kernel"),
                          "avg_launch_ms": avg_launch_ms,
                          "algorithmic_flops_per_launch": flops,
-                         "algorithmic_bytes_per_launch": w.algorithmic_bytes()},
+                         "algorithmic_bytes_per_launch": w.algorithmic_bytes() * (2 if args.backward else 1)},
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                        "samples": clk["samples"]},
-            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": args.steps,
+            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": args.steps * (3 if args.backward else 1),
             "kernel_sha": kernel_source_hash(),
         }
         print(json.dumps(line), flush=True)

@@ -54,6 +54,10 @@ def load_library():
     lib.fa2_fwd_host_workspace_bytes.restype = sz
     lib.fa2_fwd_host_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, ci, vp]
     lib.fa2_fwd_host_noalloc.restype = ci
+    lib.fa2_bwd.argtypes = [vp] * 9 + [vp, sz, ci, ci, ci, ci, cf, ci, ci, vp]
+    lib.fa2_bwd.restype = ci
+    lib.fa2_bwd_workspace_bytes.argtypes = [ci, ci, ci, ci]
+    lib.fa2_bwd_workspace_bytes.restype = sz
     lib.fa2_selftest_wait_timeout.argtypes = [ci, vp]
     lib.fa2_selftest_wait_timeout.restype = ci
     lib.fa2_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
@@ -119,6 +123,34 @@ def fa2_fwd(q, k, v, o=None, lse=None, scale=None, causal=False, stream=None):
     if rc:
         raise Fa2Error(rc, "fa2_fwd")
     return o, lse
+
+
+def fa2_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load_library().fa2_bwd_workspace_bytes(B, H, N, d))
+
+
+def fa2_bwd(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, workspace=None, scale=None, causal=False,
+            stream=None):
+    """Gradients (dq, dk, dv) of fa2_fwd for the upstream gradient dout (CUDA tensors, d = 64 or 128)."""
+    import torch
+    for t in (q, k, v, o, dout):
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == q.dtype and t.shape == q.shape):
+            raise ValueError("q, k, v, o, dout must be contiguous CUDA tensors of one shape and dtype")
+    B, H, N, d = q.shape
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(fa2_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=q.device)
+    if scale is None:
+        scale = 1.0 / float(d) ** 0.5
+    rc = load_library().fa2_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                 dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+                                 workspace.numel() * workspace.element_size(), B, H, N, d, float(scale),
+                                 int(bool(causal)), _dtype_code(q), _stream_handle(stream, q.device))
+    if rc:
+        raise Fa2Error(rc, "fa2_bwd")
+    return dq, dk, dv
 
 
 def fa2_fwd_host_workspace_bytes(B: int, H: int, N: int, d: int) -> int:

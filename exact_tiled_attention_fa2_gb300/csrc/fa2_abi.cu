@@ -245,7 +245,7 @@ int host_forward_serial(const void* q_host, const void* k_host, const void* v_ho
 // Library-owned copy streams and events of one device for the pipelined host
 // path, created on first use and kept until exit.  The mutex serialises
 // pipelined calls on the device (they share the streams and events).
-constexpr int kMaxChunks = 4;
+constexpr int kMaxChunks = 8;
 constexpr size_t kPipelineMinBytes = (size_t)48 << 20;
 
 struct CopyEngines {
@@ -420,6 +420,70 @@ __global__ void selftest_wait_timeout_kernel(uint32_t* status, uint64_t limit_ns
 }
 
 }  // namespace fa2
+
+extern "C" size_t fa2_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+  const size_t rows = (size_t)B * H * (size_t)N;
+  return align256(rows * (size_t)d * 4) + align256(rows * 4);
+}
+
+extern "C" int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                       void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N,
+                       int d, float scale, int causal, int dtype, void* stream) {
+  int rc = check_shape(B, H, N, d, scale, causal, dtype);
+  if (rc) return rc;
+  if (d != 64 && d != 128) return FA2_ERR_UNSUPPORTED;
+  const void* ptrs[11] = {q, k, v, o, lse, dout, dq, dk, dv, workspace, nullptr};
+  for (int i = 0; i < 10; ++i)
+    if (!ptrs[i]) return FA2_ERR_INVALID_ARG;
+  for (int i = 0; i < 10; ++i)
+    if (misaligned(ptrs[i])) return FA2_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA2_ERR_MISALIGNED;
+  if (workspace_bytes < fa2_bwd_workspace_bytes(B, H, N, d)) return FA2_ERR_INVALID_ARG;
+  const size_t rows = (size_t)B * H * (size_t)N;
+  const size_t tb = rows * (size_t)d * 2, lb = rows * 4, wb = fa2_bwd_workspace_bytes(B, H, N, d);
+  // every written buffer (dq, dk, dv, workspace) overlaps no input and no other output
+  const void* outs[4] = {dq, dk, dv, workspace};
+  const size_t out_bytes[4] = {tb, tb, tb, wb};
+  const void* ins[6] = {q, k, v, o, lse, dout};
+  const size_t in_bytes[6] = {tb, tb, tb, tb, lb, tb};
+  for (int a = 0; a < 4; ++a) {
+    for (int b = 0; b < 6; ++b)
+      if (ranges_overlap(outs[a], out_bytes[a], ins[b], in_bytes[b])) return FA2_ERR_INVALID_ARG;
+    for (int b = a + 1; b < 4; ++b)
+      if (ranges_overlap(outs[a], out_bytes[a], outs[b], out_bytes[b])) return FA2_ERR_INVALID_ARG;
+  }
+  DeviceState* ds = nullptr;
+  rc = device_state(&ds);
+  if (rc) return rc;
+  const bool bf16 = dtype == FA2_BF16;
+  const int bh = B * H;
+  BwdLaunchArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (encode_map(&a.tm_q, q, bh, N, d, 128, bf16) || encode_map(&a.tm_k, k, bh, N, d, 128, bf16) ||
+      encode_map(&a.tm_v, v, bh, N, d, 128, bf16) || encode_map(&a.tm_do, dout, bh, N, d, 128, bf16))
+    return FA2_ERR_CUDA;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  a.p.dq_accum = reinterpret_cast<float*>(w);
+  a.p.delta = reinterpret_cast<float*>(w + align256(rows * (size_t)d * 4));
+  a.p.lse = lse;
+  a.p.dk = dk;
+  a.p.dv = dv;
+  a.p.status = ds->status;
+  a.p.n = N;
+  a.p.bh = bh;
+  a.p.num_tiles = (N + 127) / 128;
+  a.p.scale = scale;
+  a.p.scale_log2 = scale * 1.4426950408889634f;
+  a.o = o;
+  a.dout = dout;
+  a.dq = dq;
+  a.bf16 = bf16;
+  a.causal = causal != 0;
+  a.stream = static_cast<cudaStream_t>(stream);
+  const int e = (d == 64) ? launch_bwd_d64(a) : launch_bwd_d128(a);
+  return e == 0 ? FA2_OK : FA2_ERR_CUDA;
+}
 
 extern "C" int fa2_selftest_wait_timeout(int limit_us, void* stream) {
   if (limit_us < 1 || limit_us > 1000000) return FA2_ERR_INVALID_ARG;

@@ -1,0 +1,459 @@
+// fa2_bwd.cuh -- backward pass of the exact attention forward (head dims 64 and 128).
+//
+// Gradients for an upstream dO (FlashAttention V2 in depth, section 7):
+//
+//   P   = exp(scale S - L)          S = Q K^T, L the forward logsumexp (7.1)
+//   dV  = P^T dO,   dP = dO V^T,    D_i = rowsum(dO_i o O_i)          (7.3)
+//   dS  = P o (dP - D),   dQ = scale dS K,   dK = scale dS^T Q
+//
+// Three kernels:
+//   preprocess  D_i = rowsum(dO_i o O_i) in fp32 (its own pass over dO and
+//               O, as section 7.3 describes) and zeroes the fp32 dQ accumulator;
+//   main        key/value-outer (section 7.2): a CTA owns 128 keys of one
+//               (b, h), keeps dK_j and dV_j in tensor memory and walks the
+//               query tiles that see those keys; each tile's dQ contribution
+//               is added to the fp32 accumulator with vector atomics;
+//   convert     dQ accumulator -> 16-bit dQ.
+//
+// Main kernel, per query tile i (tensor memory holds S^T and dP^T with keys on
+// the 128 lanes, so one thread owns one key row):
+//   S^T  = K_j Q_i^T              tcgen05.mma, A = K_j, B = Q_i (smem, K-major)
+//   dP^T = V_j dO_i^T             tcgen05.mma, A = V_j, B = dO_i
+//   P^T, dS^T (16-bit)            elementwise warpgroups, written back to TMEM,
+//                                 dS^T also to shared memory
+//   dV  += P^T dO_i               A = P^T from TMEM, B = dO_i (MN-major)
+//   dK  += dS^T Q_i               A = dS^T from TMEM, B = Q_i (MN-major)
+//   dQ_i = dS K_j                 A = dS from smem (MN-major), B = K_j (MN-major),
+//                                 into the dP^T columns, then atomically added
+//
+// Warp roles (384 threads): warps 0-3 and 4-7 are two elementwise warpgroups,
+// each for 64 of the tile's 128 query columns (and half of the d columns of
+// dQ, dK, dV); warp 8 owns TMEM and issues every MMA; warp 9 drives TMA.
+// Every mbarrier wait is bounded (fa2_common.cuh), and each barrier is waited
+// phase by phase, never more than one phase away from its waiter.
+#pragma once
+
+#include "fa2_fwd_pingpong.cuh"
+
+namespace fa2 {
+
+template <int D_>
+struct BwdConfig {
+  static constexpr int D = D_;
+  static constexpr int T = 128;                 // rows of a query or key tile
+  static constexpr int THREADS = 384;
+  static constexpr int MMA_WARP = 8;
+  static constexpr int TMA_WARP = 9;
+  static constexpr uint32_t TILE_BYTES = T * D * 2;
+  static constexpr uint32_t DS_BYTES = T * T * 2;    // dS^T, keys x queries, 16-bit
+  static constexpr uint32_t OFF_K = 0;
+  static constexpr uint32_t OFF_V = OFF_K + TILE_BYTES;
+  static constexpr uint32_t OFF_Q = OFF_V + TILE_BYTES;
+  static constexpr uint32_t OFF_DO = OFF_Q + TILE_BYTES;
+  static constexpr uint32_t OFF_DS = OFF_DO + TILE_BYTES;
+  static constexpr uint32_t OFF_LD = OFF_DS + DS_BYTES;   // per elementwise warp: 64 x L*log2e, 64 x D
+  static constexpr uint32_t OFF_BAR = OFF_LD + 8 * 512;
+  static constexpr uint32_t NUM_BARS = 16;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
+  static constexpr uint32_t TMEM_DV = 0;
+  static constexpr uint32_t TMEM_DK = 128;
+  static constexpr uint32_t TMEM_S = 256;       // S^T, then P^T in its first 32 columns of each half
+  static constexpr uint32_t TMEM_DP = 384;      // dP^T, then dS^T, then the dQ_i contribution
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(D == 64 || D == 128, "backward kernel: head dim 64 or 128");
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+};
+
+enum : int {
+  BB_KV = 0,
+  BB_Q = 1,        // Q_i and dO_i landed
+  BB_QEMPTY = 2,   // every MMA reading Q_i / dO_i / dS finished
+  BB_S = 3,
+  BB_DP = 4,
+  BB_P = 5,        // P^T, dS^T written (8 warp arrivals)
+  BB_DQ = 6,
+  BB_DQEMPTY = 7,  // dQ_i read out of TMEM (8 warp arrivals)
+  BB_END = 8,
+  BB_EXIT = 9,
+};
+
+struct BwdCtx {
+  uint32_t bar0, sK, sV, sQ, sDO, sDS, tmem;
+  volatile int* abort_flag;
+  uint32_t* status;
+  int bh, n, j0, i0, niter;   // key tile start row, first query tile, number of query tiles
+  __device__ __forceinline__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
+};
+
+template <class C>
+__device__ __forceinline__ void bwd_producer(const BwdCtx& t, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                                             const CUtensorMap* tm_v, const CUtensorMap* tm_do) {
+  mbar_arrive_expect_tx(t.bar(BB_KV), 2 * C::TILE_BYTES);
+  for (int kb = 0; kb < C::D / 64; ++kb) {
+    tma_load_3d(t.sK + kb * (C::T * 128), tm_k, kb * 64, t.j0, t.bh, t.bar(BB_KV));
+    tma_load_3d(t.sV + kb * (C::T * 128), tm_v, kb * 64, t.j0, t.bh, t.bar(BB_KV));
+  }
+  int loaded = 0;
+  for (int it = 0; it < t.niter; ++it) {
+    if (it > 0 && !wait_or_abort(t.bar(BB_QEMPTY), (uint32_t)(it - 1) & 1, t.abort_flag, t.status,
+                                 kSiteProducerEmpty))
+      break;
+    const int q0 = (t.i0 + it) * C::T;
+    mbar_arrive_expect_tx(t.bar(BB_Q), 2 * C::TILE_BYTES);
+    for (int kb = 0; kb < C::D / 64; ++kb) {
+      tma_load_3d(t.sQ + kb * (C::T * 128), tm_q, kb * 64, q0, t.bh, t.bar(BB_Q));
+      tma_load_3d(t.sDO + kb * (C::T * 128), tm_do, kb * 64, q0, t.bh, t.bar(BB_Q));
+    }
+    loaded = it + 1;
+  }
+  wait_drain(t.bar(BB_KV), 0, t.status);
+  if (loaded > 0) wait_drain(t.bar(BB_Q), (uint32_t)(loaded - 1) & 1, t.status);
+}
+
+template <class C, bool BF16>
+__device__ __forceinline__ void bwd_mma(const BwdCtx& t) {
+  constexpr uint32_t idesc_s = make_idesc_f16(128, C::T, BF16, false, false);     // S^T, dP^T
+  constexpr uint32_t idesc_acc = make_idesc_f16(128, C::D, BF16, false, true);    // dV, dK: A in TMEM
+  constexpr uint32_t idesc_dq = make_idesc_f16(128, C::D, BF16, true, true);      // dQ: A, B MN-major
+  const uint64_t k_kmaj = make_sdesc_sw128(t.sK, 16, 1024);
+  const uint64_t v_kmaj = make_sdesc_sw128(t.sV, 16, 1024);
+  const uint64_t q_kmaj = make_sdesc_sw128(t.sQ, 16, 1024);
+  const uint64_t do_kmaj = make_sdesc_sw128(t.sDO, 16, 1024);
+  const uint64_t q_mn = make_sdesc_sw128(t.sQ, C::T * 128, 1024);
+  const uint64_t do_mn = make_sdesc_sw128(t.sDO, C::T * 128, 1024);
+  const uint64_t k_mn = make_sdesc_sw128(t.sK, C::T * 128, 1024);
+  const uint64_t ds_mn = make_sdesc_sw128(t.sDS, C::T * 128, 1024);
+  const uint32_t tS = t.tmem + C::TMEM_S, tDP = t.tmem + C::TMEM_DP;
+  const uint32_t tDV = t.tmem + C::TMEM_DV, tDK = t.tmem + C::TMEM_DK;
+  bool ok = wait_or_abort(t.bar(BB_KV), 0, t.abort_flag, t.status, kSiteMmaK);
+  for (int it = 0; it < t.niter && ok; ++it) {
+    const uint32_t ph = (uint32_t)it & 1;
+    if (!wait_or_abort(t.bar(BB_Q), ph, t.abort_flag, t.status, kSiteMmaQ)) break;
+    tc_fence_after();
+#pragma unroll
+    for (int k = 0; k < C::D / 16; ++k)
+      umma_ss(tS, k_kmaj + kmajor_step<C>(k, C::T), q_kmaj + kmajor_step<C>(k, C::T), idesc_s, k > 0 ? 1u : 0u);
+    umma_commit(t.bar(BB_S));
+    // dP^T reuses the columns the previous tile's dQ contribution was read from
+    if (it > 0 && !wait_or_abort(t.bar(BB_DQEMPTY), ph ^ 1u, t.abort_flag, t.status, kSiteMmaO)) break;
+    tc_fence_after();
+#pragma unroll
+    for (int k = 0; k < C::D / 16; ++k)
+      umma_ss(tDP, v_kmaj + kmajor_step<C>(k, C::T), do_kmaj + kmajor_step<C>(k, C::T), idesc_s, k > 0 ? 1u : 0u);
+    umma_commit(t.bar(BB_DP));
+    if (!wait_or_abort(t.bar(BB_P), ph, t.abort_flag, t.status, kSiteMmaP)) break;
+    tc_fence_after();
+    // K = 128 queries in steps of 16: P^T / dS^T of queries 0-63 sit in the
+    // first 32 columns of each 64-column half, queries 64-127 in the second half
+#pragma unroll
+    for (int k = 0; k < C::T / 16; ++k) {
+      const uint32_t col = (uint32_t)((k >> 2) * 64 + (k & 3) * 8);
+      umma_ts(tDV, tS + col, do_mn + (uint64_t)((k * 16 * 128) >> 4), idesc_acc, (it > 0 || k > 0) ? 1u : 0u);
+    }
+#pragma unroll
+    for (int k = 0; k < C::T / 16; ++k) {
+      const uint32_t col = (uint32_t)((k >> 2) * 64 + (k & 3) * 8);
+      umma_ts(tDK, tDP + col, q_mn + (uint64_t)((k * 16 * 128) >> 4), idesc_acc, (it > 0 || k > 0) ? 1u : 0u);
+    }
+    // dQ_i = dS K_j into the dP^T columns (the dK products above read dS^T from
+    // them first: MMAs of one thread execute in order)
+#pragma unroll
+    for (int k = 0; k < C::T / 16; ++k)
+      umma_ss(tDP, ds_mn + (uint64_t)((k * 16 * 128) >> 4), k_mn + (uint64_t)((k * 16 * 128) >> 4), idesc_dq,
+              k > 0 ? 1u : 0u);
+    umma_commit(t.bar(BB_DQ));
+    umma_commit(t.bar(BB_QEMPTY));
+  }
+  if (ok) umma_commit(t.bar(BB_END));
+  umma_commit(t.bar(BB_EXIT));
+  wait_drain(t.bar(BB_EXIT), 0, t.status);
+}
+
+template <class C, bool BF16, bool CAUSAL>
+__device__ __forceinline__ void bwd_elementwise(const BwdCtx& t, const BwdParams& p, uint8_t* smem, int warp,
+                                                int lane) {
+  const int h = warp >> 2;                 // warpgroup: query columns [64h, 64h + 64)
+  const int quad = warp & 3;
+  const int r = quad * 32 + lane;          // TMEM lane: key row (S^T, dP^T, dK, dV) or query row (dQ_i)
+  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+  const uint32_t tS = t.tmem + lane_off + C::TMEM_S + 64 * h;
+  const uint32_t tDP = t.tmem + lane_off + C::TMEM_DP + 64 * h;
+  float* l2s = reinterpret_cast<float*>(smem + C::OFF_LD + warp * 512);   // this warp's 64 L*log2e, 64 D
+  float* dss = l2s + 64;
+  uint8_t* ds_row = smem + C::OFF_DS + h * (C::T * 128) + r * 128;     // this key's row of dS^T, block h
+  const int key = t.j0 + r;
+  const float sl2 = p.scale_log2;
+  const float scale = p.scale;
+  bool ok = true;
+  for (int it = 0; it < t.niter; ++it) {
+    const uint32_t ph = (uint32_t)it & 1;
+    const int q0 = (t.i0 + it) * C::T + 64 * h;   // first query of this warpgroup's columns
+    // stage L (exp2 domain) and D of the 64 queries in this warp's own slot
+    // (warp-local, so no barrier spans warps that might abandon the tile)
+    __syncwarp();
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const int c = lane + 32 * x;
+      const int q = q0 + c;
+      l2s[c] = (q < t.n) ? p.lse[(size_t)t.bh * t.n + q] * 1.4426950408889634f : INFINITY;
+      dss[c] = (q < t.n) ? p.delta[(size_t)t.bh * t.n + q] : 0.f;
+    }
+    __syncwarp();
+
+    ok = wait_or_abort(t.bar(BB_S), ph, t.abort_flag, t.status, kSiteSoftmaxS);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    tc_fence_after();
+    uint32_t sr[64];
+    tmem_ld_32x32b_x32(tS, sr);
+    tmem_ld_32x32b_x32(tS + 32, sr + 32);
+    tmem_ld_wait_x32(sr);
+    tmem_ld_wait_x32(sr + 32);
+    // a key row sees query q when key < N, q < N and (causal) key <= q
+    const bool full = (t.j0 + C::T <= t.n) && (q0 + 64 <= t.n) && (!CAUSAL || t.j0 + C::T - 1 <= q0);
+    float pv[64];
+#pragma unroll
+    for (int c = 0; c < 64; ++c) {
+      const float x = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -l2s[c]));
+      pv[c] = (full || (key < t.n && (!CAUSAL || key <= q0 + c))) ? x : 0.f;   // q >= N: L = inf gives 0
+    }
+    uint32_t pk[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) pk[c] = pack2<BF16>(pv[2 * c], pv[2 * c + 1]);
+    tmem_st_32x32b_x32(tS, pk);
+
+    ok = wait_or_abort(t.bar(BB_DP), ph, t.abort_flag, t.status, kSiteSoftmaxO);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    tc_fence_after();
+    uint32_t dr[64];
+    tmem_ld_32x32b_x32(tDP, dr);
+    tmem_ld_32x32b_x32(tDP + 32, dr + 32);
+    tmem_ld_wait_x32(dr);
+    tmem_ld_wait_x32(dr + 32);
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const float a = scale * pv[2 * c] * (__uint_as_float(dr[2 * c]) - dss[2 * c]);
+      const float b = scale * pv[2 * c + 1] * (__uint_as_float(dr[2 * c + 1]) - dss[2 * c + 1]);
+      pk[c] = pack2<BF16>(a, b);
+    }
+    tmem_st_32x32b_x32(tDP, pk);
+    // dS^T row to shared memory (128-byte swizzle: 16-byte chunk c of row r
+    // at chunk c ^ (r mod 8)), the A operand of the dQ product
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      *reinterpret_cast<uint4*>(ds_row + ((c ^ (r & 7)) * 16)) = v;
+    }
+    fence_proxy_async_smem();
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(t.bar(BB_P));
+
+    ok = wait_or_abort(t.bar(BB_DQ), ph, t.abort_flag, t.status, kSiteEpilogueO);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    tc_fence_after();
+    // dQ_i rows: lane = query row of tile i; this warpgroup adds d/2 columns
+    const int qrow = (t.i0 + it) * C::T + r;
+    float* dst = p.dq_accum + ((size_t)t.bh * t.n + (size_t)qrow) * C::D + (C::D / 2) * h;
+#pragma unroll
+    for (int c = 0; c < C::D / 2; c += 32) {
+      uint32_t o[32];
+      tmem_ld_32x32b_x32(t.tmem + lane_off + C::TMEM_DP + (C::D / 2) * h + c, o);
+      tmem_ld_wait_x32(o);
+      if (qrow < t.n) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          red_add_v4(dst + c + i, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), __uint_as_float(o[i + 2]),
+                     __uint_as_float(o[i + 3]));
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(t.bar(BB_DQEMPTY));
+  }
+  if (ok) {
+    ok = wait_or_abort(t.bar(BB_END), 0, t.abort_flag, t.status, kSiteDrain);
+    ok = __all_sync(0xffffffffu, ok);
+  }
+  if (!ok) return;
+  tc_fence_after();
+  // dV_j and dK_j rows (lane = key row): d/2 columns per warpgroup
+  const size_t row_off = ((size_t)t.bh * t.n + (size_t)key) * C::D + (C::D / 2) * h;
+#pragma unroll 1
+  for (int which = 0; which < 2; ++which) {
+    const uint32_t base = t.tmem + lane_off + (which ? C::TMEM_DK : C::TMEM_DV) + (C::D / 2) * h;
+    uint8_t* out = reinterpret_cast<uint8_t*>(which ? p.dk : p.dv) + row_off * 2;
+#pragma unroll 1
+    for (int c = 0; c < C::D / 2; c += 32) {
+      uint32_t o[32];
+      tmem_ld_32x32b_x32(base + c, o);
+      tmem_ld_wait_x32(o);
+      uint32_t pk16[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) pk16[i] = pack2<BF16>(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
+      if (key < t.n) {
+        uint4* dst4 = reinterpret_cast<uint4*>(out + c * 2);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst4[i] = make_uint4(pk16[4 * i], pk16[4 * i + 1], pk16[4 * i + 2], pk16[4 * i + 3]);
+      }
+    }
+  }
+}
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(384, 1)
+    fa2_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                   const BwdParams p) {
+  using C = BwdConfig<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  const int warp = (int)(threadIdx.x >> 5);
+  const int lane = (int)(threadIdx.x & 31);
+
+  BwdCtx t;
+  t.bar0 = sbase + C::OFF_BAR;
+  t.sK = sbase + C::OFF_K;
+  t.sV = sbase + C::OFF_V;
+  t.sQ = sbase + C::OFF_Q;
+  t.sDO = sbase + C::OFF_DO;
+  t.sDS = sbase + C::OFF_DS;
+  t.abort_flag = abort_flag;
+  t.status = p.status;
+  t.n = p.n;
+  int unit;
+  unit_of_block((int)blockIdx.x, p.bh, p.num_tiles, t.bh, unit);
+  // the key tiles with the most query tiles (the first ones, when causal) start first
+  const int jt = p.num_tiles - 1 - unit;
+  t.j0 = jt * C::T;
+  t.i0 = CAUSAL ? jt : 0;
+  t.niter = p.num_tiles - t.i0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(t.bar(BB_KV), 1);
+    mbar_init(t.bar(BB_Q), 1);
+    mbar_init(t.bar(BB_QEMPTY), 1);
+    mbar_init(t.bar(BB_S), 1);
+    mbar_init(t.bar(BB_DP), 1);
+    mbar_init(t.bar(BB_P), 8);
+    mbar_init(t.bar(BB_DQ), 1);
+    mbar_init(t.bar(BB_DQEMPTY), 8);
+    mbar_init(t.bar(BB_END), 1);
+    mbar_init(t.bar(BB_EXIT), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::TMA_WARP && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  t.tmem = *tmem_slot;
+
+  if (warp == C::TMA_WARP) {
+    if (lane == 0) bwd_producer<C>(t, &tm_q, &tm_k, &tm_v, &tm_do);
+  } else if (warp == C::MMA_WARP) {
+    if (lane == 0) bwd_mma<C, BF16>(t);
+    __syncwarp();
+  } else if (warp < 8) {
+    bwd_elementwise<C, BF16, CAUSAL>(t, p, smem, warp, lane);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(t.tmem, C::TMEM_COLS);
+  }
+}
+
+// D_i = rowsum(dO_i o O_i) in fp32, and the row's fp32 dQ accumulator zeroed.
+// D/8 threads per row, 8 elements (16 bytes) each.
+template <int D, bool BF16>
+__global__ void fa2_bwd_preprocess_kernel(const void* __restrict__ o, const void* __restrict__ dout,
+                                          float* __restrict__ delta, float* __restrict__ dq_accum, long long rows) {
+  constexpr int TPR = D / 8;
+  const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long row = g / TPR;
+  const int part = (int)(g % TPR);
+  float acc = 0.f;
+  if (row < rows) {
+    const size_t off = (size_t)row * D + (size_t)part * 8;
+    const uint4 a = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(o) + off);
+    const uint4 b = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(dout) + off);
+    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 x = unpack2<BF16>(av[i]), y = unpack2<BF16>(bv[i]);
+      acc = fmaf(x.x, y.x, acc);
+      acc = fmaf(x.y, y.y, acc);
+    }
+    float4* z = reinterpret_cast<float4*>(dq_accum + off);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int m = TPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+  if (row < rows && part == 0) delta[row] = acc;
+}
+
+// 16-bit dQ from the fp32 accumulator, 8 elements per thread.
+template <bool BF16>
+__global__ void fa2_bwd_dq_convert_kernel(const float* __restrict__ acc, void* __restrict__ dq, long long n8) {
+  const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= n8) return;
+  const float4 a = reinterpret_cast<const float4*>(acc)[2 * g];
+  const float4 b = reinterpret_cast<const float4*>(acc)[2 * g + 1];
+  reinterpret_cast<uint4*>(dq)[g] =
+      make_uint4(pack2<BF16>(a.x, a.y), pack2<BF16>(a.z, a.w), pack2<BF16>(b.x, b.y), pack2<BF16>(b.z, b.w));
+}
+
+template <int D, bool BF16, bool CAUSAL>
+int launch_bwd(const BwdLaunchArgs& a) {
+  using C = BwdConfig<D>;
+  const long long rows = (long long)a.p.bh * a.p.n;
+  {
+    const long long threads = rows * (D / 8);
+    const unsigned blocks = (unsigned)((threads + 255) / 256);
+    fa2_bwd_preprocess_kernel<D, BF16><<<blocks, 256, 0, a.stream>>>(a.o, a.dout, const_cast<float*>(a.p.delta),
+                                                                     a.p.dq_accum, rows);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return (int)e;
+  }
+  auto kern = fa2_bwd_kernel<D, BF16, CAUSAL>;
+  static std::atomic<unsigned long long> configured{0};
+  int e = once_per_device(configured, [&]() -> int {
+    return (int)cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
+  });
+  if (e != 0) return e;
+  kern<<<(unsigned)(a.p.bh * a.p.num_tiles), C::THREADS, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v,
+                                                                                     a.tm_do, a.p);
+  e = (int)cudaGetLastError();
+  if (e != 0) return e;
+  const long long n8 = rows * D / 8;
+  fa2_bwd_dq_convert_kernel<BF16><<<(unsigned)((n8 + 255) / 256), 256, 0, a.stream>>>(a.p.dq_accum, a.dq, n8);
+  return (int)cudaGetLastError();
+}
+
+template <int D>
+int launch_bwd_dispatch(const BwdLaunchArgs& a) {
+  if (a.bf16) return a.causal ? launch_bwd<D, true, true>(a) : launch_bwd<D, true, false>(a);
+  return a.causal ? launch_bwd<D, false, true>(a) : launch_bwd<D, false, false>(a);
+}
+
+}  // namespace fa2

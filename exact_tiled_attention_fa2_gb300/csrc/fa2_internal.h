@@ -34,6 +34,34 @@ struct LaunchArgs {
   cudaStream_t stream;
 };
 
+struct BwdParams {
+  const float* lse;    // [B,H,N] forward logsumexp (natural log)
+  const float* delta;  // [B,H,N] D_i = rowsum(dO_i o O_i), from the preprocess kernel
+  float* dq_accum;     // [B,H,N,d] fp32, zeroed by the preprocess kernel
+  void* dk;            // [B,H,N,d] 16-bit outputs
+  void* dv;
+  uint32_t* status;
+  int n;
+  int bh;
+  int num_tiles;       // ceil(N / 128): key tiles = query tiles
+  float scale;
+  float scale_log2;
+};
+
+struct BwdLaunchArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // boxes of 64 columns x 128 rows
+  BwdParams p;
+  const void* o;       // forward output, for D
+  const void* dout;    // upstream gradient
+  void* dq;            // 16-bit dQ output
+  bool bf16;
+  bool causal;
+  cudaStream_t stream;
+};
+
+int launch_bwd_d64(const BwdLaunchArgs& a);
+int launch_bwd_d128(const BwdLaunchArgs& a);
+
 // Host-side tile geometry the launcher needs to build tensor maps: rows of Q
 // per CTA tile and rows of K/V per streamed tile, per head dim.
 struct TileGeometry {

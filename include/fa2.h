@@ -81,7 +81,7 @@ int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  * fa2_fwd_host_workspace_bytes(B,H,N,d) bytes, 256-byte aligned, owned by the
  * caller.  Returns FA2_ERR_DEVICE_TIMEOUT if a kernel wait timed out.
  *
- * Problems with at least 48 MB of input are cut into up to 4 groups of
+ * Problems with at least 48 MB of input are cut into up to 8 groups of
  * (b,h) slices: the copy-in of the next group and the copy-out of the
  * previous one run on two copy streams the library creates once per device
  * while the forward pass of the current group runs on `stream` (which first
@@ -136,6 +136,34 @@ int fa2_fwd_host_noalloc(const void* q_host, const void* k_host, const void* v_h
  * `detail` (may be NULL) receives the raw status bits (role and wait site).
  */
 int fa2_get_device_status(void* stream, uint32_t* detail);
+
+/*
+ * fa2_bwd -- gradients of fa2_fwd for an upstream gradient dout
+ * (FlashAttention V2 in depth, section 7: P = exp(S - L) rebuilt from the
+ * forward's logsumexp, dV = P^T dO, dP = dO V^T, D_i = rowsum(dO_i o O_i),
+ * dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q).  Asynchronous on
+ * `stream`.
+ *
+ *   q, k, v, o, dout : device, [B,H,N,d] `dtype` (o is fa2_fwd's output)
+ *   lse              : device, [B,H,N] float32, fa2_fwd's logsumexp
+ *   dq, dk, dv       : device, [B,H,N,d] `dtype`, written
+ *   workspace        : device, >= fa2_bwd_workspace_bytes(B,H,N,d) bytes,
+ *                      256-byte aligned, owned by the caller: an fp32 dQ
+ *                      accumulator [B,H,N,d] and D [B,H,N], both written
+ *                      before they are read
+ *   d                : 64 or 128 (FA2_ERR_UNSUPPORTED otherwise)
+ *   other arguments  : as fa2_fwd
+ *
+ * dK and dV are each written once; dQ is accumulated over key tiles with
+ * fp32 atomic adds, so its last bits may vary between runs.  Outputs and
+ * workspace must not overlap any input or each other.
+ */
+int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+            void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+            int B, int H, int N, int d, float scale, int causal, int dtype, void* stream);
+
+/* Device workspace fa2_bwd needs: fp32 [B,H,N,d] + fp32 [B,H,N], each 256-byte aligned. */
+size_t fa2_bwd_workspace_bytes(int B, int H, int N, int d);
 
 /*
  * fa2_selftest_wait_timeout -- exercises the kernels' failure path without a

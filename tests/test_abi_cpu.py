@@ -34,7 +34,8 @@ def _declared_functions():
 def test_header_declares_entry_points():
     names = _declared_functions()
     for required in ("fa2_fwd", "fa2_fwd_host", "fa2_fwd_host_workspace_bytes", "fa2_get_device_status",
-                     "fa2_status_string", "fa2_version", "fa2_selftest_wait_timeout"):
+                     "fa2_status_string", "fa2_version", "fa2_selftest_wait_timeout", "fa2_bwd",
+                     "fa2_bwd_workspace_bytes"):
         assert required in names
 
 
