@@ -127,6 +127,20 @@ int cached_maps(LaunchArgs& a, const void* q, const void* k, const void* v, int 
   return FA2_OK;
 }
 
+// fp32 [B*H, N, d] view of the dQ accumulator; boxes of 32 columns x 32 rows
+// (one warp's rows and a 128-byte column block), 128-byte swizzle, for TMA
+// reduce-add.  Rows past N are clipped.
+int encode_dq_map(CUtensorMap* m, void* base, int bh, int n, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)n * (cuuint64_t)d * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA2_OK : FA2_ERR_CUDA;
+}
+
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
   uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + nb && y < x + na;
@@ -464,6 +478,7 @@ extern "C" int fa2_bwd(const void* q, const void* k, const void* v, const void* 
       encode_map(&a.tm_v, v, bh, N, d, 128, bf16) || encode_map(&a.tm_do, dout, bh, N, d, 128, bf16))
     return FA2_ERR_CUDA;
   uint8_t* w = static_cast<uint8_t*>(workspace);
+  if (encode_dq_map(&a.tm_dq, w, bh, N, d)) return FA2_ERR_CUDA;
   a.p.dq_accum = reinterpret_cast<float*>(w);
   a.p.delta = reinterpret_cast<float*>(w + align256(rows * (size_t)d * 4));
   a.p.lse = lse;

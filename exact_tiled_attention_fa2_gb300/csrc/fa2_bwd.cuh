@@ -12,7 +12,8 @@
 //   main        key/value-outer (section 7.2): a CTA owns 128 keys of one
 //               (b, h), keeps dK_j and dV_j in tensor memory and walks the
 //               query tiles that see those keys; each tile's dQ contribution
-//               is added to the fp32 accumulator with vector atomics;
+//               is staged in shared memory and added to the fp32 accumulator
+//               by TMA reduce-add (the accumulation across key tiles, 7.2);
 //   convert     dQ accumulator -> 16-bit dQ.
 //
 // Main kernel, per query tile i (tensor memory holds S^T and dP^T with keys on
@@ -24,7 +25,8 @@
 //   dV  += P^T dO_i               A = P^T from TMEM, B = dO_i (MN-major)
 //   dK  += dS^T Q_i               A = dS^T from TMEM, B = Q_i (MN-major)
 //   dQ_i = dS K_j                 A = dS from smem (MN-major), B = K_j (MN-major),
-//                                 into the dP^T columns, then atomically added
+//                                 into the dP^T columns; each warp copies its 32
+//                                 rows out, frees the columns, and TMA adds them
 //
 // Warp roles (384 threads): warps 0-3 and 4-7 are two elementwise warpgroups,
 // each for 64 of the tile's 128 query columns (and half of the d columns of
@@ -46,13 +48,15 @@ struct BwdConfig {
   static constexpr int TMA_WARP = 9;
   static constexpr uint32_t TILE_BYTES = T * D * 2;
   static constexpr uint32_t DS_BYTES = T * T * 2;    // dS^T, keys x queries, 16-bit
+  static constexpr int QSTAGES = (D == 64) ? 2 : 1;   // Q_i / dO_i buffers (the next tile loads meanwhile)
+  static constexpr uint32_t DQ_WARP_BYTES = 32 * (D / 2) * 4;  // a warp's 32 rows x d/2 fp32 dQ columns
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + TILE_BYTES;
-  static constexpr uint32_t OFF_Q = OFF_V + TILE_BYTES;
-  static constexpr uint32_t OFF_DO = OFF_Q + TILE_BYTES;
-  static constexpr uint32_t OFF_DS = OFF_DO + TILE_BYTES;
-  static constexpr uint32_t OFF_LD = OFF_DS + DS_BYTES;   // per elementwise warp: 64 x L*log2e, 64 x D
-  static constexpr uint32_t OFF_BAR = OFF_LD + 8 * 512;
+  static constexpr uint32_t OFF_Q = OFF_V + TILE_BYTES;            // + stage * TILE_BYTES
+  static constexpr uint32_t OFF_DO = OFF_Q + QSTAGES * TILE_BYTES;  // + stage * TILE_BYTES
+  static constexpr uint32_t OFF_DS = OFF_DO + QSTAGES * TILE_BYTES;
+  static constexpr uint32_t OFF_DQ = OFF_DS + DS_BYTES;          // + warp * DQ_WARP_BYTES, 32x32 fp32 boxes
+  static constexpr uint32_t OFF_BAR = OFF_DQ + 8 * DQ_WARP_BYTES;
   static constexpr uint32_t NUM_BARS = 16;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
@@ -67,8 +71,6 @@ struct BwdConfig {
 
 enum : int {
   BB_KV = 0,
-  BB_Q = 1,        // Q_i and dO_i landed
-  BB_QEMPTY = 2,   // every MMA reading Q_i / dO_i / dS finished
   BB_S = 3,
   BB_DP = 4,
   BB_P = 5,        // P^T, dS^T written (8 warp arrivals)
@@ -76,6 +78,8 @@ enum : int {
   BB_DQEMPTY = 7,  // dQ_i read out of TMEM (8 warp arrivals)
   BB_END = 8,
   BB_EXIT = 9,
+  BB_Q = 10,       // + stage: Q_i and dO_i landed
+  BB_QEMPTY = 12,  // + stage: every MMA reading that stage finished
 };
 
 struct BwdCtx {
@@ -96,19 +100,23 @@ __device__ __forceinline__ void bwd_producer(const BwdCtx& t, const CUtensorMap*
   }
   int loaded = 0;
   for (int it = 0; it < t.niter; ++it) {
-    if (it > 0 && !wait_or_abort(t.bar(BB_QEMPTY), (uint32_t)(it - 1) & 1, t.abort_flag, t.status,
-                                 kSiteProducerEmpty))
+    const int s = it % C::QSTAGES, u = it / C::QSTAGES;
+    if (u > 0 && !wait_or_abort(t.bar(BB_QEMPTY + s), (uint32_t)(u - 1) & 1, t.abort_flag, t.status,
+                                kSiteProducerEmpty))
       break;
     const int q0 = (t.i0 + it) * C::T;
-    mbar_arrive_expect_tx(t.bar(BB_Q), 2 * C::TILE_BYTES);
+    mbar_arrive_expect_tx(t.bar(BB_Q + s), 2 * C::TILE_BYTES);
     for (int kb = 0; kb < C::D / 64; ++kb) {
-      tma_load_3d(t.sQ + kb * (C::T * 128), tm_q, kb * 64, q0, t.bh, t.bar(BB_Q));
-      tma_load_3d(t.sDO + kb * (C::T * 128), tm_do, kb * 64, q0, t.bh, t.bar(BB_Q));
+      tma_load_3d(t.sQ + s * C::TILE_BYTES + kb * (C::T * 128), tm_q, kb * 64, q0, t.bh, t.bar(BB_Q + s));
+      tma_load_3d(t.sDO + s * C::TILE_BYTES + kb * (C::T * 128), tm_do, kb * 64, q0, t.bh, t.bar(BB_Q + s));
     }
     loaded = it + 1;
   }
   wait_drain(t.bar(BB_KV), 0, t.status);
-  if (loaded > 0) wait_drain(t.bar(BB_Q), (uint32_t)(loaded - 1) & 1, t.status);
+  for (int s = 0; s < C::QSTAGES; ++s) {
+    const int last = loaded - 1 - ((loaded - 1 - s) % C::QSTAGES + C::QSTAGES) % C::QSTAGES;   // last tile in stage s
+    if (last >= 0) wait_drain(t.bar(BB_Q + s), (uint32_t)(last / C::QSTAGES) & 1, t.status);
+  }
 }
 
 template <class C, bool BF16>
@@ -118,10 +126,10 @@ __device__ __forceinline__ void bwd_mma(const BwdCtx& t) {
   constexpr uint32_t idesc_dq = make_idesc_f16(128, C::D, BF16, true, true);      // dQ: A, B MN-major
   const uint64_t k_kmaj = make_sdesc_sw128(t.sK, 16, 1024);
   const uint64_t v_kmaj = make_sdesc_sw128(t.sV, 16, 1024);
-  const uint64_t q_kmaj = make_sdesc_sw128(t.sQ, 16, 1024);
-  const uint64_t do_kmaj = make_sdesc_sw128(t.sDO, 16, 1024);
-  const uint64_t q_mn = make_sdesc_sw128(t.sQ, C::T * 128, 1024);
-  const uint64_t do_mn = make_sdesc_sw128(t.sDO, C::T * 128, 1024);
+  const uint64_t q_kmaj0 = make_sdesc_sw128(t.sQ, 16, 1024);
+  const uint64_t do_kmaj0 = make_sdesc_sw128(t.sDO, 16, 1024);
+  const uint64_t q_mn0 = make_sdesc_sw128(t.sQ, C::T * 128, 1024);
+  const uint64_t do_mn0 = make_sdesc_sw128(t.sDO, C::T * 128, 1024);
   const uint64_t k_mn = make_sdesc_sw128(t.sK, C::T * 128, 1024);
   const uint64_t ds_mn = make_sdesc_sw128(t.sDS, C::T * 128, 1024);
   const uint32_t tS = t.tmem + C::TMEM_S, tDP = t.tmem + C::TMEM_DP;
@@ -129,7 +137,11 @@ __device__ __forceinline__ void bwd_mma(const BwdCtx& t) {
   bool ok = wait_or_abort(t.bar(BB_KV), 0, t.abort_flag, t.status, kSiteMmaK);
   for (int it = 0; it < t.niter && ok; ++it) {
     const uint32_t ph = (uint32_t)it & 1;
-    if (!wait_or_abort(t.bar(BB_Q), ph, t.abort_flag, t.status, kSiteMmaQ)) break;
+    const int qs = it % C::QSTAGES;
+    const uint64_t stage_step = (uint64_t)((qs * C::TILE_BYTES) >> 4);
+    const uint64_t q_kmaj = q_kmaj0 + stage_step, do_kmaj = do_kmaj0 + stage_step;
+    const uint64_t q_mn = q_mn0 + stage_step, do_mn = do_mn0 + stage_step;
+    if (!wait_or_abort(t.bar(BB_Q + qs), (uint32_t)(it / C::QSTAGES) & 1, t.abort_flag, t.status, kSiteMmaQ)) break;
     tc_fence_after();
 #pragma unroll
     for (int k = 0; k < C::D / 16; ++k)
@@ -163,7 +175,7 @@ __device__ __forceinline__ void bwd_mma(const BwdCtx& t) {
       umma_ss(tDP, ds_mn + (uint64_t)((k * 16 * 128) >> 4), k_mn + (uint64_t)((k * 16 * 128) >> 4), idesc_dq,
               k > 0 ? 1u : 0u);
     umma_commit(t.bar(BB_DQ));
-    umma_commit(t.bar(BB_QEMPTY));
+    umma_commit(t.bar(BB_QEMPTY + qs));
   }
   if (ok) umma_commit(t.bar(BB_END));
   umma_commit(t.bar(BB_EXIT));
@@ -172,16 +184,15 @@ __device__ __forceinline__ void bwd_mma(const BwdCtx& t) {
 
 template <class C, bool BF16, bool CAUSAL>
 __device__ __forceinline__ void bwd_elementwise(const BwdCtx& t, const BwdParams& p, uint8_t* smem, int warp,
-                                                int lane) {
+                                                int lane, const CUtensorMap* tm_dq) {
   const int h = warp >> 2;                 // warpgroup: query columns [64h, 64h + 64)
   const int quad = warp & 3;
   const int r = quad * 32 + lane;          // TMEM lane: key row (S^T, dP^T, dK, dV) or query row (dQ_i)
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
   const uint32_t tS = t.tmem + lane_off + C::TMEM_S + 64 * h;
   const uint32_t tDP = t.tmem + lane_off + C::TMEM_DP + 64 * h;
-  float* l2s = reinterpret_cast<float*>(smem + C::OFF_LD + warp * 512);   // this warp's 64 L*log2e, 64 D
-  float* dss = l2s + 64;
   uint8_t* ds_row = smem + C::OFF_DS + h * (C::T * 128) + r * 128;     // this key's row of dS^T, block h
+  uint8_t* dq_stage = smem + C::OFF_DQ + warp * C::DQ_WARP_BYTES;         // this warp's dQ boxes
   const int key = t.j0 + r;
   const float sl2 = p.scale_log2;
   const float scale = p.scale;
@@ -189,17 +200,18 @@ __device__ __forceinline__ void bwd_elementwise(const BwdCtx& t, const BwdParams
   for (int it = 0; it < t.niter; ++it) {
     const uint32_t ph = (uint32_t)it & 1;
     const int q0 = (t.i0 + it) * C::T + 64 * h;   // first query of this warpgroup's columns
-    // stage L (exp2 domain) and D of the 64 queries in this warp's own slot
-    // (warp-local, so no barrier spans warps that might abandon the tile)
-    __syncwarp();
-#pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      const int c = lane + 32 * x;
-      const int q = q0 + c;
-      l2s[c] = (q < t.n) ? p.lse[(size_t)t.bh * t.n + q] * 1.4426950408889634f : INFINITY;
-      dss[c] = (q < t.n) ? p.delta[(size_t)t.bh * t.n + q] : 0.f;
+    // L (exp2 domain) and D of the 64 queries: lane c holds queries c and
+    // c + 32, every lane takes each value by shuffle (warp-local, so no
+    // barrier spans warps that might abandon the tile)
+    float l_lo, l_hi, d_lo, d_hi;
+    {
+      const int qa = q0 + lane, qb = q0 + lane + 32;
+      const size_t base = (size_t)t.bh * t.n;
+      l_lo = (qa < t.n) ? p.lse[base + qa] * 1.4426950408889634f : INFINITY;
+      l_hi = (qb < t.n) ? p.lse[base + qb] * 1.4426950408889634f : INFINITY;
+      d_lo = (qa < t.n) ? p.delta[base + qa] : 0.f;
+      d_hi = (qb < t.n) ? p.delta[base + qb] : 0.f;
     }
-    __syncwarp();
 
     ok = wait_or_abort(t.bar(BB_S), ph, t.abort_flag, t.status, kSiteSoftmaxS);
     ok = __all_sync(0xffffffffu, ok);
@@ -215,7 +227,8 @@ __device__ __forceinline__ void bwd_elementwise(const BwdCtx& t, const BwdParams
     float pv[64];
 #pragma unroll
     for (int c = 0; c < 64; ++c) {
-      const float x = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -l2s[c]));
+      const float lq = __shfl_sync(0xffffffffu, c < 32 ? l_lo : l_hi, c & 31);
+      const float x = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lq));
       pv[c] = (full || (key < t.n && (!CAUSAL || key <= q0 + c))) ? x : 0.f;   // q >= N: L = inf gives 0
     }
     uint32_t pk[32];
@@ -234,8 +247,10 @@ __device__ __forceinline__ void bwd_elementwise(const BwdCtx& t, const BwdParams
     tmem_ld_wait_x32(dr + 32);
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
-      const float a = scale * pv[2 * c] * (__uint_as_float(dr[2 * c]) - dss[2 * c]);
-      const float b = scale * pv[2 * c + 1] * (__uint_as_float(dr[2 * c + 1]) - dss[2 * c + 1]);
+      const float da = __shfl_sync(0xffffffffu, c < 16 ? d_lo : d_hi, (2 * c) & 31);
+      const float db = __shfl_sync(0xffffffffu, c < 16 ? d_lo : d_hi, (2 * c + 1) & 31);
+      const float a = scale * pv[2 * c] * (__uint_as_float(dr[2 * c]) - da);
+      const float b = scale * pv[2 * c + 1] * (__uint_as_float(dr[2 * c + 1]) - db);
       pk[c] = pack2<BF16>(a, b);
     }
     tmem_st_32x32b_x32(tDP, pk);
@@ -256,25 +271,40 @@ __device__ __forceinline__ void bwd_elementwise(const BwdCtx& t, const BwdParams
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
     tc_fence_after();
-    // dQ_i rows: lane = query row of tile i; this warpgroup adds d/2 columns
-    const int qrow = (t.i0 + it) * C::T + r;
-    float* dst = p.dq_accum + ((size_t)t.bh * t.n + (size_t)qrow) * C::D + (C::D / 2) * h;
+    // dQ_i rows: lane = query row of tile i; this warpgroup adds d/2 columns.
+    // Copy them to registers and free the TMEM columns at once, then stage
+    // them in this warp's shared-memory boxes (128-byte swizzle) and let TMA
+    // add the boxes to the fp32 accumulator asynchronously.
+    uint32_t dq[C::D / 2];
 #pragma unroll
-    for (int c = 0; c < C::D / 2; c += 32) {
-      uint32_t o[32];
-      tmem_ld_32x32b_x32(t.tmem + lane_off + C::TMEM_DP + (C::D / 2) * h + c, o);
-      tmem_ld_wait_x32(o);
-      if (qrow < t.n) {
+    for (int c = 0; c < C::D / 2; c += 32) tmem_ld_32x32b_x32(t.tmem + lane_off + C::TMEM_DP + (C::D / 2) * h + c, dq + c);
 #pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          red_add_v4(dst + c + i, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), __uint_as_float(o[i + 2]),
-                     __uint_as_float(o[i + 3]));
-      }
-    }
+    for (int c = 0; c < C::D / 2; c += 32) tmem_ld_wait_x32(dq + c);
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(t.bar(BB_DQEMPTY));
+    if (lane == 0) bulk_wait_read_all();   // the previous tile's boxes were read out
+    __syncwarp();
+#pragma unroll
+    for (int b = 0; b < C::D / 64; ++b) {
+      uint8_t* row = dq_stage + b * 4096 + lane * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) * 16)) =
+            make_uint4(dq[32 * b + 4 * c], dq[32 * b + 4 * c + 1], dq[32 * b + 4 * c + 2], dq[32 * b + 4 * c + 3]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      const int y = (t.i0 + it) * C::T + quad * 32;   // rows past N are clipped by the reduce
+#pragma unroll
+      for (int b = 0; b < C::D / 64; ++b)
+        tma_reduce_add_3d(tm_dq, smem_u32(dq_stage + b * 4096), (C::D / 2) * h + 32 * b, y, t.bh);
+      bulk_commit_group();
+    }
   }
+  if (lane == 0) bulk_wait_all();   // this warp's reduce-adds performed before the CTA exits
+  __syncwarp();
   if (ok) {
     ok = wait_or_abort(t.bar(BB_END), 0, t.abort_flag, t.status, kSiteDrain);
     ok = __all_sync(0xffffffffu, ok);
@@ -308,7 +338,7 @@ template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
     fa2_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                   const BwdParams p) {
+                   const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using C = BwdConfig<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -339,8 +369,10 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(t.bar(BB_KV), 1);
-    mbar_init(t.bar(BB_Q), 1);
-    mbar_init(t.bar(BB_QEMPTY), 1);
+    for (int s = 0; s < C::QSTAGES; ++s) {
+      mbar_init(t.bar(BB_Q + s), 1);
+      mbar_init(t.bar(BB_QEMPTY + s), 1);
+    }
     mbar_init(t.bar(BB_S), 1);
     mbar_init(t.bar(BB_DP), 1);
     mbar_init(t.bar(BB_P), 8);
@@ -356,6 +388,7 @@ __global__ void __launch_bounds__(384, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_dq);
   }
   if (warp == C::MMA_WARP) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -372,7 +405,7 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) bwd_mma<C, BF16>(t);
     __syncwarp();
   } else if (warp < 8) {
-    bwd_elementwise<C, BF16, CAUSAL>(t, p, smem, warp, lane);
+    bwd_elementwise<C, BF16, CAUSAL>(t, p, smem, warp, lane, &tm_dq);
   }
   tc_fence_before();
   __syncthreads();
@@ -442,7 +475,7 @@ int launch_bwd(const BwdLaunchArgs& a) {
   });
   if (e != 0) return e;
   kern<<<(unsigned)(a.p.bh * a.p.num_tiles), C::THREADS, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v,
-                                                                                     a.tm_do, a.p);
+                                                                                     a.tm_do, a.tm_dq, a.p);
   e = (int)cudaGetLastError();
   if (e != 0) return e;
   const long long n8 = rows * D / 8;

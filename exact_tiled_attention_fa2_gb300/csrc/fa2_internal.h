@@ -50,6 +50,7 @@ struct BwdParams {
 
 struct BwdLaunchArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // boxes of 64 columns x 128 rows
+  CUtensorMap tm_dq;                    // fp32 dQ accumulator, boxes of 32 columns x 32 rows
   BwdParams p;
   const void* o;       // forward output, for D
   const void* dout;    // upstream gradient
