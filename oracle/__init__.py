@@ -65,6 +65,9 @@ def _load():
         lib.oracle_attention_bwd.argtypes = [p16, p16, p16, p16, ctypes.c_int, i64, i64, i64, i64, ctypes.c_double,
                                              ctypes.c_int, pd, pd, pd, pd, ctypes.c_int]
         lib.oracle_attention_bwd.restype = ctypes.c_int
+        lib.oracle_attention_fwd_masked.argtypes = [p16, p16, p16, ctypes.c_int, i64, i64, i64, i64, i64,
+                                                    ctypes.c_double, i64, i64, pd, pd, ctypes.c_int]
+        lib.oracle_attention_fwd_masked.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -180,3 +183,28 @@ def attention_bwd(q, k, v, dout, dtype: int, scale: float, causal: bool, threads
     if rc:
         raise ValueError("oracle_attention_bwd failed (%d)" % rc)
     return dq, dk, dv, delta
+
+
+def attention_fwd_masked(q, k, v, dtype: int, scale: float, window_left: int = -1, window_right: int = -1,
+                         threads: int = 0):
+    """Forward with a band mask and N_q != N_k: q [B,H,Nq,d], k, v [B,H,Nk,d] (16-bit bit patterns).
+
+    Key j is visible to query i iff j >= i + (Nk - Nq) - window_left and
+    j <= i + (Nk - Nq) + window_right (a negative window is unbounded on that
+    side; causal is window_right = 0).  Rows with nothing visible: O = 0,
+    L = -inf.  Returns float64 (O [B,H,Nq,d], L [B,H,Nq]).
+    """
+    q, k, v = _bits(q), _bits(k), _bits(v)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if k.shape != (B, H, Nk, d) or v.shape != k.shape:
+        raise ValueError("k, v must be [B,H,Nk,d] with q's B, H, d")
+    o = np.empty((B, H, Nq, d))
+    lse = np.empty((B, H, Nq))
+    rc = _load().oracle_attention_fwd_masked(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
+                                             _ptr(v, ctypes.c_uint16), int(dtype), B, H, Nq, Nk, d, float(scale),
+                                             int(window_left), int(window_right), _ptr(o, ctypes.c_double),
+                                             _ptr(lse, ctypes.c_double), int(threads))
+    if rc:
+        raise ValueError("oracle_attention_fwd_masked failed (%d)" % rc)
+    return o, lse

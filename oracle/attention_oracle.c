@@ -370,6 +370,91 @@ int oracle_attention_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v
   return rc;
 }
 
+/* ------------------------------------------------------------------ masks and N_q != N_k */
+
+/*
+ * Forward with a general band mask and separate query / key lengths.  Query
+ * i (0 <= i < Nq) and key j (0 <= j < Nk) are aligned at the end of the key
+ * sequence (offset off = Nk - Nq, so the last query faces the last key), and
+ * key j is visible iff
+ *
+ *     j >= i + off - window_left    (when window_left >= 0)
+ *     j <= i + off + window_right   (when window_right >= 0; causal is window_right = 0)
+ *
+ * -- the additive 0 / -inf mask of the Flash Attention 2 page ("Causal
+ * masking", Option A: sliding windows and the like are a 0/-inf add before
+ * softmax).  A row that sees no key has O = 0 and L = -inf.  q: [B,H,Nq,d],
+ * k, v: [B,H,Nk,d]; o: [B,H,Nq,d], lse: [B,H,Nq].
+ */
+int oracle_attention_fwd_masked(const uint16_t* q, const uint16_t* k, const uint16_t* v, int dtype, int64_t B,
+                                int64_t H, int64_t Nq, int64_t Nk, int64_t d, double scale, int64_t window_left,
+                                int64_t window_right, double* o_out, double* lse_out, int threads) {
+  if (!q || !k || !v || !o_out || !lse_out || (dtype != ORACLE_FP16 && dtype != ORACLE_BF16)) return ORACLE_ERR_ARG;
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1 || !isfinite(scale)) return ORACLE_ERR_ARG;
+#ifdef _OPENMP
+  if (threads > 0) omp_set_num_threads(threads);
+#else
+  (void)threads;
+#endif
+  const int64_t off = Nk - Nq;
+  double* kmat = (double*)malloc(sizeof(double) * (size_t)(Nk * d));
+  double* vmat = (double*)malloc(sizeof(double) * (size_t)(Nk * d));
+  if (!kmat || !vmat) { free(kmat); free(vmat); return ORACLE_ERR_NOMEM; }
+  int status = ORACLE_OK;
+  for (int64_t bh = 0; bh < B * H && status == ORACLE_OK; ++bh) {
+    for (int64_t x = 0; x < Nk * d; ++x) {
+      kmat[x] = widen(k[bh * Nk * d + x], dtype);
+      vmat[x] = widen(v[bh * Nk * d + x], dtype);
+    }
+    int nomem = 0;
+#pragma omp parallel reduction(| : nomem)
+    {
+      double* srow = (double*)malloc(sizeof(double) * (size_t)Nk);
+      double* qrow = (double*)malloc(sizeof(double) * (size_t)d);
+      if (!srow || !qrow) {
+        nomem = 1;
+      } else {
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t i = 0; i < Nq; ++i) {
+          for (int64_t c = 0; c < d; ++c) qrow[c] = widen(q[(bh * Nq + i) * d + c], dtype);
+          int64_t lo = 0, hi = Nk - 1;
+          if (window_left >= 0 && i + off - window_left > lo) lo = i + off - window_left;
+          if (window_right >= 0 && i + off + window_right < hi) hi = i + off + window_right;
+          double* orow = o_out + (bh * Nq + i) * d;
+          double m = -INFINITY;
+          for (int64_t j = lo; j <= hi; ++j) {
+            double acc = 0.0;
+            for (int64_t c = 0; c < d; ++c) acc += qrow[c] * kmat[j * d + c];
+            srow[j] = scale * acc;
+            if (srow[j] > m) m = srow[j];
+          }
+          for (int64_t c = 0; c < d; ++c) orow[c] = 0.0;
+          if (hi < lo) {
+            lse_out[bh * Nq + i] = -INFINITY;
+            continue;
+          }
+          double sum = 0.0;
+          for (int64_t j = lo; j <= hi; ++j) {
+            srow[j] = exp(srow[j] - m);
+            sum += srow[j];
+          }
+          for (int64_t j = lo; j <= hi; ++j) {
+            const double pj = srow[j] / sum;
+            for (int64_t c = 0; c < d; ++c) orow[c] += pj * vmat[j * d + c];
+          }
+          lse_out[bh * Nq + i] = m + log(sum);
+        }
+      }
+      free(srow);
+      free(qrow);
+    }
+    if (nomem) status = ORACLE_ERR_NOMEM;
+  }
+  free(kmat);
+  free(vmat);
+  return status;
+}
+
 /* Threads OpenMP will use (1 without OpenMP); reported by the CPU baseline. */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

@@ -88,3 +88,22 @@ def test_bwd_rejects_unsupported_head_dim():
     with pytest.raises(fa2.Fa2Error) as e:
         fa2.fa2_bwd(q, q.clone(), q.clone(), q.clone(), torch.zeros(1, 1, 64, device="cuda"), q.clone())
     assert e.value.code == fa2.FA2_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("index", [2, 3])
+def test_bwd_workload_heads(index):
+    """The full workload's backward in the benchmark's launch configuration;
+    two whole heads (first and last) checked against the oracle."""
+    w = sy.WORKLOADS[index]
+    q, k, v = w.inputs()
+    dout = sy.make_qkv(w.B, w.H, w.N, w.d, w.dtype, w.seed(0) + 500)[0]
+    tq, tk, tv, tdo = (to_dev(x, w.dtype) for x in (q, k, v, dout))
+    o, lse = fa2.fa2_fwd(tq, tk, tv, scale=w.scale, causal=w.causal)
+    dq, dk, dv = fa2.fa2_bwd(tq, tk, tv, o, lse, tdo, scale=w.scale, causal=w.causal)
+    torch.cuda.synchronize()
+    assert fa2.fa2_get_device_status()[0] == fa2.FA2_OK
+    got_all = [g.double().cpu().numpy() for g in (dq, dk, dv)]
+    for b, h in ((0, 0), (w.B - 1, w.H - 1)):
+        sl = lambda x: np.ascontiguousarray(x[b:b + 1, h:h + 1])
+        ref = oracle.attention_bwd(sl(q), sl(k), sl(v), sl(dout), w.dtype, w.scale, w.causal)
+        check([g[b:b + 1, h:h + 1] for g in got_all], ref, w.dtype, "%s head (%d,%d)" % (w.name, b, h))
