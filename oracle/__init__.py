@@ -66,8 +66,12 @@ def _load():
                                              ctypes.c_int, pd, pd, pd, pd, ctypes.c_int]
         lib.oracle_attention_bwd.restype = ctypes.c_int
         lib.oracle_attention_fwd_masked.argtypes = [p16, p16, p16, ctypes.c_int, i64, i64, i64, i64, i64,
-                                                    ctypes.c_double, i64, i64, pd, pd, ctypes.c_int]
+                                                    ctypes.c_double, i64, i64, i64, pd, pd, ctypes.c_int]
         lib.oracle_attention_fwd_masked.restype = ctypes.c_int
+        lib.oracle_attention_rows_masked.argtypes = [p16, p16, p16, ctypes.c_int, i64, i64, i64, i64, i64,
+                                                     ctypes.c_double, i64, i64, i64, pi64, pi64, i64, pd, pd,
+                                                     ctypes.c_int]
+        lib.oracle_attention_rows_masked.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -185,26 +189,52 @@ def attention_bwd(q, k, v, dout, dtype: int, scale: float, causal: bool, threads
     return dq, dk, dv, delta
 
 
-def attention_fwd_masked(q, k, v, dtype: int, scale: float, window_left: int = -1, window_right: int = -1,
-                         threads: int = 0):
-    """Forward with a band mask and N_q != N_k: q [B,H,Nq,d], k, v [B,H,Nk,d] (16-bit bit patterns).
-
-    Key j is visible to query i iff j >= i + (Nk - Nq) - window_left and
-    j <= i + (Nk - Nq) + window_right (a negative window is unbounded on that
-    side; causal is window_right = 0).  Rows with nothing visible: O = 0,
-    L = -inf.  Returns float64 (O [B,H,Nq,d], L [B,H,Nq]).
-    """
+def _masked_shapes(q, k, v):
     q, k, v = _bits(q), _bits(k), _bits(v)
     B, H, Nq, d = q.shape
     Nk = k.shape[2]
     if k.shape != (B, H, Nk, d) or v.shape != k.shape:
         raise ValueError("k, v must be [B,H,Nk,d] with q's B, H, d")
+    return q, k, v, B, H, Nq, Nk, d
+
+
+def attention_fwd_masked(q, k, v, dtype: int, scale: float, window_left: int = -1, window_right: int = -1,
+                         prefix_len: int = 0, threads: int = 0):
+    """Forward with a band / prefix mask and N_q != N_k: q [B,H,Nq,d], k, v [B,H,Nk,d] (16-bit bit patterns).
+
+    Key j is visible to query i iff j < prefix_len, or j >= i + (Nk - Nq) -
+    window_left and j <= i + (Nk - Nq) + window_right (a negative window is
+    unbounded on that side; causal is window_right = 0).  Rows with nothing
+    visible: O = 0, L = -inf.  Returns float64 (O [B,H,Nq,d], L [B,H,Nq]).
+    """
+    q, k, v, B, H, Nq, Nk, d = _masked_shapes(q, k, v)
     o = np.empty((B, H, Nq, d))
     lse = np.empty((B, H, Nq))
     rc = _load().oracle_attention_fwd_masked(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
                                              _ptr(v, ctypes.c_uint16), int(dtype), B, H, Nq, Nk, d, float(scale),
-                                             int(window_left), int(window_right), _ptr(o, ctypes.c_double),
-                                             _ptr(lse, ctypes.c_double), int(threads))
+                                             int(window_left), int(window_right), int(prefix_len),
+                                             _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double), int(threads))
     if rc:
         raise ValueError("oracle_attention_fwd_masked failed (%d)" % rc)
+    return o, lse
+
+
+def attention_rows_masked(q, k, v, dtype: int, scale: float, bh_idx, row_idx, window_left: int = -1,
+                          window_right: int = -1, prefix_len: int = 0, threads: int = 0):
+    """attention_fwd_masked at sampled (bh, row) pairs: O rows [count, d] and L [count], float64."""
+    q, k, v, B, H, Nq, Nk, d = _masked_shapes(q, k, v)
+    bh_idx = np.ascontiguousarray(bh_idx, dtype=np.int64)
+    row_idx = np.ascontiguousarray(row_idx, dtype=np.int64)
+    count = bh_idx.size
+    if row_idx.size != count:
+        raise ValueError("bh_idx and row_idx must have one length")
+    o = np.empty((count, d))
+    lse = np.empty((count,))
+    rc = _load().oracle_attention_rows_masked(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
+                                              _ptr(v, ctypes.c_uint16), int(dtype), B, H, Nq, Nk, d, float(scale),
+                                              int(window_left), int(window_right), int(prefix_len),
+                                              _ptr(bh_idx, ctypes.c_int64), _ptr(row_idx, ctypes.c_int64), count,
+                                              _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double), int(threads))
+    if rc:
+        raise ValueError("oracle_attention_rows_masked failed (%d)" % rc)
     return o, lse

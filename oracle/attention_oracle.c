@@ -373,30 +373,82 @@ int oracle_attention_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v
 /* ------------------------------------------------------------------ masks and N_q != N_k */
 
 /*
- * Forward with a general band mask and separate query / key lengths.  Query
- * i (0 <= i < Nq) and key j (0 <= j < Nk) are aligned at the end of the key
+ * Forward with a general mask and separate query / key lengths.  Query i
+ * (0 <= i < Nq) and key j (0 <= j < Nk) are aligned at the end of the key
  * sequence (offset off = Nk - Nq, so the last query faces the last key), and
  * key j is visible iff
  *
- *     j >= i + off - window_left    (when window_left >= 0)
- *     j <= i + off + window_right   (when window_right >= 0; causal is window_right = 0)
+ *     j < prefix_len                           (keys every query sees), or
+ *     j >= i + off - window_left               (when window_left >= 0) and
+ *     j <= i + off + window_right              (when window_right >= 0; causal is window_right = 0)
  *
  * -- the additive 0 / -inf mask of the Flash Attention 2 page ("Causal
- * masking", Option A: sliding windows and the like are a 0/-inf add before
- * softmax).  A row that sees no key has O = 0 and L = -inf.  q: [B,H,Nq,d],
- * k, v: [B,H,Nk,d]; o: [B,H,Nq,d], lse: [B,H,Nq].
+ * masking", Option A: sliding windows, prefix-LM and the like are a 0/-inf
+ * add before softmax).  A row that sees no key has O = 0 and L = -inf.
  */
+static int key_visible(int64_t i, int64_t j, int64_t off, int64_t window_left, int64_t window_right,
+                       int64_t prefix_len) {
+  if (j < prefix_len) return 1;
+  if (window_left >= 0 && j < i + off - window_left) return 0;
+  if (window_right >= 0 && j > i + off + window_right) return 0;
+  return 1;
+}
+
+/* One output row by the definition: s_j = scale q.k_j over the visible keys,
+ * P = softmax(s), o = sum_j P_j v_j, L = m + ln sum_j exp(s_j - m).  kmat,
+ * vmat: [Nk, d] float64; srow: Nk scratch. */
+static void masked_row(const double* qrow, const double* kmat, const double* vmat, int64_t i, int64_t Nq, int64_t Nk,
+                       int64_t d, double scale, int64_t window_left, int64_t window_right, int64_t prefix_len,
+                       double* srow, double* orow, double* lse) {
+  const int64_t off = Nk - Nq;
+  double m = -INFINITY;
+  int64_t seen = 0;
+  for (int64_t j = 0; j < Nk; ++j) {
+    if (!key_visible(i, j, off, window_left, window_right, prefix_len)) continue;
+    double acc = 0.0;
+    for (int64_t c = 0; c < d; ++c) acc += qrow[c] * kmat[j * d + c];
+    srow[j] = scale * acc;
+    if (srow[j] > m) m = srow[j];
+    ++seen;
+  }
+  for (int64_t c = 0; c < d; ++c) orow[c] = 0.0;
+  if (seen == 0) {
+    *lse = -INFINITY;
+    return;
+  }
+  double sum = 0.0;
+  for (int64_t j = 0; j < Nk; ++j) {
+    if (!key_visible(i, j, off, window_left, window_right, prefix_len)) continue;
+    srow[j] = exp(srow[j] - m);
+    sum += srow[j];
+  }
+  for (int64_t j = 0; j < Nk; ++j) {
+    if (!key_visible(i, j, off, window_left, window_right, prefix_len)) continue;
+    const double pj = srow[j] / sum;
+    for (int64_t c = 0; c < d; ++c) orow[c] += pj * vmat[j * d + c];
+  }
+  *lse = m + log(sum);
+}
+
+static int masked_args_ok(const uint16_t* q, const uint16_t* k, const uint16_t* v, int dtype, int64_t B, int64_t H,
+                          int64_t Nq, int64_t Nk, int64_t d, double scale, int64_t prefix_len) {
+  if (!q || !k || !v || (dtype != ORACLE_FP16 && dtype != ORACLE_BF16)) return 0;
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1 || !isfinite(scale) || prefix_len < 0) return 0;
+  return 1;
+}
+
+/* q: [B,H,Nq,d], k, v: [B,H,Nk,d] (16-bit bit patterns); o: [B,H,Nq,d], lse: [B,H,Nq]. */
 int oracle_attention_fwd_masked(const uint16_t* q, const uint16_t* k, const uint16_t* v, int dtype, int64_t B,
                                 int64_t H, int64_t Nq, int64_t Nk, int64_t d, double scale, int64_t window_left,
-                                int64_t window_right, double* o_out, double* lse_out, int threads) {
-  if (!q || !k || !v || !o_out || !lse_out || (dtype != ORACLE_FP16 && dtype != ORACLE_BF16)) return ORACLE_ERR_ARG;
-  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1 || !isfinite(scale)) return ORACLE_ERR_ARG;
+                                int64_t window_right, int64_t prefix_len, double* o_out, double* lse_out,
+                                int threads) {
+  if (!masked_args_ok(q, k, v, dtype, B, H, Nq, Nk, d, scale, prefix_len) || !o_out || !lse_out)
+    return ORACLE_ERR_ARG;
 #ifdef _OPENMP
   if (threads > 0) omp_set_num_threads(threads);
 #else
   (void)threads;
 #endif
-  const int64_t off = Nk - Nq;
   double* kmat = (double*)malloc(sizeof(double) * (size_t)(Nk * d));
   double* vmat = (double*)malloc(sizeof(double) * (size_t)(Nk * d));
   if (!kmat || !vmat) { free(kmat); free(vmat); return ORACLE_ERR_NOMEM; }
@@ -417,32 +469,8 @@ int oracle_attention_fwd_masked(const uint16_t* q, const uint16_t* k, const uint
 #pragma omp for schedule(dynamic, 4)
         for (int64_t i = 0; i < Nq; ++i) {
           for (int64_t c = 0; c < d; ++c) qrow[c] = widen(q[(bh * Nq + i) * d + c], dtype);
-          int64_t lo = 0, hi = Nk - 1;
-          if (window_left >= 0 && i + off - window_left > lo) lo = i + off - window_left;
-          if (window_right >= 0 && i + off + window_right < hi) hi = i + off + window_right;
-          double* orow = o_out + (bh * Nq + i) * d;
-          double m = -INFINITY;
-          for (int64_t j = lo; j <= hi; ++j) {
-            double acc = 0.0;
-            for (int64_t c = 0; c < d; ++c) acc += qrow[c] * kmat[j * d + c];
-            srow[j] = scale * acc;
-            if (srow[j] > m) m = srow[j];
-          }
-          for (int64_t c = 0; c < d; ++c) orow[c] = 0.0;
-          if (hi < lo) {
-            lse_out[bh * Nq + i] = -INFINITY;
-            continue;
-          }
-          double sum = 0.0;
-          for (int64_t j = lo; j <= hi; ++j) {
-            srow[j] = exp(srow[j] - m);
-            sum += srow[j];
-          }
-          for (int64_t j = lo; j <= hi; ++j) {
-            const double pj = srow[j] / sum;
-            for (int64_t c = 0; c < d; ++c) orow[c] += pj * vmat[j * d + c];
-          }
-          lse_out[bh * Nq + i] = m + log(sum);
+          masked_row(qrow, kmat, vmat, i, Nq, Nk, d, scale, window_left, window_right, prefix_len, srow,
+                     o_out + (bh * Nq + i) * d, lse_out + bh * Nq + i);
         }
       }
       free(srow);
@@ -453,6 +481,57 @@ int oracle_attention_fwd_masked(const uint16_t* q, const uint16_t* k, const uint
   free(kmat);
   free(vmat);
   return status;
+}
+
+/* The same definition at sampled (bh, row) pairs only: o: [count, d],
+ * lse: [count].  For problems too large to evaluate whole. */
+int oracle_attention_rows_masked(const uint16_t* q, const uint16_t* k, const uint16_t* v, int dtype, int64_t B,
+                                 int64_t H, int64_t Nq, int64_t Nk, int64_t d, double scale, int64_t window_left,
+                                 int64_t window_right, int64_t prefix_len, const int64_t* bh_idx,
+                                 const int64_t* row_idx, int64_t count, double* o_out, double* lse_out,
+                                 int threads) {
+  if (!masked_args_ok(q, k, v, dtype, B, H, Nq, Nk, d, scale, prefix_len) || !o_out || !lse_out || count < 0 ||
+      (count > 0 && (!bh_idx || !row_idx)))
+    return ORACLE_ERR_ARG;
+  for (int64_t s = 0; s < count; ++s)
+    if (bh_idx[s] < 0 || bh_idx[s] >= B * H || row_idx[s] < 0 || row_idx[s] >= Nq) return ORACLE_ERR_ARG;
+#ifdef _OPENMP
+  if (threads > 0) omp_set_num_threads(threads);
+#else
+  (void)threads;
+#endif
+  int nomem = 0;
+#pragma omp parallel reduction(| : nomem)
+  {
+    double* kmat = (double*)malloc(sizeof(double) * (size_t)(Nk * d));
+    double* vmat = (double*)malloc(sizeof(double) * (size_t)(Nk * d));
+    double* srow = (double*)malloc(sizeof(double) * (size_t)Nk);
+    double* qrow = (double*)malloc(sizeof(double) * (size_t)d);
+    int64_t have = -1;  /* the (b,h) whose K and V are widened in kmat / vmat */
+    if (!kmat || !vmat || !srow || !qrow) {
+      nomem = 1;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t s = 0; s < count; ++s) {
+        const int64_t bh = bh_idx[s], i = row_idx[s];
+        if (bh != have) {
+          for (int64_t x = 0; x < Nk * d; ++x) {
+            kmat[x] = widen(k[bh * Nk * d + x], dtype);
+            vmat[x] = widen(v[bh * Nk * d + x], dtype);
+          }
+          have = bh;
+        }
+        for (int64_t c = 0; c < d; ++c) qrow[c] = widen(q[(bh * Nq + i) * d + c], dtype);
+        masked_row(qrow, kmat, vmat, i, Nq, Nk, d, scale, window_left, window_right, prefix_len, srow,
+                   o_out + s * d, lse_out + s);
+      }
+    }
+    free(kmat);
+    free(vmat);
+    free(srow);
+    free(qrow);
+  }
+  return nomem ? ORACLE_ERR_NOMEM : ORACLE_OK;
 }
 
 /* Threads OpenMP will use (1 without OpenMP); reported by the CPU baseline. */

@@ -92,3 +92,81 @@ def test_brute_force_band():
             assert o[0, 0, i, c] == pytest.approx(float(sum(e * Decimal(repr(float(V[j, c]))) for j, e in ex) / tot),
                                                   abs=1e-13)
         assert lse[0, 0, i] == pytest.approx(float(tot.ln()), abs=1e-13)
+
+
+# ---------------------------------------------------------------- prefix (prefix-LM) and sampled rows
+
+
+def _row_over_keys(q, k, v, dtype, scale, i, keys):
+    """Row i attending to exactly the key indices `keys`, as the last row of an
+    unmasked square problem over those keys (pinned full-attention definition)."""
+    keys = np.asarray(keys, dtype=np.int64)
+    qs = np.repeat(q[:, :, i:i + 1], keys.size, axis=2)
+    so, sl = oracle.attention_fwd(qs, np.ascontiguousarray(k[:, :, keys]), np.ascontiguousarray(v[:, :, keys]), dtype,
+                                  scale, False)
+    return so[:, :, -1], sl[:, :, -1]
+
+
+@pytest.mark.parametrize("wl,wr", [(-1, 0), (3, 0), (0, 0), (2, 5)])
+def test_prefix_covering_all_keys_is_full_attention(wl, wr):
+    q, k, v = _qkv(1, 2, 23, 23, 8, sy.FP16, 11)
+    a = oracle.attention_fwd_masked(q, k, v, sy.FP16, 0.3, window_left=wl, window_right=wr, prefix_len=23)
+    b = oracle.attention_fwd(q, k, v, sy.FP16, 0.3, False)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("dtype", [sy.FP16, sy.BF16])
+def test_prefix_lm_splits_into_full_prefix_and_causal_rest(dtype):
+    """Causal with prefix P (N_q = N_k = N): rows i < P see exactly keys [0, P)
+    (full attention on the first P rows and keys); rows i >= P see [0, i]
+    (the causal rows)."""
+    N, P = 31, 9
+    q, k, v = _qkv(2, 1, N, N, 8, dtype, 13)
+    o, lse = oracle.attention_fwd_masked(q, k, v, dtype, 0.45, window_left=-1, window_right=0, prefix_len=P)
+    fo, fl = oracle.attention_fwd(np.ascontiguousarray(q[:, :, :P]), np.ascontiguousarray(k[:, :, :P]),
+                                  np.ascontiguousarray(v[:, :, :P]), dtype, 0.45, False)
+    co, cl = oracle.attention_fwd(q, k, v, dtype, 0.45, True)
+    np.testing.assert_allclose(o[:, :, :P], fo, atol=1e-14, rtol=0)
+    np.testing.assert_allclose(lse[:, :, :P], fl, atol=1e-14, rtol=0)
+    np.testing.assert_array_equal(o[:, :, P:], co[:, :, P:])
+    np.testing.assert_array_equal(lse[:, :, P:], cl[:, :, P:])
+
+
+@pytest.mark.parametrize("Nq,Nk,wl,wr,P", [(20, 20, 2, 0, 3), (12, 30, 4, 1, 5), (30, 12, 1, 0, 2)])
+def test_prefix_with_window_sees_the_union_of_both_key_sets(Nq, Nk, wl, wr, P):
+    """A window that leaves a gap after the prefix: row i sees [0, P) plus its
+    band, by the unmasked definition over exactly that key set."""
+    q, k, v = _qkv(1, 2, Nq, Nk, 5, sy.BF16, 17)
+    o, lse = oracle.attention_fwd_masked(q, k, v, sy.BF16, 0.6, window_left=wl, window_right=wr, prefix_len=P)
+    off = Nk - Nq
+    for i in range(Nq):
+        band = set(range(max(0, i + off - wl), min(Nk - 1, i + off + wr) + 1))
+        keys = sorted(band | set(range(min(P, Nk))))
+        ro, rl = _row_over_keys(q, k, v, sy.BF16, 0.6, i, keys)
+        np.testing.assert_allclose(o[:, :, i], ro, atol=1e-14, rtol=0)
+        np.testing.assert_allclose(lse[:, :, i], rl, atol=1e-14, rtol=0)
+
+
+@pytest.mark.parametrize("Nq,Nk,wl,wr,P", [(40, 40, -1, -1, 0), (40, 40, -1, 0, 0), (50, 20, 6, 0, 0),
+                                           (20, 50, 3, 2, 4), (33, 33, -1, 0, 10)])
+def test_sampled_rows_equal_the_whole_problem(Nq, Nk, wl, wr, P):
+    q, k, v = _qkv(2, 3, Nq, Nk, 8, sy.FP16, 19)
+    o, lse = oracle.attention_fwd_masked(q, k, v, sy.FP16, 0.35, window_left=wl, window_right=wr, prefix_len=P)
+    rng = np.random.default_rng(5)
+    bh = rng.integers(0, 6, size=40)
+    rows = rng.integers(0, Nq, size=40)
+    so, sl = oracle.attention_rows_masked(q, k, v, sy.FP16, 0.35, bh, rows, window_left=wl, window_right=wr,
+                                          prefix_len=P)
+    np.testing.assert_array_equal(so, o.reshape(6, Nq, 8)[bh, rows])
+    np.testing.assert_array_equal(sl, lse.reshape(6, Nq)[bh, rows])
+
+
+def test_sampled_rows_reject_out_of_range_indices():
+    q, k, v = _qkv(1, 1, 8, 8, 4, sy.FP16, 21)
+    with pytest.raises(ValueError):
+        oracle.attention_rows_masked(q, k, v, sy.FP16, 1.0, [0], [8])
+    with pytest.raises(ValueError):
+        oracle.attention_rows_masked(q, k, v, sy.FP16, 1.0, [1], [0])
+    with pytest.raises(ValueError):
+        oracle.attention_fwd_masked(q, k, v, sy.FP16, 1.0, prefix_len=-1)
