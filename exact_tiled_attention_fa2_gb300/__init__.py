@@ -23,9 +23,28 @@ FA2_ERR_MISALIGNED = 3
 FA2_ERR_CUDA = 4
 FA2_ERR_DEVICE_TIMEOUT = 5
 FA2_ERR_SCRATCH_LIMIT = 6
+FA2_ERR_DEVICE_SEQLENS = 7
 FA2_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _lib = None
+
+
+class Fa2FwdParams(ctypes.Structure):
+    """Mirror of ``fa2_fwd_params`` in include/fa2.h (checked against the library's sizeof)."""
+
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("batch", ctypes.c_int), ("heads", ctypes.c_int),
+        ("seqlen_q", ctypes.c_int), ("seqlen_k", ctypes.c_int),
+        ("head_dim", ctypes.c_int), ("dtype", ctypes.c_int), ("scale", ctypes.c_float),
+        ("window_left", ctypes.c_int), ("window_right", ctypes.c_int), ("prefix_len", ctypes.c_int),
+        ("q_strides", ctypes.c_int64 * 3), ("k_strides", ctypes.c_int64 * 3),
+        ("v_strides", ctypes.c_int64 * 3), ("o_strides", ctypes.c_int64 * 3),
+        ("lse_strides", ctypes.c_int64 * 2),
+        ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
+        ("total_q", ctypes.c_int), ("total_k", ctypes.c_int),
+    ]
 
 
 class Fa2Error(RuntimeError):
@@ -66,6 +85,13 @@ def load_library():
     lib.fa2_status_string.restype = ctypes.c_char_p
     lib.fa2_version.argtypes = []
     lib.fa2_version.restype = ci
+    lib.fa2_fwd_params_size.argtypes = []
+    lib.fa2_fwd_params_size.restype = sz
+    lib.fa2_fwd_ex.argtypes = [ctypes.POINTER(Fa2FwdParams), vp]
+    lib.fa2_fwd_ex.restype = ci
+    if lib.fa2_fwd_params_size() != ctypes.sizeof(Fa2FwdParams):
+        raise RuntimeError("fa2_fwd_params layout mismatch: library %d bytes, binding %d bytes"
+                           % (lib.fa2_fwd_params_size(), ctypes.sizeof(Fa2FwdParams)))
     _lib = lib
     return lib
 
@@ -122,6 +148,83 @@ def fa2_fwd(q, k, v, o=None, lse=None, scale=None, causal=False, stream=None):
                                 _stream_handle(stream, q.device))
     if rc:
         raise Fa2Error(rc, "fa2_fwd")
+    return o, lse
+
+
+def fa2_fwd_ex(q, k, v, o=None, lse=None, scale=None, window_left=-1, window_right=-1, prefix_len=0,
+               cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, stream=None):
+    """General forward (fa2_fwd_ex): strided views, N_q != N_k, band / prefix masks, packed batches.
+
+    Unpacked: q [B, H, N_q, d], k and v [B, H, N_k, d], any CUDA views whose
+    last dimension is contiguous (e.g. ``x.transpose(1, 2)`` of a [B, N, H, d]
+    tensor); o (default: new contiguous [B, H, N_q, d]) and lse (default: new
+    [B, H, N_q] float32) may be views too.
+
+    Packed (cu_seqlens_q and cu_seqlens_k, int32 CUDA [B + 1]): q [total_q, H, d],
+    k and v [total_k, H, d]; o [total_q, H, d] and lse [H, total_q] by default;
+    ``max_seqlen_q`` (default: total_q) bounds every sequence's query count.
+
+    Query i of a sequence sees key j iff j < prefix_len or
+    i + off - window_left <= j <= i + off + window_right, off = N_k - N_q
+    (-1 = unbounded).  causal is window (-1, 0).  Returns (o, lse).
+    """
+    import torch
+    packed = cu_seqlens_q is not None or cu_seqlens_k is not None
+    if packed and (cu_seqlens_q is None or cu_seqlens_k is None):
+        raise ValueError("give both cu_seqlens_q and cu_seqlens_k, or neither")
+    for t in (q, k, v):
+        if not t.is_cuda or t.stride(-1) != 1:
+            raise ValueError("q, k, v must be CUDA tensors with a contiguous last dimension")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    d = q.shape[-1]
+    p = Fa2FwdParams()
+    if packed:
+        if q.dim() != 3 or k.dim() != 3 or v.shape != k.shape or k.shape[1:] != q.shape[1:]:
+            raise ValueError("packed q must be [total_q, H, d] and k, v [total_k, H, d]")
+        for c in (cu_seqlens_q, cu_seqlens_k):
+            if not c.is_cuda or c.dtype != torch.int32 or c.dim() != 1 or not c.is_contiguous():
+                raise ValueError("cu_seqlens must be contiguous int32 CUDA tensors [B + 1]")
+        total_q, H, _ = q.shape
+        total_k = k.shape[0]
+        B = cu_seqlens_q.numel() - 1
+        if cu_seqlens_k.numel() != B + 1:
+            raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
+        if o is None:
+            o = torch.empty_like(q, memory_format=torch.contiguous_format)
+        if lse is None:
+            lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
+        n_q = total_q if max_seqlen_q is None else int(max_seqlen_q)
+        p.batch, p.heads, p.seqlen_q, p.seqlen_k = B, H, n_q, 0
+        p.total_q, p.total_k = total_q, total_k
+        for name, t in (("q_strides", q), ("k_strides", k), ("v_strides", v), ("o_strides", o)):
+            getattr(p, name)[:] = [0, t.stride(1), t.stride(0)]
+        p.lse_strides[:] = [0, lse.stride(0)]
+        p.cu_seqlens_q = cu_seqlens_q.data_ptr()
+        p.cu_seqlens_k = cu_seqlens_k.data_ptr()
+    else:
+        if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape or k.shape[:2] != q.shape[:2] or k.shape[3] != d:
+            raise ValueError("q must be [B, H, N_q, d] and k, v [B, H, N_k, d]")
+        B, H, n_q, _ = q.shape
+        if o is None:
+            o = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+        if lse is None:
+            lse = torch.empty((B, H, n_q), dtype=torch.float32, device=q.device)
+        if lse.stride(-1) != 1:
+            raise ValueError("lse must have a contiguous last dimension")
+        p.batch, p.heads, p.seqlen_q, p.seqlen_k = B, H, n_q, k.shape[2]
+        for name, t in (("q_strides", q), ("k_strides", k), ("v_strides", v), ("o_strides", o)):
+            getattr(p, name)[:] = [t.stride(0), t.stride(1), t.stride(2)]
+        p.lse_strides[:] = [lse.stride(0), lse.stride(1)]
+    if o.dtype != q.dtype or o.stride(-1) != 1 or lse.dtype != torch.float32:
+        raise ValueError("o must share q's dtype with a contiguous last dimension; lse must be float32")
+    p.q, p.k, p.v, p.o, p.lse = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr()
+    p.head_dim, p.dtype = d, _dtype_code(q)
+    p.scale = 1.0 / float(d) ** 0.5 if scale is None else float(scale)
+    p.window_left, p.window_right, p.prefix_len = int(window_left), int(window_right), int(prefix_len)
+    rc = load_library().fa2_fwd_ex(ctypes.byref(p), _stream_handle(stream, q.device))
+    if rc:
+        raise Fa2Error(rc, "fa2_fwd_ex")
     return o, lse
 
 

@@ -24,6 +24,7 @@ TileGeometry tile_geometry(int d) {
   TileGeometry g;
   g.q_rows = 128;
   g.kv_rows = (d == 256) ? 64 : 128;
+  g.cta_rows = (d == 256) ? 128 : 256;
   return g;
 }
 
@@ -75,8 +76,79 @@ int device_state(DeviceState** out) {
   return FA2_OK;
 }
 
-// [B*H, N, d] view of a [B,H,N,d] tensor; boxes of 64 columns x `rows` rows,
-// 128-byte swizzle.  Rows past N read as zeros (and are clipped on store).
+// Whether (batch, head) of a tensor with element strides st = {batch, head,
+// row} can be addressed as one coordinate b*H + h with a single stride.
+bool mergeable(long long heads, long long batch, const long long st[3]) {
+  return heads == 1 || batch == 1 || st[0] == heads * st[1];
+}
+
+// View of a 16-bit tensor with element strides st = {batch, head, row}: 3-D
+// (d, rows, heads*batch) when `merged` (see mergeable), else 4-D (d, rows,
+// heads, batch); boxes of 64 columns x `box_rows` rows, 128-byte swizzle.
+// Rows past `rows` read as zeros.  The stride of a dimension of size 1 never
+// addresses anything and is replaced by a valid placeholder.
+int encode_map_rows(CUtensorMap* m, const void* base, int d, long long rows, long long heads, long long batch,
+                    const long long st[3], int box_rows, bool bf16, bool merged) {
+  const long long row_st = rows > 1 ? st[2] : d, head_st = heads > 1 ? st[1] : d, batch_st = batch > 1 ? st[0] : d;
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads, (cuuint64_t)batch};
+  cuuint64_t strides[3] = {(cuuint64_t)row_st * 2, (cuuint64_t)head_st * 2, (cuuint64_t)batch_st * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  cuuint32_t rank = 4;
+  if (merged) {
+    dims[2] = (cuuint64_t)(heads * batch);
+    strides[1] = (cuuint64_t)(heads > 1 ? head_st : batch_st) * 2;
+    rank = 3;
+  }
+  CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rank,
+                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA2_OK : FA2_ERR_CUDA;
+}
+
+// Everything the forward tensor maps depend on.  Zero-filled before use so
+// that whole-struct comparison is exact.
+struct MapKey {
+  int dev, dtype, d, merged;
+  const void* ptr[3];        // q, k, v
+  long long dims[3][3];      // rows, heads, batch of each
+  long long strides[3][3];   // batch, head, row strides of each (elements)
+};
+
+// The tensor maps of the last forward call on this host thread: repeated
+// calls on the same buffers and shapes (the usual case in a loop) skip
+// re-encoding them.
+struct MapCache {
+  bool valid = false;
+  MapKey key;
+  CUtensorMap tm_q, tm_k, tm_v;
+};
+thread_local MapCache t_maps;
+
+int cached_maps(LaunchArgs& a, const MapKey& key) {
+  MapCache& c = t_maps;
+  if (!(c.valid && std::memcmp(&c.key, &key, sizeof(MapKey)) == 0)) {
+    const bool bf16 = key.dtype == FA2_BF16;
+    const TileGeometry g = tile_geometry(key.d);
+    CUtensorMap* maps[3] = {&c.tm_q, &c.tm_k, &c.tm_v};
+    c.valid = false;
+    for (int i = 0; i < 3; ++i) {
+      if (encode_map_rows(maps[i], key.ptr[i], key.d, key.dims[i][0], key.dims[i][1], key.dims[i][2],
+                          key.strides[i], i == 0 ? g.q_rows : g.kv_rows, bf16, key.merged != 0))
+        return FA2_ERR_CUDA;
+    }
+    std::memcpy(&c.key, &key, sizeof(MapKey));
+    c.valid = true;
+  }
+  a.tm_q = c.tm_q;
+  a.tm_k = c.tm_k;
+  a.tm_v = c.tm_v;
+  return FA2_OK;
+}
+
+// [B*H, N, d] view of a contiguous [B,H,N,d] tensor; boxes of 64 columns x
+// `rows` rows, 128-byte swizzle (the backward kernels' maps).
 int encode_map(CUtensorMap* m, const void* base, int bh, int n, int d, int rows, bool bf16) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)n * (cuuint64_t)d * 2};
@@ -87,44 +159,6 @@ int encode_map(CUtensorMap* m, const void* base, int bh, int n, int d, int rows,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA2_OK : FA2_ERR_CUDA;
-}
-
-// The tensor maps of the last call on this host thread: repeated calls on the
-// same buffers and sizes (the usual case in a loop) skip re-encoding them.
-struct MapCache {
-  bool valid = false;
-  int dev = -1, bh = 0, n = 0, d = 0, dtype = -1;
-  const void *q = nullptr, *k = nullptr, *v = nullptr;
-  CUtensorMap tm_q, tm_k, tm_v;
-};
-thread_local MapCache t_maps;
-
-int cached_maps(LaunchArgs& a, const void* q, const void* k, const void* v, int bh, int n, int d, int dtype) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FA2_ERR_CUDA;
-  MapCache& c = t_maps;
-  if (!(c.valid && c.dev == dev && c.q == q && c.k == k && c.v == v && c.bh == bh && c.n == n && c.d == d &&
-        c.dtype == dtype)) {
-    const bool bf16 = dtype == FA2_BF16;
-    const TileGeometry g = tile_geometry(d);
-    c.valid = false;
-    if (encode_map(&c.tm_q, q, bh, n, d, g.q_rows, bf16) || encode_map(&c.tm_k, k, bh, n, d, g.kv_rows, bf16) ||
-        encode_map(&c.tm_v, v, bh, n, d, g.kv_rows, bf16))
-      return FA2_ERR_CUDA;
-    c.dev = dev;
-    c.q = q;
-    c.k = k;
-    c.v = v;
-    c.bh = bh;
-    c.n = n;
-    c.d = d;
-    c.dtype = dtype;
-    c.valid = true;
-  }
-  a.tm_q = c.tm_q;
-  a.tm_k = c.tm_k;
-  a.tm_v = c.tm_v;
-  return FA2_OK;
 }
 
 // fp32 [B*H, N, d] view of the dQ accumulator; boxes of 32 columns x 32 rows
@@ -167,47 +201,209 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 using namespace fa2;
 
+namespace fa2 {
+namespace {
+
+// Byte range [base, base + span) a strided 16-bit tensor (or float32 when
+// elem == 4) can touch: dims = {batch, heads, rows}, strides in elements,
+// `inner` contiguous elements per row.
+struct Extent {
+  const void* base;
+  size_t bytes;
+};
+
+Extent extent(const void* base, const long long dims[3], const long long st[3], long long inner, int elem) {
+  long long last = inner - 1;
+  for (int i = 0; i < 3; ++i)
+    if (dims[i] > 1) last += (dims[i] - 1) * st[i];
+  return Extent{base, (size_t)(last + 1) * (size_t)elem};
+}
+
+bool overlap(const Extent& a, const Extent& b) { return ranges_overlap(a.base, a.bytes, b.base, b.bytes); }
+
+constexpr long long kMaxStride = 1ll << 39;  // elements: 16-bit strides stay below the TMA limit of 2^40 bytes
+
+// 0, or the status for a stride of a dimension of size n.
+int check_stride(long long n, long long st, bool tma) {
+  if (n <= 1) return FA2_OK;
+  if (st <= 0 || st >= kMaxStride) return FA2_ERR_INVALID_ARG;
+  if (tma && (st & 7)) return FA2_ERR_MISALIGNED;
+  return FA2_OK;
+}
+
+int forward_checked(const fa2_fwd_params& a, cudaStream_t stream);
+
+// Validates the general forward arguments (no CUDA call), then launches.  A
+// batch whose (batch, head) strides merge in every tensor (batch stride =
+// H x head stride, as in contiguous [B,H,N,d]) runs as one batch of B*H heads.
+int forward(const fa2_fwd_params& a_in, cudaStream_t stream) {
+  fa2_fwd_params a = a_in;
+  const bool packed = a.cu_seqlens_q != nullptr || a.cu_seqlens_k != nullptr;
+  if (!packed && a.batch > 1 && a.heads > 1) {
+    const int64_t* st[4] = {a.q_strides, a.k_strides, a.v_strides, a.o_strides};
+    bool fold = a.lse_strides[0] == (int64_t)a.heads * a.lse_strides[1];
+    for (const int64_t* s : st) fold = fold && s[0] == (int64_t)a.heads * s[1];
+    if (fold && (long long)a.batch * a.heads <= INT_MAX) {
+      a.heads *= a.batch;
+      a.batch = 1;
+    }
+  }
+  return forward_checked(a, stream);
+}
+
+int forward_checked(const fa2_fwd_params& a, cudaStream_t stream) {
+  if (a.dtype != FA2_FP16 && a.dtype != FA2_BF16) return FA2_ERR_INVALID_ARG;
+  if (a.batch < 1 || a.heads < 1 || a.seqlen_q < 1) return FA2_ERR_INVALID_ARG;
+  if (!std::isfinite(a.scale) || !(a.scale > 0.f)) return FA2_ERR_INVALID_ARG;
+  if (a.window_left < -1 || a.window_right < -1 || a.prefix_len < 0) return FA2_ERR_INVALID_ARG;
+  const int d = a.head_dim;
+  if (d != 64 && d != 128 && d != 256) return FA2_ERR_UNSUPPORTED;
+  const bool packed = a.cu_seqlens_q != nullptr || a.cu_seqlens_k != nullptr;
+  if (packed && !(a.cu_seqlens_q && a.cu_seqlens_k)) return FA2_ERR_INVALID_ARG;
+  if (packed ? (a.total_q < 1 || a.total_k < 1) : a.seqlen_k < 1) return FA2_ERR_INVALID_ARG;
+  if (!a.q || !a.k || !a.v || !a.o || !a.lse) return FA2_ERR_INVALID_ARG;
+  if (misaligned(a.q) || misaligned(a.k) || misaligned(a.v) || misaligned(a.o)) return FA2_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(a.lse) & 3u) return FA2_ERR_MISALIGNED;
+  if (packed && ((reinterpret_cast<uintptr_t>(a.cu_seqlens_q) | reinterpret_cast<uintptr_t>(a.cu_seqlens_k)) & 3u))
+    return FA2_ERR_MISALIGNED;
+  const TileGeometry g = tile_geometry(d);
+  const long long units = ((long long)a.seqlen_q + g.cta_rows - 1) / g.cta_rows;
+  if ((long long)a.batch * a.heads * units > INT_MAX) return FA2_ERR_UNSUPPORTED;
+
+  // tensor batch dimension (1 when packed: sequences are rows) and row counts
+  const long long tb = packed ? 1 : a.batch;
+  const long long rows_q = packed ? a.total_q : a.seqlen_q;
+  const long long rows_k = packed ? a.total_k : a.seqlen_k;
+  const long long dq[3] = {tb, a.heads, rows_q}, dk[3] = {tb, a.heads, rows_k};
+  long long st_in[3][3];
+  const int64_t* st_src[3] = {a.q_strides, a.k_strides, a.v_strides};
+  for (int t = 0; t < 3; ++t)
+    for (int i = 0; i < 3; ++i) st_in[t][i] = (long long)st_src[t][i];
+  for (int t = 0; t < 3; ++t) {
+    const long long* dims = t == 0 ? dq : dk;
+    for (int i = 0; i < 3; ++i) {
+      const int rc = check_stride(dims[i], st_in[t][i], true);
+      if (rc) return rc;
+    }
+  }
+  for (int i = 0; i < 3; ++i) {
+    const int rc = check_stride(dq[i], a.o_strides[i], true);
+    if (rc) return rc;
+  }
+  const long long lse_st[3] = {packed ? 0 : (long long)a.lse_strides[0], (long long)a.lse_strides[1], 1};
+  for (int i = 0; i < 2; ++i)
+    if (dq[i] > 1 && (lse_st[i] < 0 || lse_st[i] >= kMaxStride)) return FA2_ERR_INVALID_ARG;
+  // o and lse overlap nothing they are not
+  const long long o_st[3] = {(long long)a.o_strides[0], (long long)a.o_strides[1], (long long)a.o_strides[2]};
+  const Extent e_o = extent(a.o, dq, o_st, d, 2), e_l = extent(a.lse, dq, lse_st, 1, 4);
+  const Extent ins[3] = {extent(a.q, dq, st_in[0], d, 2), extent(a.k, dk, st_in[1], d, 2),
+                         extent(a.v, dk, st_in[2], d, 2)};
+  if (overlap(e_o, e_l)) return FA2_ERR_INVALID_ARG;
+  for (const Extent& in : ins)
+    if (overlap(e_o, in) || overlap(e_l, in)) return FA2_ERR_INVALID_ARG;
+
+  DeviceState* ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc) return rc;
+  MapKey key;
+  std::memset(&key, 0, sizeof(key));
+  if (cudaGetDevice(&key.dev) != cudaSuccess) return FA2_ERR_CUDA;
+  key.dtype = a.dtype;
+  key.d = d;
+  const void* ptrs[3] = {a.q, a.k, a.v};
+  for (int t = 0; t < 3; ++t) {
+    const long long* dims = t == 0 ? dq : dk;
+    key.ptr[t] = ptrs[t];
+    key.dims[t][0] = dims[2];  // rows, heads, batch
+    key.dims[t][1] = dims[1];
+    key.dims[t][2] = dims[0];
+    for (int i = 0; i < 3; ++i) key.strides[t][i] = st_in[t][i];
+  }
+  key.merged = 1;
+  for (int t = 0; t < 3; ++t)
+    if (!mergeable(a.heads, tb, st_in[t])) key.merged = 0;
+  LaunchArgs la;
+  std::memset(&la, 0, sizeof(la));
+  rc = cached_maps(la, key);
+  if (rc) return rc;
+  KernelParams& p = la.p;
+  p.o = a.o;
+  p.lse = a.lse;
+  p.status = ds->status;
+  p.cu_q = packed ? a.cu_seqlens_q : nullptr;
+  p.cu_k = packed ? a.cu_seqlens_k : nullptr;
+  p.o_bs = packed ? 0 : a.o_strides[0];
+  p.o_hs = a.o_strides[1];
+  p.o_rs = a.o_strides[2];
+  p.l_bs = lse_st[0];
+  p.l_hs = lse_st[1];
+  p.n_q = a.seqlen_q;
+  p.n_k = packed ? a.total_k : a.seqlen_k;
+  p.total_q = (int)rows_q;
+  p.total_k = (int)rows_k;
+  p.heads = a.heads;
+  p.merged_bh = key.merged;
+  p.bh = a.batch * a.heads;
+  p.units = (int)units;
+  p.window_left = a.window_left;
+  p.window_right = a.window_right;
+  p.prefix = a.prefix_len;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  la.bf16 = a.dtype == FA2_BF16;
+  la.band = a.window_left >= 0 || a.prefix_len > 0;
+  la.stream = stream;
+  int e = 0;
+  switch (d) {
+    case 64: e = launch_fwd_d64(la); break;
+    case 128: e = launch_fwd_d128(la); break;
+    default: e = launch_fwd_d256(la); break;
+  }
+  return e == 0 ? FA2_OK : FA2_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace fa2
+
+extern "C" size_t fa2_fwd_params_size(void) { return sizeof(fa2_fwd_params); }
+
+extern "C" int fa2_fwd_ex(const fa2_fwd_params* params, void* stream) {
+  if (!params) return FA2_ERR_INVALID_ARG;
+  return forward(*params, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
                        int d, float scale, int causal, int dtype, void* stream) {
   int rc = check_shape(B, H, N, d, scale, causal, dtype);
   if (rc) return rc;
   if (!q || !k || !v || !o || !lse) return FA2_ERR_INVALID_ARG;
   if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(o) || misaligned(lse)) return FA2_ERR_MISALIGNED;
-  const size_t elems = (size_t)B * H * (size_t)N * d;
-  const size_t tbytes = elems * 2, lbytes = (size_t)B * H * (size_t)N * 4;
-  const void* ins[3] = {q, k, v};
-  for (const void* in : ins) {
-    if (ranges_overlap(o, tbytes, in, tbytes) || ranges_overlap(lse, lbytes, in, tbytes)) return FA2_ERR_INVALID_ARG;
-  }
-  if (ranges_overlap(o, tbytes, lse, lbytes)) return FA2_ERR_INVALID_ARG;
-
-  DeviceState* ds = nullptr;
-  rc = device_state(&ds);
-  if (rc) return rc;
-  const bool bf16 = dtype == FA2_BF16;
-  const TileGeometry g = tile_geometry(d);
-  LaunchArgs a;
+  fa2_fwd_params a;
   std::memset(&a, 0, sizeof(a));
-  const int bh = B * H;
-  rc = cached_maps(a, q, k, v, bh, N, d, dtype);
-  if (rc) return rc;
-  a.p.o = o;
-  a.p.lse = lse;
-  a.p.status = ds->status;
-  a.p.n = N;
-  a.p.num_q_tiles = (N + g.q_rows - 1) / g.q_rows;
-  a.p.bh = bh;
-  a.p.scale_log2 = scale * 1.4426950408889634f;
-  a.bf16 = bf16;
-  a.causal = causal != 0;
-  a.stream = static_cast<cudaStream_t>(stream);
-  int e = 0;
-  switch (d) {
-    case 64: e = launch_fwd_d64(a); break;
-    case 128: e = launch_fwd_d128(a); break;
-    default: e = launch_fwd_d256(a); break;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.batch = B;
+  a.heads = H;
+  a.seqlen_q = N;
+  a.seqlen_k = N;
+  a.head_dim = d;
+  a.dtype = dtype;
+  a.scale = scale;
+  a.window_left = -1;
+  a.window_right = causal ? 0 : -1;
+  a.prefix_len = 0;
+  const long long row = d, head = (long long)N * d, batch = (long long)H * N * d;
+  int64_t* st[4] = {a.q_strides, a.k_strides, a.v_strides, a.o_strides};
+  for (int64_t* s : st) {
+    s[0] = batch;
+    s[1] = head;
+    s[2] = row;
   }
-  return e == 0 ? FA2_OK : FA2_ERR_CUDA;
+  a.lse_strides[0] = (long long)H * N;
+  a.lse_strides[1] = N;
+  return forward(a, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" size_t fa2_fwd_host_workspace_bytes(int B, int H, int N, int d) {
@@ -520,6 +716,8 @@ extern "C" int fa2_get_device_status(void* stream, uint32_t* detail) {
   if (word && cudaMemcpy(ds->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
     return FA2_ERR_CUDA;
   if (detail) *detail = word;
+  if (word & kStatusTimeout) return FA2_ERR_DEVICE_TIMEOUT;
+  if (word & kStatusBadSeqlens) return FA2_ERR_DEVICE_SEQLENS;
   return word ? FA2_ERR_DEVICE_TIMEOUT : FA2_OK;
 }
 
@@ -532,6 +730,7 @@ extern "C" const char* fa2_status_string(int status) {
     case FA2_ERR_CUDA: return "CUDA runtime or driver call failed";
     case FA2_ERR_DEVICE_TIMEOUT: return "a kernel wait timed out; the tile was abandoned";
     case FA2_ERR_SCRATCH_LIMIT: return "problem exceeds the static device scratch of fa2_fwd_host_noalloc";
+    case FA2_ERR_DEVICE_SEQLENS: return "packed-batch row offsets out of range; those sequences were not written";
     default: return "unknown status";
   }
 }

@@ -87,19 +87,213 @@ __device__ __forceinline__ float2 unpack2(uint32_t u) {
   }
 }
 
-// A key tile is split into P = P_hi + P_lo (two 16-bit PV products) when the
-// input is bf16 and the tile is one where rows see few keys: tiles crossing
-// the causal diagonal, or every tile when all keys fit in two tiles.  bf16
-// keeps 8 significant bits, so a lone rounded P term would otherwise move O
-// by up to 2^-9 of a value row; the split brings P to ~16 bits there.
-template <class C, bool BF16, bool CAUSAL>
-__device__ __forceinline__ bool split_tile(int j, int q0, int n) {
+// Which keys a query row sees: an additive 0 / -inf mask on S in the sense
+// of the Flash Attention 2 page, "Causal masking" (Option A), whose tiles
+// that the mask removes entirely are skipped.  For a sequence of N_q queries
+// and N_k keys, query i is aligned with key i + off, off = N_k - N_q (the
+// last query with the last key), and sees key j < N_k iff
+//     j < pre_end                       (a prefix every query sees), or
+//     i + off - wl <= j <= i + off + wr (a band; wl or wr < 0: unbounded).
+// Causal is (wl, wr) = (-1, 0); a window of w keys back is (w, 0).
+struct KeyMask {
+  int n_k, off, wl, wr, pre_end;
+
+  // First band key of row i, in [0, n_k] (n_k: none).
+  __device__ __forceinline__ int row_lo(int i) const {
+    if (wl < 0) return 0;
+    const long long x = (long long)i + off - wl;
+    return (int)(x < 0 ? 0 : (x > n_k ? n_k : x));
+  }
+  // Last band key of row i, in [-1, n_k - 1] (-1: none).
+  __device__ __forceinline__ int row_hi(int i) const {
+    if (wr < 0) return n_k - 1;
+    const long long x = (long long)i + off + wr;
+    return (int)(x < -1 ? -1 : (x > n_k - 1 ? n_k - 1 : x));
+  }
+  // Keys [lo, end) some row of [first, last] sees; false if none.  Both band
+  // ends are non-decreasing in the row, so this is one interval.
+  template <bool BAND>
+  __device__ __forceinline__ bool tile_range(int first, int last, int& lo, int& end) const {
+    int a = BAND ? row_lo(first) : 0, b = row_hi(last);
+    if (pre_end > 0) {
+      a = 0;
+      b = b > pre_end - 1 ? b : pre_end - 1;
+    }
+    lo = a;
+    end = b + 1;
+    return b >= a;
+  }
+};
+
+// Which key tiles of one query tile need no element mask (every valid row
+// sees all of the tile), as thresholds on a tile index t counted from some
+// origin: t < pre (inside the prefix) or lo <= t < hi (right of the last
+// valid row's left band edge, left of the first row's right band edge and
+// inside N_k).
+struct TileMask {
+  int pre, lo, hi;
+  __device__ __forceinline__ bool full(int t) const { return t < pre || (t >= lo && t < hi); }
+  // The same thresholds counted from tile index `origin` instead.
+  __device__ __forceinline__ TileMask from(int origin) const { return TileMask{pre - origin, lo - origin, hi - origin}; }
+};
+
+// Thresholds (tile index 0 = keys [0, bc)) for query rows [first, last].
+template <bool BAND>
+__device__ __forceinline__ TileMask tile_mask(const KeyMask& km, int first, int last, int bc) {
+  TileMask t;
+  t.pre = km.pre_end / bc;
+  t.lo = BAND ? (km.row_lo(last) + bc - 1) / bc : 0;
+  t.hi = (km.row_hi(first) + 1) / bc;  // row_hi <= n_k - 1 keeps the tile inside N_k
+  return t;
+}
+
+// bf16 P is split into P = P_hi + P_lo (two 16-bit PV products) on tiles
+// where rows see few keys: tiles the mask cuts (diagonal and band-edge
+// tiles) and every tile when all keys fit in two tiles.  bf16 keeps 8
+// significant bits, so a lone rounded P term would otherwise move O by up to
+// 2^-9 of a value row; the split brings P to ~16 bits there.
+template <bool BF16>
+__device__ __forceinline__ bool split_tile(bool masked, bool few_keys) {
   if constexpr (!BF16) {
     return false;
   } else {
-    const bool diag = CAUSAL && (j * C::BC + C::BC - 1 > q0);
-    return diag || (n <= 2 * C::BC);
+    return masked || few_keys;
   }
+}
+
+// Set to -inf, in place, the scores of the keys of tile [k0, k0 + BC) that
+// query row `row` does not see.  BAND: the first visible key may depend on
+// the row (a bounded left window or a prefix); otherwise every row sees keys
+// [0, row_hi] and one comparison per score suffices.
+template <int BC, bool BAND>
+__device__ __forceinline__ void mask_scores(uint32_t* sr, const KeyMask& km, int row, int k0) {
+  const int c_hi = km.row_hi(row) - k0;
+  if constexpr (BAND) {
+    const int c_pre = km.pre_end - k0;
+    const int c_lo = km.row_lo(row) - k0;
+#pragma unroll
+    for (int c = 0; c < BC; ++c) {
+      const bool vis = (c < c_pre) || (c >= c_lo && c <= c_hi);
+      if (!vis) sr[c] = __float_as_uint(-INFINITY);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < BC; ++c)
+      if (c > c_hi) sr[c] = __float_as_uint(-INFINITY);
+  }
+}
+
+// Loads one 64-column box of `rows` rows of head h, batch b, whichever rank
+// the map has (3-D maps merge batch and head into one coordinate b*H + h;
+// the merged coordinate is precomputed by the caller as `hb`).
+__device__ __forceinline__ void tma_load_rows(uint32_t dst, const CUtensorMap* map, bool merged, int x, int row, int h,
+                                              int b, int hb, uint32_t bar) {
+  if (merged)
+    tma_load_3d(dst, map, x, row, hb, bar);
+  else
+    tma_load_4d(dst, map, x, row, h, b, bar);
+}
+
+// One (batch, head) slice: where its rows start in the tensors and how long
+// it is.  Packed batches read their offsets from cu_q / cu_k.
+struct SeqInfo {
+  int b, h;            // batch coordinate in the tensors (0 for packed batches) and head
+  int n_q, n_k;
+  int row0_q, row0_k;  // first row of the sequence in q/o/lse and in k/v
+};
+
+// False (and the bad-offsets status bit set) when the offsets of a
+// packed sequence are out of range.
+__device__ __forceinline__ bool seq_info(const KernelParams& p, int bh, SeqInfo& s) {
+  if (p.bh == p.heads) {  // one batch (the host folds mergeable batches into heads)
+    s.b = 0;
+    s.h = bh;
+  } else {
+    s.b = bh / p.heads;
+    s.h = bh - s.b * p.heads;
+  }
+  if (!p.cu_q) {
+    s.n_q = p.n_q;
+    s.n_k = p.n_k;
+    s.row0_q = 0;
+    s.row0_k = 0;
+    return true;
+  }
+  const int q_a = __ldg(p.cu_q + s.b), q_b = __ldg(p.cu_q + s.b + 1);
+  const int k_a = __ldg(p.cu_k + s.b), k_b = __ldg(p.cu_k + s.b + 1);
+  const bool ok = 0 <= q_a && q_a <= q_b && q_b <= p.total_q && q_b - q_a <= p.n_q && 0 <= k_a && k_a <= k_b &&
+                  k_b <= p.total_k;
+  if (!ok) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusBadSeqlens);
+    return false;
+  }
+  s.b = 0;
+  s.n_q = q_b - q_a;
+  s.n_k = k_b - k_a;
+  s.row0_q = q_a;
+  s.row0_k = k_a;
+  return true;
+}
+
+__device__ __forceinline__ KeyMask key_mask(const KernelParams& p, const SeqInfo& s) {
+  KeyMask km;
+  km.n_k = s.n_k;
+  km.off = s.n_k - s.n_q;
+  km.wl = p.window_left;
+  km.wr = p.window_right;
+  km.pre_end = p.prefix < s.n_k ? p.prefix : s.n_k;
+  return km;
+}
+
+// Per-CTA facts the softmax warps need only in masked tiles and in the
+// epilogue.  They live in shared memory (written once before the roles
+// split) so that they hold no registers through the main loop.
+struct CtaFacts {
+  SeqInfo seq;
+  KeyMask km;
+};
+
+// Epilogue store of one output row: O = O~ / l rounded to 16 bits, LSE in
+// natural log; a row that sees no key gets O = 0 and LSE = -inf.
+template <int D, bool BF16>
+__device__ __forceinline__ void store_row(const KernelParams& p, const SeqInfo& s, int row, uint32_t tO, float m_run,
+                                          float l_run) {
+  const bool empty = !(l_run > 0.f);
+  const float inv_l = empty ? 0.f : 1.f / l_run;
+  const bool valid = row < s.n_q;
+  uint8_t* o_row = reinterpret_cast<uint8_t*>(p.o) +
+                   2 * ((long long)s.b * p.o_bs + (long long)s.h * p.o_hs + (long long)(s.row0_q + row) * p.o_rs);
+#pragma unroll 1
+  for (int c = 0; c < D; c += 32) {
+    uint32_t o[32];
+    tmem_ld_32x32b_x32(tO + c, o);
+    tmem_ld_wait_x32(o);
+    uint32_t packed[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      packed[i] = empty ? 0u : pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+    if (valid) {
+      uint4* dst = reinterpret_cast<uint4*>(o_row + c * 2);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+    }
+  }
+  if (valid)
+    p.lse[(long long)s.b * p.l_bs + (long long)s.h * p.l_hs + s.row0_q + row] =
+        empty ? -INFINITY : (m_run + log2f(l_run)) * 0.6931471805599453f;
+}
+
+// Rows of a query tile that see no key at all: O = 0, LSE = -inf, without
+// touching tensor memory.
+template <int D>
+__device__ __forceinline__ void store_empty_row(const KernelParams& p, const SeqInfo& s, int row) {
+  if (row >= s.n_q) return;
+  uint8_t* o_row = reinterpret_cast<uint8_t*>(p.o) +
+                   2 * ((long long)s.b * p.o_bs + (long long)s.h * p.o_hs + (long long)(s.row0_q + row) * p.o_rs);
+#pragma unroll
+  for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(o_row + c * 2) = make_uint4(0u, 0u, 0u, 0u);
+  p.lse[(long long)s.b * p.l_bs + (long long)s.h * p.l_hs + s.row0_q + row] = -INFINITY;
 }
 
 // Order of work units over a 1-D grid of (B*H) x units blocks.  Heads go in
@@ -126,16 +320,5 @@ __device__ __forceinline__ void unit_of_block(int block, int bh_total, int units
   bh = g * kHeadGroup + r % size;
   unit = units - 1 - r / size;
 }
-
-// Addresses and sizes of one query tile's work, shared by its warp roles.
-struct TileCtx {
-  uint32_t bar0;       // shared address of barrier 0
-  uint32_t sQ, sK, sV; // shared addresses of the tiles
-  uint32_t tmem;       // TMEM base (lane 0, first allocated column)
-  volatile int* abort_flag;
-  uint32_t* status;
-  int bh, q0, n, nkv;
-  __device__ __forceinline__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
-};
 
 }  // namespace fa2

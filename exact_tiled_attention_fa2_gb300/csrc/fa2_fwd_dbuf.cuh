@@ -42,7 +42,8 @@ struct DbufConfig {
   static constexpr uint32_t OFF_BAR = OFF_V + VSTAGES * KV_BYTES;
   static constexpr uint32_t NUM_BARS = 24;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
+  static constexpr uint32_t MISC_BYTES = 128;  // TMEM address, abort flag, CtaFacts
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;
   static constexpr uint32_t TMEM_S = 0;     // + 64 * buffer
   static constexpr uint32_t TMEM_O = 128;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -67,14 +68,32 @@ enum : int {
                    // phases ahead of the parity the MMA thread waits for.
 };
 
+// One query tile's work, shared by the CTA's warp roles.
+struct DbufCtx {
+  uint32_t bar0, sQ, sK, sV, tmem;
+  volatile int* abort_flag;
+  uint32_t* status;
+  SeqInfo seq;
+  KeyMask km;
+  int q0;    // first query row of the tile
+  int kv0;   // first key tile the tile visits
+  int nkv;   // key tiles it visits (0: none)
+  TileMask tm;    // unmasked key tiles, by index counted from kv0
+  bool few_keys;  // N_k <= 2 key tiles: every bf16 P is split
+  __device__ __forceinline__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
+};
+
 // K_j is needed two products before V_j, so the K and V streams are issued
 // independently: whichever ring has a free slot gets the next load.
 template <class C>
-__device__ __forceinline__ void db_producer(const TileCtx& t, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                                            const CUtensorMap* tm_v) {
+__device__ __forceinline__ void db_producer(const DbufCtx& t, const KernelParams& p, const CUtensorMap* tm_q,
+                                            const CUtensorMap* tm_k, const CUtensorMap* tm_v) {
+  const int h = t.seq.h, b = t.seq.b, hb = b * p.heads + h;
+  const bool merged = p.merged_bh != 0;
+  const int krow0 = t.seq.row0_k + t.kv0 * C::BC;
   mbar_arrive_expect_tx(t.bar(DB_Q), C::Q_BYTES);
   for (int kb = 0; kb < C::D / 64; ++kb)
-    tma_load_3d(t.sQ + kb * (C::BR * 128), tm_q, kb * 64, t.q0, t.bh, t.bar(DB_Q));
+    tma_load_rows(t.sQ + kb * (C::BR * 128), tm_q, merged, kb * 64, t.seq.row0_q + t.q0, h, b, hb, t.bar(DB_Q));
   int jk = 0, jv = 0;
   uint64_t idle_since = 0;
   while (jk < t.nkv || jv < t.nkv) {
@@ -84,8 +103,8 @@ __device__ __forceinline__ void db_producer(const TileCtx& t, const CUtensorMap*
       if (u == 0 || mbar_try_wait(t.bar(DB_KEMPTY + s), (u - 1) & 1)) {
         mbar_arrive_expect_tx(t.bar(DB_KFULL + s), C::KV_BYTES);
         for (int kb = 0; kb < C::D / 64; ++kb)
-          tma_load_3d(t.sK + s * C::KV_BYTES + kb * (C::BC * 128), tm_k, kb * 64, jk * C::BC, t.bh,
-                      t.bar(DB_KFULL + s));
+          tma_load_rows(t.sK + s * C::KV_BYTES + kb * (C::BC * 128), tm_k, merged, kb * 64, krow0 + jk * C::BC, h,
+                        b, hb, t.bar(DB_KFULL + s));
         ++jk;
         progressed = true;
       }
@@ -95,8 +114,8 @@ __device__ __forceinline__ void db_producer(const TileCtx& t, const CUtensorMap*
       if (u == 0 || mbar_try_wait(t.bar(DB_VEMPTY + s), (u - 1) & 1)) {
         mbar_arrive_expect_tx(t.bar(DB_VFULL + s), C::KV_BYTES);
         for (int kb = 0; kb < C::D / 64; ++kb)
-          tma_load_3d(t.sV + s * C::KV_BYTES + kb * (C::BC * 128), tm_v, kb * 64, jv * C::BC, t.bh,
-                      t.bar(DB_VFULL + s));
+          tma_load_rows(t.sV + s * C::KV_BYTES + kb * (C::BC * 128), tm_v, merged, kb * 64, krow0 + jv * C::BC, h,
+                        b, hb, t.bar(DB_VFULL + s));
         ++jv;
         progressed = true;
       }
@@ -128,8 +147,8 @@ __device__ __forceinline__ void db_producer(const TileCtx& t, const CUtensorMap*
   }
 }
 
-template <class C, bool BF16, bool CAUSAL>
-__device__ __forceinline__ void db_mma(const TileCtx& t) {
+template <class C, bool BF16>
+__device__ __forceinline__ void db_mma(const DbufCtx& t) {
   constexpr uint32_t idesc_qk = make_idesc_f16(C::BR, C::BC, BF16, false, false);
   constexpr uint32_t idesc_pv = make_idesc_f16(C::BR, C::D, BF16, false, true);
   const uint64_t dq0 = make_sdesc_sw128(t.sQ, 16, 1024);
@@ -150,7 +169,7 @@ __device__ __forceinline__ void db_mma(const TileCtx& t) {
     umma_commit(t.bar(DB_KEMPTY + sk));
     return true;
   };
-  if (wait_or_abort(t.bar(DB_Q), 0, t.abort_flag, t.status, kSiteMmaQ)) {
+  if (t.nkv > 0 && wait_or_abort(t.bar(DB_Q), 0, t.abort_flag, t.status, kSiteMmaQ)) {
     tc_fence_after();
     ok = issue_s(0);
     if (ok && t.nkv > 1) ok = issue_s(1);
@@ -163,7 +182,7 @@ __device__ __forceinline__ void db_mma(const TileCtx& t) {
       const uint64_t b0 = dv0 + (uint64_t)((sv * C::KV_BYTES) >> 4);
       const uint32_t tS = t.tmem + C::TMEM_S + 64 * (j & 1);
       const uint32_t tO = t.tmem + C::TMEM_O;
-      if (split_tile<C, BF16, CAUSAL>(j, t.q0, t.n)) {
+      if (split_tile<BF16>(!t.tm.full(j), t.few_keys)) {
 #pragma unroll
         for (int k = 0; k < C::BC / 16; ++k) {
           const uint64_t b = b0 + (uint64_t)((k * 16 * 128) >> 4);
@@ -187,14 +206,21 @@ __device__ __forceinline__ void db_mma(const TileCtx& t) {
   wait_drain(t.bar(DB_EXIT), 0, t.status);
 }
 
-template <class C, bool BF16, bool CAUSAL>
-__device__ __forceinline__ void db_softmax(const TileCtx& t, const KernelParams& p, int warp, int lane) {
+template <class C, bool BF16, bool BAND>
+__device__ __forceinline__ void db_softmax(const DbufCtx& t, const KernelParams& p, const CtaFacts* facts, int warp,
+                                           int lane) {
   const int quad = warp & 3;
   const int r = quad * 32 + lane;
   const int row = t.q0 + r;
+  if (t.nkv == 0) {
+    store_empty_row<C::D>(p, t.seq, row);
+    return;
+  }
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
   const uint32_t tO = t.tmem + lane_off + C::TMEM_O;
   const float sl2 = p.scale_log2;
+  const TileMask tmask = t.tm;
+  const bool few_keys = t.few_keys;
   float m_run = -INFINITY;
   float l_run = 0.f;
   bool ok = true;
@@ -209,15 +235,8 @@ __device__ __forceinline__ void db_softmax(const TileCtx& t, const KernelParams&
     for (int c = 0; c < C::BC; c += 32) tmem_ld_32x32b_x32(tS + c, sr + c);
 #pragma unroll
     for (int c = 0; c < C::BC; c += 32) tmem_ld_wait_x32(sr + c);
-    const int k0 = j * C::BC;
-    const bool masked = (k0 + C::BC > t.n) || (CAUSAL && (k0 + C::BC - 1 > t.q0));
-    if (masked) {
-#pragma unroll
-      for (int c = 0; c < C::BC; ++c) {
-        const int key = k0 + c;
-        if (key >= t.n || (CAUSAL && key > row)) sr[c] = __float_as_uint(-INFINITY);
-      }
-    }
+    const bool masked = !tmask.full(j);
+    if (masked) mask_scores<C::BC, BAND>(sr, facts->km, row, (t.kv0 + j) * C::BC);
     float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
     for (int c = 0; c < C::BC; c += 8) {
@@ -234,7 +253,7 @@ __device__ __forceinline__ void db_softmax(const TileCtx& t, const KernelParams&
     const float2 scale2 = make_float2(sl2, sl2);
     const float2 neg_m2 = make_float2(-m_use, -m_use);
     float2 sum0 = make_float2(0.f, 0.f), sum1 = make_float2(0.f, 0.f);
-    if (split_tile<C, BF16, CAUSAL>(j, t.q0, t.n)) {
+    if (split_tile<BF16>(masked, few_keys)) {
 #pragma unroll
       for (int ch = 0; ch < C::BC / 32; ++ch) pp_p_chunk<C, BF16, true>(sr, ch, tS, scale2, neg_m2, sum0, sum1);
     } else {
@@ -278,28 +297,12 @@ __device__ __forceinline__ void db_softmax(const TileCtx& t, const KernelParams&
   }
   if (!ok) return;
   tc_fence_after();
-  const float inv_l = 1.f / l_run;
-  uint8_t* o_row = reinterpret_cast<uint8_t*>(p.o) + ((size_t)t.bh * (size_t)t.n + (size_t)row) * (C::D * 2);
-#pragma unroll 1
-  for (int c = 0; c < C::D; c += 32) {
-    uint32_t o[32];
-    tmem_ld_32x32b_x32(tO + c, o);
-    tmem_ld_wait_x32(o);
-    uint32_t packed[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      packed[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-    if (row < t.n) {
-      uint4* dst = reinterpret_cast<uint4*>(o_row + c * 2);
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-    }
-  }
-  if (row < t.n) p.lse[(size_t)t.bh * (size_t)t.n + (size_t)row] = (m_run + log2f(l_run)) * 0.6931471805599453f;
+  store_row<C::D, BF16>(p, facts->seq, row, tO, m_run, l_run);
 }
 
-template <int D, bool BF16, bool CAUSAL>
+// BAND: the first key a query row sees may depend on the row (a bounded left
+// window or a prefix); it selects the element mask's form.
+template <int D, bool BF16, bool BAND>
 __global__ void __launch_bounds__(192, 1)
     fa2_fwd_dbuf_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const KernelParams p) {
@@ -310,22 +313,37 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t sbase = smem_u32(smem);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  CtaFacts* facts = reinterpret_cast<CtaFacts*>(smem + C::OFF_MISC + 16);
+  static_assert(16 + sizeof(CtaFacts) <= C::MISC_BYTES, "shared-memory misc area");
   const int warp = (int)(threadIdx.x >> 5);
   const int lane = (int)(threadIdx.x & 31);
 
-  TileCtx t;
+  DbufCtx t;
+  int bh, q_tile;
+  unit_of_block((int)blockIdx.x, p.bh, p.units, bh, q_tile);
+  // The whole CTA leaves together, before any barrier or TMEM set-up, when
+  // its sequence is malformed or shorter than this tile's rows.
+  if (!seq_info(p, bh, t.seq)) return;
+  t.q0 = q_tile * C::BR;
+  if (t.q0 >= t.seq.n_q) return;
   t.bar0 = sbase + C::OFF_BAR;
   t.sQ = sbase + C::OFF_Q;
   t.sK = sbase + C::OFF_K;
   t.sV = sbase + C::OFF_V;
   t.abort_flag = abort_flag;
   t.status = p.status;
-  t.n = p.n;
-  int q_tile;
-  unit_of_block((int)blockIdx.x, p.bh, p.num_q_tiles, t.bh, q_tile);
-  t.q0 = q_tile * C::BR;
-  const int kv_end = CAUSAL ? min(t.n, t.q0 + C::BR) : t.n;
-  t.nkv = (kv_end + C::BC - 1) / C::BC;
+  t.km = key_mask(p, t.seq);
+  const int last = min(t.q0 + C::BR, t.seq.n_q) - 1;
+  int lo, end;
+  if (t.km.template tile_range<BAND>(t.q0, last, lo, end)) {
+    t.kv0 = lo / C::BC;
+    t.nkv = (end + C::BC - 1) / C::BC - t.kv0;
+  } else {
+    t.kv0 = 0;
+    t.nkv = 0;
+  }
+  t.tm = tile_mask<BAND>(t.km, t.q0, last, C::BC).from(t.kv0);
+  t.few_keys = t.km.n_k <= 2 * C::BC;
 
   if (threadIdx.x == 0) {
     mbar_init(t.bar(DB_Q), 1);
@@ -345,6 +363,8 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(t.bar(DB_OLAST), 1);
     mbar_init(t.bar(DB_EXIT), 1);
     *abort_flag = 0;
+    facts->seq = t.seq;
+    facts->km = t.km;
     fence_mbar_init();
   }
   if (warp == C::TMA_WARP && lane == 0) {
@@ -362,12 +382,12 @@ __global__ void __launch_bounds__(192, 1)
   t.tmem = *tmem_slot;
 
   if (warp == C::TMA_WARP) {
-    if (lane == 0) db_producer<C>(t, &tm_q, &tm_k, &tm_v);
+    if (lane == 0 && t.nkv > 0) db_producer<C>(t, p, &tm_q, &tm_k, &tm_v);
   } else if (warp == C::MMA_WARP) {
-    if (lane == 0) db_mma<C, BF16, CAUSAL>(t);
+    if (lane == 0) db_mma<C, BF16>(t);
     __syncwarp();
   } else {
-    db_softmax<C, BF16, CAUSAL>(t, p, warp, lane);
+    db_softmax<C, BF16, BAND>(t, p, facts, warp, lane);
   }
   tc_fence_before();
   __syncthreads();
@@ -377,24 +397,26 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool BAND>
 int launch_fwd_dbuf(const LaunchArgs& a) {
   using C = DbufConfig<D>;
-  auto kern = fa2_fwd_dbuf_kernel<D, BF16, CAUSAL>;
+  auto kern = fa2_fwd_dbuf_kernel<D, BF16, BAND>;
   static std::atomic<unsigned long long> configured{0};
   const int e = once_per_device(configured, [&]() -> int {
     return (int)cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
   });
   if (e != 0) return e;
-  dim3 grid((unsigned)(a.p.bh * a.p.num_q_tiles));
+  static_assert(C::BR == 128, "query rows per CTA: tile_geometry(d).cta_rows sizes the grid");
+  dim3 grid((unsigned)(a.p.bh * a.p.units));
   kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.p);
   return (int)cudaGetLastError();
 }
 
 template <int D>
 int launch_fwd_dbuf_dispatch(const LaunchArgs& a) {
-  if (a.bf16) return a.causal ? launch_fwd_dbuf<D, true, true>(a) : launch_fwd_dbuf<D, true, false>(a);
-  return a.causal ? launch_fwd_dbuf<D, false, true>(a) : launch_fwd_dbuf<D, false, false>(a);
+  if (a.band) return a.bf16 ? launch_fwd_dbuf<D, true, true>(a) : launch_fwd_dbuf<D, false, true>(a);
+  return a.bf16 ? launch_fwd_dbuf<D, true, false>(a) : launch_fwd_dbuf<D, false, false>(a);
 }
+
 
 }  // namespace fa2

@@ -57,7 +57,8 @@ struct PingPongConfig {
   static constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;
   static constexpr uint32_t NUM_BARS = 32;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
+  static constexpr uint32_t MISC_BYTES = 128;  // TMEM address, abort flag, CtaFacts
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;
   static constexpr uint32_t TMEM_S = 0;     // + 128 * tile
   static constexpr uint32_t TMEM_O = 256;   // + D * tile
   static constexpr uint32_t TMEM_COLS = 512;
@@ -81,10 +82,15 @@ struct PairCtx {
   uint32_t bar0, sQ, sK, sV, tmem;
   volatile int* abort_flag;
   uint32_t* status;
-  int bh, n;
-  int q0[2];    // first query row of each tile
-  int nkv[2];   // key/value tiles each tile visits (0: tile lies past N)
-  int nkv_max;
+  SeqInfo seq;
+  KeyMask km;
+  int kv0;       // first streamed key tile (index within the sequence)
+  int nu;        // key tiles streamed through the CTA
+  int q0[2];     // first query row of each tile
+  int first[2];  // streamed index of each tile's first key tile
+  int nkv[2];    // key tiles each tile visits (0: none)
+  TileMask tm[2];  // unmasked key tiles of each tile, by streamed index
+  bool few_keys; // N_k <= 2 key tiles: every bf16 P is split
   __device__ __forceinline__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
 };
 
@@ -95,30 +101,34 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 }
 
 template <class C>
-__device__ __forceinline__ void pp_producer(const PairCtx& t, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                                            const CUtensorMap* tm_v) {
+__device__ __forceinline__ void pp_producer(const PairCtx& t, const KernelParams& p, const CUtensorMap* tm_q,
+                                            const CUtensorMap* tm_k, const CUtensorMap* tm_v) {
+  const int h = t.seq.h, b = t.seq.b, hb = b * p.heads + h;
+  const bool merged = p.merged_bh != 0;
   for (int q = 0; q < C::NQ; ++q) {
     if (t.nkv[q] == 0) continue;
     mbar_arrive_expect_tx(t.bar(PB_Q + q), C::Q_BYTES);
     for (int kb = 0; kb < C::D / 64; ++kb)
-      tma_load_3d(t.sQ + q * C::Q_BYTES + kb * (C::BR * 128), tm_q, kb * 64, t.q0[q], t.bh, t.bar(PB_Q + q));
+      tma_load_rows(t.sQ + q * C::Q_BYTES + kb * (C::BR * 128), tm_q, merged, kb * 64, t.seq.row0_q + t.q0[q], h, b,
+                    hb, t.bar(PB_Q + q));
   }
   int last_use[C::STAGES];
   for (int s = 0; s < C::STAGES; ++s) last_use[s] = -1;
-  for (int j = 0; j < t.nkv_max; ++j) {
-    const int s = j % C::STAGES;
-    const int u = j / C::STAGES;
-    if (u > 0 && !wait_or_abort(t.bar(PB_KVEMPTY + s), (u - 1) & 1, t.abort_flag, t.status, kSiteProducerEmpty))
+  for (int u = 0; u < t.nu; ++u) {
+    const int s = u % C::STAGES;
+    const int w = u / C::STAGES;
+    if (w > 0 && !wait_or_abort(t.bar(PB_KVEMPTY + s), (w - 1) & 1, t.abort_flag, t.status, kSiteProducerEmpty))
       break;
+    const int row = t.seq.row0_k + (t.kv0 + u) * C::BC;
     mbar_arrive_expect_tx(t.bar(PB_KFULL + s), C::KV_BYTES);
     for (int kb = 0; kb < C::D / 64; ++kb)
-      tma_load_3d(t.sK + s * C::KV_BYTES + kb * (C::BC * 128), tm_k, kb * 64, j * C::BC, t.bh,
-                  t.bar(PB_KFULL + s));
+      tma_load_rows(t.sK + s * C::KV_BYTES + kb * (C::BC * 128), tm_k, merged, kb * 64, row, h, b, hb,
+                    t.bar(PB_KFULL + s));
     mbar_arrive_expect_tx(t.bar(PB_VFULL + s), C::KV_BYTES);
     for (int kb = 0; kb < C::D / 64; ++kb)
-      tma_load_3d(t.sV + s * C::KV_BYTES + kb * (C::BC * 128), tm_v, kb * 64, j * C::BC, t.bh,
-                  t.bar(PB_VFULL + s));
-    last_use[s] = u;
+      tma_load_rows(t.sV + s * C::KV_BYTES + kb * (C::BC * 128), tm_v, merged, kb * 64, row, h, b, hb,
+                    t.bar(PB_VFULL + s));
+    last_use[s] = w;
   }
   for (int q = 0; q < C::NQ; ++q)
     if (t.nkv[q] > 0) wait_drain(t.bar(PB_Q + q), 0, t.status);
@@ -138,7 +148,7 @@ __device__ __forceinline__ constexpr uint64_t kmajor_step(int k, int rows) {
   return (uint64_t)(((k >> 2) * (rows * 128) + (k & 3) * 32) >> 4);
 }
 
-template <class C, bool BF16, bool CAUSAL>
+template <class C, bool BF16, bool BAND>
 __device__ __forceinline__ void pp_mma(const PairCtx& t) {
   constexpr uint32_t idesc_qk = make_idesc_f16(C::BR, C::BC, BF16, false, false);
   constexpr uint32_t idesc_pv = make_idesc_f16(C::BR, C::D, BF16, false, true);
@@ -146,66 +156,87 @@ __device__ __forceinline__ void pp_mma(const PairCtx& t) {
   const uint64_t dk0 = make_sdesc_sw128(t.sK, 16, 1024);
   const uint64_t dv0 = make_sdesc_sw128(t.sV, C::BC * 128, 1024);
   bool ok = true;
-  auto issue_s = [&](int q, int j) {
+  auto issue_s = [&](int q, int u) {
     const uint64_t a0 = dq0 + (uint64_t)((q * C::Q_BYTES) >> 4);
-    const uint64_t b0 = dk0 + (uint64_t)(((j % C::STAGES) * C::KV_BYTES) >> 4);
+    const uint64_t b0 = dk0 + (uint64_t)(((u % C::STAGES) * C::KV_BYTES) >> 4);
     const uint32_t tS = t.tmem + C::TMEM_S + 128 * q;
 #pragma unroll
     for (int k = 0; k < C::D / 16; ++k)
       umma_ss(tS, a0 + kmajor_step<C>(k, C::BR), b0 + kmajor_step<C>(k, C::BC), idesc_qk, k > 0 ? 1u : 0u);
     umma_commit(t.bar(PB_S + q));
   };
-  auto issue_pv = [&](int q, int j) {
-    const uint64_t b0 = dv0 + (uint64_t)(((j % C::STAGES) * C::KV_BYTES) >> 4);
+  auto issue_pv = [&](int q, int u) {
+    const uint64_t b0 = dv0 + (uint64_t)(((u % C::STAGES) * C::KV_BYTES) >> 4);
     const uint32_t tS = t.tmem + C::TMEM_S + 128 * q;
     const uint32_t tO = t.tmem + C::TMEM_O + C::D * q;
-    if (split_tile<C, BF16, CAUSAL>(j, t.q0[q], t.n)) {
+    const int jj = BAND ? u - t.first[q] : u;
+    if (split_tile<BF16>(!t.tm[q].full(u), t.few_keys)) {
 #pragma unroll
       for (int k = 0; k < C::BC / 16; ++k) {
         const uint64_t b = b0 + (uint64_t)((k * 16 * 128) >> 4);
-        umma_ts(tO, tS + k * 8, b, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+        umma_ts(tO, tS + k * 8, b, idesc_pv, (jj > 0 || k > 0) ? 1u : 0u);
         umma_ts(tO, tS + C::BC / 2 + k * 8, b, idesc_pv, 1u);
       }
     } else {
 #pragma unroll
       for (int k = 0; k < C::BC / 16; ++k)
-        umma_ts(tO, tS + k * 8, b0 + (uint64_t)((k * 16 * 128) >> 4), idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+        umma_ts(tO, tS + k * 8, b0 + (uint64_t)((k * 16 * 128) >> 4), idesc_pv, (jj > 0 || k > 0) ? 1u : 0u);
     }
-    if (j + 1 == t.nkv[q]) umma_commit(t.bar(PB_O + q));
+    if (jj + 1 == t.nkv[q]) umma_commit(t.bar(PB_O + q));
   };
 #pragma unroll
   for (int q = 0; q < C::NQ; ++q)
     if (ok && t.nkv[q] > 0) ok = wait_or_abort(t.bar(PB_Q + q), 0, t.abort_flag, t.status, kSiteMmaQ);
-  if (ok) ok = wait_or_abort(t.bar(PB_KFULL), 0, t.abort_flag, t.status, kSiteMmaK);
+  if (ok && t.nu > 0) ok = wait_or_abort(t.bar(PB_KFULL), 0, t.abort_flag, t.status, kSiteMmaK);
   if (ok) {
     tc_fence_after();
 #pragma unroll
     for (int q = 0; q < C::NQ; ++q)
-      if (t.nkv[q] > 0) issue_s(q, 0);
-    for (int j = 0; j < t.nkv_max && ok; ++j) {
-      const int s = j % C::STAGES;
-      const int s1 = (j + 1) % C::STAGES;
+      if (t.nkv[q] > 0 && t.first[q] == 0) issue_s(q, 0);
+    // Per streamed tile u: O~_A += P_A V_u, S_A(u+1); O~_B += P_B V_u, S_B(u+1),
+    // each product only for the tiles whose key range holds that tile.  Every
+    // u lies in some tile's range (the ranges are made contiguous at set-up),
+    // so both loads of stage u are waited for before it is handed back.
+    // Without BAND every range starts at streamed tile 0 (first == 0), and
+    // the loop needs no branch for a tile that starts later: this loop body
+    // is the MMA thread's hot code, and its size shows in the step time.
+    for (int u = 0; u < t.nu && ok; ++u) {
+      const int s = u % C::STAGES;
+      const int s1 = (u + 1) % C::STAGES;
       bool have_v = false, have_k = false;
 #pragma unroll
       for (int q = 0; q < C::NQ; ++q) {
-        if (!ok || j >= t.nkv[q]) continue;
-        ok = wait_or_abort(t.bar(PB_P + q), (uint32_t)j & 1, t.abort_flag, t.status, kSiteMmaP);
-        if (ok && !have_v) {
-          ok = wait_or_abort(t.bar(PB_VFULL + s), (uint32_t)(j / C::STAGES) & 1, t.abort_flag, t.status, kSiteMmaV);
-          have_v = true;
-        }
         if (!ok) continue;
-        tc_fence_after();
-        issue_pv(q, j);
-        if (j + 1 < t.nkv[q]) {
+        const int jj = BAND ? u - t.first[q] : u;
+        if (BAND && jj == -1) {  // tile q starts at the next streamed tile: its first S product
           if (!have_k) {
-            ok = wait_or_abort(t.bar(PB_KFULL + s1), (uint32_t)((j + 1) / C::STAGES) & 1, t.abort_flag, t.status,
+            ok = wait_or_abort(t.bar(PB_KFULL + s1), (uint32_t)((u + 1) / C::STAGES) & 1, t.abort_flag, t.status,
                                kSiteMmaK);
             have_k = true;
             if (!ok) continue;
             tc_fence_after();
           }
-          issue_s(q, j + 1);
+          issue_s(q, u + 1);
+          continue;
+        }
+        if (jj < 0 || jj >= t.nkv[q]) continue;
+        ok = wait_or_abort(t.bar(PB_P + q), (uint32_t)jj & 1, t.abort_flag, t.status, kSiteMmaP);
+        if (ok && !have_v) {
+          ok = wait_or_abort(t.bar(PB_VFULL + s), (uint32_t)(u / C::STAGES) & 1, t.abort_flag, t.status, kSiteMmaV);
+          have_v = true;
+        }
+        if (!ok) continue;
+        tc_fence_after();
+        issue_pv(q, u);
+        if (jj + 1 < t.nkv[q]) {
+          if (!have_k) {
+            ok = wait_or_abort(t.bar(PB_KFULL + s1), (uint32_t)((u + 1) / C::STAGES) & 1, t.abort_flag, t.status,
+                               kSiteMmaK);
+            have_k = true;
+            if (!ok) continue;
+            tc_fence_after();
+          }
+          issue_s(q, u + 1);
         }
       }
       if (ok) umma_commit(t.bar(PB_KVEMPTY + s));
@@ -242,14 +273,22 @@ __device__ __forceinline__ void pp_p_chunk(const uint32_t* sr, int ch, uint32_t 
   if constexpr (SPLIT) tmem_st_32x32b_x16(tS + C::BC / 2 + ch * 16, pl);
 }
 
-template <class C, bool BF16, bool CAUSAL>
-__device__ __forceinline__ void pp_softmax(const PairCtx& t, const KernelParams& p, int q, int warp, int lane) {
+template <class C, bool BF16, bool BAND>
+__device__ __forceinline__ void pp_softmax(const PairCtx& t, const KernelParams& p, const CtaFacts* facts, int q,
+                                           int warp, int lane) {
   const int nkv = q ? t.nkv[1] : t.nkv[0];   // selects, not a runtime-indexed local array
   const int q0 = q ? t.q0[1] : t.q0[0];
-  if (nkv == 0) return;
+  const int kt0 = t.kv0 + (q ? t.first[1] : t.first[0]);
+  const TileMask tmask = (q ? t.tm[1] : t.tm[0]).from(q ? t.first[1] : t.first[0]);  // by local index j
+  const bool few_keys = t.few_keys;
   const int quad = warp & 3;
   const int r = quad * 32 + lane;
   const int row = q0 + r;
+  if (q0 >= t.seq.n_q) return;
+  if (nkv == 0) {
+    store_empty_row<C::D>(p, t.seq, row);
+    return;
+  }
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
   const uint32_t tS = t.tmem + lane_off + C::TMEM_S + 128 * q;
   const uint32_t tO = t.tmem + lane_off + C::TMEM_O + C::D * q;
@@ -267,15 +306,8 @@ __device__ __forceinline__ void pp_softmax(const PairCtx& t, const KernelParams&
     for (int c = 0; c < C::BC; c += 32) tmem_ld_32x32b_x32(tS + c, sr + c);
 #pragma unroll
     for (int c = 0; c < C::BC; c += 32) tmem_ld_wait_x32(sr + c);
-    const int k0 = j * C::BC;
-    const bool masked = (k0 + C::BC > t.n) || (CAUSAL && (k0 + C::BC - 1 > q0));
-    if (masked) {
-#pragma unroll
-      for (int c = 0; c < C::BC; ++c) {
-        const int key = k0 + c;
-        if (key >= t.n || (CAUSAL && key > row)) sr[c] = __float_as_uint(-INFINITY);
-      }
-    }
+    const bool masked = !tmask.full(j);
+    if (masked) mask_scores<C::BC, BAND>(sr, facts->km, row, (kt0 + j) * C::BC);
     float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
     for (int c = 0; c < C::BC; c += 8) {
@@ -289,7 +321,7 @@ __device__ __forceinline__ void pp_softmax(const PairCtx& t, const KernelParams&
     const float m_new = raise ? m_tile : m_run;
     const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
     const float alpha = raise ? ex2_approx(m_run - m_use) : 1.f;
-    const bool split = split_tile<C, BF16, CAUSAL>(j, q0, t.n);
+    const bool split = split_tile<BF16>(masked, few_keys);
     const float2 scale2 = make_float2(sl2, sl2);
     const float2 neg_m2 = make_float2(-m_use, -m_use);
     float2 sum0 = make_float2(0.f, 0.f), sum1 = make_float2(0.f, 0.f);
@@ -329,28 +361,13 @@ __device__ __forceinline__ void pp_softmax(const PairCtx& t, const KernelParams&
   }
   if (!ok) return;
   tc_fence_after();
-  const float inv_l = 1.f / l_run;
-  uint8_t* o_row = reinterpret_cast<uint8_t*>(p.o) + ((size_t)t.bh * (size_t)t.n + (size_t)row) * (C::D * 2);
-#pragma unroll 1
-  for (int c = 0; c < C::D; c += 32) {
-    uint32_t o[32];
-    tmem_ld_32x32b_x32(tO + c, o);
-    tmem_ld_wait_x32(o);
-    uint32_t packed[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      packed[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-    if (row < t.n) {
-      uint4* dst = reinterpret_cast<uint4*>(o_row + c * 2);
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-    }
-  }
-  if (row < t.n) p.lse[(size_t)t.bh * (size_t)t.n + (size_t)row] = (m_run + log2f(l_run)) * 0.6931471805599453f;
+  store_row<C::D, BF16>(p, facts->seq, row, tO, m_run, l_run);
 }
 
-template <int D, bool BF16, bool CAUSAL>
+// BAND: the first key a query row sees may depend on the row (a bounded left
+// window or a prefix), so the two tiles' key ranges may start at different
+// key tiles; without it both start at key tile 0.
+template <int D, bool BF16, bool BAND>
 __global__ void __launch_bounds__(384, 1)
     fa2_fwd_pingpong_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const KernelParams p) {
@@ -361,30 +378,59 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t sbase = smem_u32(smem);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  CtaFacts* facts = reinterpret_cast<CtaFacts*>(smem + C::OFF_MISC + 16);
+  static_assert(16 + sizeof(CtaFacts) <= C::MISC_BYTES, "shared-memory misc area");
   const int warp = (int)(threadIdx.x >> 5);
   const int lane = (int)(threadIdx.x & 31);
 
   PairCtx t;
+  int bh, pair;
+  unit_of_block((int)blockIdx.x, p.bh, p.units, bh, pair);
+  // The whole CTA leaves together, before any barrier or TMEM set-up, when
+  // its sequence is malformed or shorter than this pair's rows.
+  if (!seq_info(p, bh, t.seq)) return;
+  if (pair * (C::NQ * C::BR) >= t.seq.n_q) return;
   t.bar0 = sbase + C::OFF_BAR;
   t.sQ = sbase + C::OFF_Q;
   t.sK = sbase + C::OFF_K;
   t.sV = sbase + C::OFF_V;
   t.abort_flag = abort_flag;
   t.status = p.status;
-  t.n = p.n;
-  const int pairs = (t.n + C::NQ * C::BR - 1) / (C::NQ * C::BR);
-  int pair;
-  unit_of_block((int)blockIdx.x, p.bh, pairs, t.bh, pair);
-  t.nkv_max = 0;
+  t.km = key_mask(p, t.seq);
+  int lo_tile[C::NQ];
+  int kv0 = 0x7fffffff, kv_end = 0;
+#pragma unroll
   for (int q = 0; q < C::NQ; ++q) {
-    t.q0[q] = pair * (C::NQ * C::BR) + q * C::BR;
-    if (t.q0[q] >= t.n) {
-      t.nkv[q] = 0;
+    const int q0 = pair * (C::NQ * C::BR) + q * C::BR;
+    t.q0[q] = q0;
+    t.nkv[q] = 0;
+    lo_tile[q] = 0;
+    if (q0 < t.seq.n_q) {
+      const int last = min(q0 + C::BR, t.seq.n_q) - 1;
+      t.tm[q] = tile_mask<BAND>(t.km, q0, last, C::BC);
+      int lo, end;
+      if (t.km.template tile_range<BAND>(q0, last, lo, end)) {
+        lo_tile[q] = lo / C::BC;
+        t.nkv[q] = (end + C::BC - 1) / C::BC - lo_tile[q];
+        kv0 = min(kv0, lo_tile[q]);
+        kv_end = max(kv_end, lo_tile[q] + t.nkv[q]);
+      }
     } else {
-      const int kv_end = CAUSAL ? min(t.n, t.q0[q] + C::BR) : t.n;
-      t.nkv[q] = (kv_end + C::BC - 1) / C::BC;
+      t.tm[q] = t.tm[0];
     }
-    t.nkv_max = max(t.nkv_max, t.nkv[q]);
+  }
+  // The streamed range must have no tile that neither query tile uses.  Both
+  // band edges are non-decreasing in the row, so with a tile of each kind the
+  // ranges touch or overlap; should they not, tile A is stretched across the
+  // gap (the extra tiles are masked out element by element: P = 0 there).
+  if (BAND && t.nkv[0] > 0 && t.nkv[1] > 0 && lo_tile[1] > lo_tile[0] + t.nkv[0]) t.nkv[0] = lo_tile[1] - lo_tile[0];
+  t.kv0 = kv_end > 0 ? kv0 : 0;
+  t.nu = kv_end > 0 ? kv_end - kv0 : 0;
+  t.few_keys = t.km.n_k <= 2 * C::BC;
+#pragma unroll
+  for (int q = 0; q < C::NQ; ++q) {
+    t.first[q] = t.nkv[q] > 0 ? lo_tile[q] - t.kv0 : 0;
+    t.tm[q] = t.tm[q].from(t.kv0);
   }
 
   if (threadIdx.x == 0) {
@@ -401,6 +447,8 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(t.bar(PB_EXIT), 1);
     *abort_flag = 0;
+    facts->seq = t.seq;
+    facts->km = t.km;
     fence_mbar_init();
   }
   if (warp == C::TMA_WARP && lane == 0) {
@@ -420,14 +468,14 @@ __global__ void __launch_bounds__(384, 1)
   if (warp >= 8) {
     regs_decrease<C::REGS_OTHER>();
     if (warp == C::TMA_WARP) {
-      if (lane == 0) pp_producer<C>(t, &tm_q, &tm_k, &tm_v);
+      if (lane == 0) pp_producer<C>(t, p, &tm_q, &tm_k, &tm_v);
     } else if (warp == C::MMA_WARP) {
-      if (lane == 0) pp_mma<C, BF16, CAUSAL>(t);
+      if (lane == 0) pp_mma<C, BF16, BAND>(t);
       __syncwarp();
     }
   } else {
     regs_increase<C::REGS_SOFTMAX>();
-    pp_softmax<C, BF16, CAUSAL>(t, p, warp >> 2, warp, lane);
+    pp_softmax<C, BF16, BAND>(t, p, facts, warp >> 2, warp, lane);
   }
   tc_fence_before();
   __syncthreads();
@@ -437,10 +485,10 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool BAND>
 int launch_fwd_pingpong(const LaunchArgs& a) {
   using C = PingPongConfig<D>;
-  auto kern = fa2_fwd_pingpong_kernel<D, BF16, CAUSAL>;
+  auto kern = fa2_fwd_pingpong_kernel<D, BF16, BAND>;
   static std::atomic<unsigned long long> configured{0};
   const int e = once_per_device(configured, [&]() -> int {
     // The softmax warpgroups' setmaxnreg.inc only completes if the block was
@@ -452,16 +500,17 @@ int launch_fwd_pingpong(const LaunchArgs& a) {
     return (int)cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
   });
   if (e != 0) return e;
-  const int pairs = (a.p.n + C::NQ * C::BR - 1) / (C::NQ * C::BR);
-  dim3 grid((unsigned)(a.p.bh * pairs));
+  static_assert(C::NQ * C::BR == 256, "query rows per CTA: tile_geometry(d).cta_rows sizes the grid");
+  dim3 grid((unsigned)(a.p.bh * a.p.units));
   kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.p);
   return (int)cudaGetLastError();
 }
 
 template <int D>
 int launch_fwd_pingpong_dispatch(const LaunchArgs& a) {
-  if (a.bf16) return a.causal ? launch_fwd_pingpong<D, true, true>(a) : launch_fwd_pingpong<D, true, false>(a);
-  return a.causal ? launch_fwd_pingpong<D, false, true>(a) : launch_fwd_pingpong<D, false, false>(a);
+  if (a.band) return a.bf16 ? launch_fwd_pingpong<D, true, true>(a) : launch_fwd_pingpong<D, false, true>(a);
+  return a.bf16 ? launch_fwd_pingpong<D, true, false>(a) : launch_fwd_pingpong<D, false, false>(a);
 }
+
 
 }  // namespace fa2

@@ -16,21 +16,41 @@ namespace fa2 {
 // FA2_ERR_DEVICE_TIMEOUT.
 constexpr uint32_t kStatusTimeout = 1u;
 
+// Forward-pass arguments the kernels read.  Element (b, h, i) of O lives at
+// o + b*o_bs + h*o_hs + (row0_q(b) + i)*o_rs elements, of LSE at
+// lse + b*l_bs + h*l_hs + row0_q(b) + i, where row0_q(b) is cu_q[b] for packed
+// variable-length batches and 0 otherwise (keys: cu_k[b] and 0).
 struct KernelParams {
-  void* o;            // [B,H,N,d] 16-bit output
-  float* lse;         // [B,H,N] float32 output
+  void* o;            // 16-bit output
+  float* lse;         // float32 output
   uint32_t* status;   // device status word (library-owned)
-  int n;              // sequence length N
-  int num_q_tiles;    // ceil(N / 128)
+  const int* cu_q;    // [B+1] query row offsets of packed sequences, or null
+  const int* cu_k;    // [B+1] key row offsets, or null (set iff cu_q is)
+  long long o_bs, o_hs, o_rs;  // O strides in elements (head-dim stride 1)
+  long long l_bs, l_hs;        // LSE strides in elements (row stride 1)
+  int n_q;            // query rows per sequence (packed: the maximum)
+  int n_k;            // keys per sequence (packed: the maximum)
+  int total_q;        // packed: rows of q/o/lse (bound for cu_q); else n_q
+  int total_k;        // packed: rows of k/v (bound for cu_k); else n_k
+  int heads;          // H
+  int merged_bh;      // 1: the tensor maps are 3-D (d, rows, B*H), coordinate b*H + h; 0: 4-D
   int bh;             // B * H
+  int units;          // query units (tiles or tile pairs) per (b, h), from n_q
+  int window_left;    // key j visible to query i iff i+off-wl <= j <= i+off+wr
+  int window_right;   //   (off = N_k - N_q; -1 = unbounded on that side),
+  int prefix;         //   or j < prefix (keys every query sees)
   float scale_log2;   // scale * log2(e): scores go to the exp2 domain
 };
 
+// Bit of the status word a forward kernel sets when a packed batch's row
+// offsets are out of range; that sequence is left unwritten.
+constexpr uint32_t kStatusBadSeqlens = 2u;
+
 struct LaunchArgs {
-  CUtensorMap tm_q, tm_k, tm_v;
+  CUtensorMap tm_q, tm_k, tm_v;  // (d, rows, B*H) or (d, rows, H, B) maps, boxes of 64 columns
   KernelParams p;
   bool bf16;
-  bool causal;
+  bool band;  // window_left >= 0 or prefix > 0: a row's first visible key depends on the row
   cudaStream_t stream;
 };
 
@@ -63,11 +83,13 @@ struct BwdLaunchArgs {
 int launch_bwd_d64(const BwdLaunchArgs& a);
 int launch_bwd_d128(const BwdLaunchArgs& a);
 
-// Host-side tile geometry the launcher needs to build tensor maps: rows of Q
-// per CTA tile and rows of K/V per streamed tile, per head dim.
+// Host-side tile geometry the launcher needs to build tensor maps and size
+// the grid: rows of Q per tile, rows of K/V per streamed tile and query rows
+// per CTA, per head dim.
 struct TileGeometry {
   int q_rows;
   int kv_rows;
+  int cta_rows;
 };
 
 TileGeometry tile_geometry(int d);

@@ -45,7 +45,8 @@ typedef enum {
   FA2_ERR_MISALIGNED = 3,     /* a pointer is not 16-byte aligned */
   FA2_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed */
   FA2_ERR_DEVICE_TIMEOUT = 5, /* a kernel wait ran out of time (fa2_get_device_status) */
-  FA2_ERR_SCRATCH_LIMIT = 6   /* problem too large for fa2_fwd_host_noalloc's static scratch */
+  FA2_ERR_SCRATCH_LIMIT = 6,  /* problem too large for fa2_fwd_host_noalloc's static scratch */
+  FA2_ERR_DEVICE_SEQLENS = 7  /* packed-batch offsets out of range (fa2_get_device_status) */
 } fa2_status;
 
 /*
@@ -70,6 +71,91 @@ typedef enum {
  */
 int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
             int B, int H, int N, int d, float scale, int causal, int dtype, void* stream);
+
+/*
+ * fa2_fwd_params -- arguments of fa2_fwd_ex, the general forward pass:
+ * strided layouts, unequal query and key lengths, band and prefix masks and
+ * packed variable-length batches.
+ *
+ * Which keys a query sees (the additive 0 / -inf mask of the Flash Attention
+ * 2 page, "Causal masking", Option A, with the key tiles the mask removes
+ * entirely skipped): in a sequence of N_q queries and N_k keys, query i is
+ * aligned with key i + off, off = N_k - N_q (the last query with the last
+ * key), and sees key j (0 <= j < N_k) iff
+ *
+ *     j < prefix_len,  or
+ *     i + off - window_left <= j <= i + off + window_right
+ *
+ * where a window of -1 is unbounded on that side.  So (-1, -1) is full
+ * attention, (-1, 0) causal (j <= i when N_q = N_k), (w, 0) a sliding window
+ * of the w keys before each query and itself, and (-1, 0) with prefix_len = P
+ * a prefix-LM (the first P keys visible to every query).  A query that sees
+ * no key gets O = 0 and LSE = -inf.
+ *
+ * Element (b, h, i, c) of a tensor X in {q, o} is at
+ *   X + b*X_strides[0] + h*X_strides[1] + (r0 + i)*X_strides[2] + c
+ * elements, and of k, v likewise with key rows; lse (b, h, i) is at
+ *   lse + b*lse_strides[0] + h*lse_strides[1] + (r0 + i).
+ * Unpacked batches: r0 = 0, i < seqlen_q, j < seqlen_k.  Packed batches
+ * (cu_seqlens_q and cu_seqlens_k both set): sequence b's query rows are
+ * cu_seqlens_q[b] <= r < cu_seqlens_q[b+1] of q/o/lse (r0 = cu_seqlens_q[b])
+ * and its keys cu_seqlens_k[b] <= r < cu_seqlens_k[b+1] of k/v; the batch
+ * strides are ignored.
+ */
+typedef struct fa2_fwd_params {
+  const void* q;          /* device, `dtype`, 16-byte aligned; read only */
+  const void* k;          /* device, `dtype`, 16-byte aligned; read only */
+  const void* v;          /* device, `dtype`, 16-byte aligned; read only */
+  void* o;                /* device, `dtype`, 16-byte aligned; written */
+  float* lse;             /* device, float32, 4-byte aligned; written (natural log) */
+  int batch;              /* B >= 1 (packed: number of sequences) */
+  int heads;              /* H >= 1 */
+  int seqlen_q;           /* N_q >= 1 (packed: the longest sequence's query count) */
+  int seqlen_k;           /* N_k >= 1 (packed: ignored) */
+  int head_dim;           /* d: 64, 128 or 256 */
+  int dtype;              /* FA2_FP16 or FA2_BF16 */
+  float scale;            /* finite, > 0 */
+  int window_left;        /* >= 0, or -1 = unbounded */
+  int window_right;       /* >= 0, or -1 = unbounded */
+  int prefix_len;         /* >= 0 */
+  int64_t q_strides[3];   /* batch, head, row strides in elements; multiples of 8 */
+  int64_t k_strides[3];   /*   (a stride of a dimension of size 1 is ignored) */
+  int64_t v_strides[3];
+  int64_t o_strides[3];
+  int64_t lse_strides[2]; /* batch, head strides in elements (row stride 1); >= 0 */
+  const int* cu_seqlens_q; /* device, [batch + 1] int32 row offsets, or NULL */
+  const int* cu_seqlens_k; /* device, [batch + 1] int32 row offsets, or NULL */
+  int total_q;            /* packed: rows of q, o and lse (>= 1); else ignored */
+  int total_k;            /* packed: rows of k and v (>= 1); else ignored */
+} fa2_fwd_params;
+
+/* sizeof(fa2_fwd_params) as compiled into the library (binding check). */
+size_t fa2_fwd_params_size(void);
+
+/*
+ * fa2_fwd_ex -- the forward pass for fa2_fwd_params (asynchronous on
+ * `stream`).  Same arithmetic and kernels as fa2_fwd, which is the special
+ * case of contiguous [B,H,N,d] tensors, N_q = N_k = N, no prefix and
+ * window (-1, causal ? 0 : -1).
+ *
+ * Checks before any launch: sizes, dtype, head dim, scale and windows as
+ * documented above (FA2_ERR_INVALID_ARG / FA2_ERR_UNSUPPORTED); pointers
+ * non-null and aligned and strides of dimensions larger than 1 positive
+ * multiples of 8 elements below 2^39 (FA2_ERR_MISALIGNED for alignment,
+ * FA2_ERR_INVALID_ARG otherwise); the byte ranges o and lse can touch
+ * overlap neither each other nor those of q, k and v (FA2_ERR_INVALID_ARG);
+ * only one of cu_seqlens_q / cu_seqlens_k set (FA2_ERR_INVALID_ARG).  The
+ * caller keeps o's elements distinct (no two (b,h,i,c) at one address).
+ *
+ * Packed offsets live on the device and are checked by the kernel: a
+ * sequence with cu_seqlens_q[b] > cu_seqlens_q[b+1], an offset outside
+ * [0, total_q] (or [0, total_k] for keys), or more than seqlen_q queries is
+ * left unwritten and the next fa2_get_device_status returns
+ * FA2_ERR_DEVICE_SEQLENS.  Rows of k and v outside a sequence may be read
+ * (key tiles are 128 rows) and are multiplied by P = 0, so they must hold
+ * finite values; rows past total_k read as zero.  Deterministic.
+ */
+int fa2_fwd_ex(const fa2_fwd_params* params, void* stream);
 
 /*
  * fa2_fwd_host -- the same forward pass on HOST buffers, end to end.
@@ -130,9 +216,10 @@ int fa2_fwd_host_noalloc(const void* q_host, const void* k_host, const void* v_h
 
 /*
  * fa2_get_device_status -- synchronises `stream`, then returns and clears the
- * current device's status word: FA2_OK, or FA2_ERR_DEVICE_TIMEOUT if some
+ * current device's status word: FA2_OK, FA2_ERR_DEVICE_TIMEOUT if some
  * kernel's bounded wait on an mbarrier gave up (the kernel then abandoned its
- * tile, released its tensor memory and returned instead of hanging).
+ * tile, released its tensor memory and returned instead of hanging), else
+ * FA2_ERR_DEVICE_SEQLENS if fa2_fwd_ex met out-of-range packed offsets.
  * `detail` (may be NULL) receives the raw status bits (role and wait site).
  */
 int fa2_get_device_status(void* stream, uint32_t* detail);
@@ -155,7 +242,7 @@ int fa2_get_device_status(void* stream, uint32_t* detail);
  *   other arguments  : as fa2_fwd
  *
  * dK and dV are each written once; dQ is accumulated over key tiles with
- * fp32 atomic adds, so its last bits may vary between runs.  Outputs and
+ * fp32 reduce-adds in L2 (TMA), so its last bits may vary between runs.  Outputs and
  * workspace must not overlap any input or each other.
  */
 int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,

@@ -46,7 +46,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(7):
+    for code in range(8):
         s = fa2.fa2_status_string(code)
         assert isinstance(s, str) and s
     assert fa2.fa2_status_string(0) == "ok"
@@ -118,3 +118,77 @@ def test_host_entry_point_checks(lib):
 def test_selftest_limit_checked(lib):
     assert lib.fa2_selftest_wait_timeout(0, None) == fa2.FA2_ERR_INVALID_ARG
     assert lib.fa2_selftest_wait_timeout(1000001, None) == fa2.FA2_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- fa2_fwd_ex argument checks
+
+
+def _params(**kw):
+    """A valid contiguous [1, 2, 64, 64] problem (pointers are stand-ins), then overrides."""
+    p = fa2.Fa2FwdParams()
+    p.q, p.k, p.v, p.o, p.lse = A, 2 * A, 3 * A, 4 * A, 5 * A
+    p.batch, p.heads, p.seqlen_q, p.seqlen_k, p.head_dim = 1, 2, 64, 64, 64
+    p.dtype, p.scale = 0, 0.125
+    p.window_left, p.window_right, p.prefix_len = -1, -1, 0
+    for name in ("q_strides", "k_strides", "v_strides", "o_strides"):
+        getattr(p, name)[:] = [2 * 64 * 64, 64 * 64, 64]
+    p.lse_strides[:] = [128, 64]
+    for key, val in kw.items():
+        if isinstance(val, list):
+            getattr(p, key)[:] = val
+        else:
+            setattr(p, key, val)
+    return p
+
+
+def _ex(lib, **kw):
+    return lib.fa2_fwd_ex(ctypes.byref(_params(**kw)), None)
+
+
+def test_params_struct_matches_library(lib):
+    assert lib.fa2_fwd_params_size() == ctypes.sizeof(fa2.Fa2FwdParams)
+
+
+def test_ex_null_params(lib):
+    assert lib.fa2_fwd_ex(None, None) == fa2.FA2_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(window_left=-2), fa2.FA2_ERR_INVALID_ARG),
+    (dict(window_right=-5), fa2.FA2_ERR_INVALID_ARG),
+    (dict(prefix_len=-1), fa2.FA2_ERR_INVALID_ARG),
+    (dict(seqlen_k=0), fa2.FA2_ERR_INVALID_ARG),
+    (dict(seqlen_q=0), fa2.FA2_ERR_INVALID_ARG),
+    (dict(head_dim=96), fa2.FA2_ERR_UNSUPPORTED),
+    (dict(dtype=3), fa2.FA2_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa2.FA2_ERR_INVALID_ARG),
+    (dict(q_strides=[8192, 4096, 68]), fa2.FA2_ERR_MISALIGNED),      # row stride not a multiple of 8
+    (dict(k_strides=[8192, 4100, 64]), fa2.FA2_ERR_MISALIGNED),      # head stride not a multiple of 8
+    (dict(v_strides=[8192, 0, 64]), fa2.FA2_ERR_INVALID_ARG),        # zero stride on a dimension of size 2
+    (dict(o_strides=[8192, 4096, -64]), fa2.FA2_ERR_INVALID_ARG),    # negative stride
+    (dict(q_strides=[8192, 4096, 1 << 40]), fa2.FA2_ERR_INVALID_ARG),
+    (dict(lse=5 * A + 2), fa2.FA2_ERR_MISALIGNED),
+    (dict(o=4 * A + 8), fa2.FA2_ERR_MISALIGNED),
+    (dict(o=2 * A + 2048), fa2.FA2_ERR_INVALID_ARG),                 # o inside k
+    (dict(lse=3 * A + 4096), fa2.FA2_ERR_INVALID_ARG),               # lse inside v
+    (dict(lse=4 * A + 8192), fa2.FA2_ERR_INVALID_ARG),               # lse inside o
+    (dict(cu_seqlens_q=7 * A), fa2.FA2_ERR_INVALID_ARG),             # only one offsets array
+    (dict(cu_seqlens_q=7 * A, cu_seqlens_k=8 * A, total_q=0, total_k=64), fa2.FA2_ERR_INVALID_ARG),
+    (dict(cu_seqlens_q=7 * A + 2, cu_seqlens_k=8 * A, total_q=64, total_k=64), fa2.FA2_ERR_MISALIGNED),
+    (dict(q=0), fa2.FA2_ERR_INVALID_ARG),
+    (dict(batch=2 ** 20, heads=2 ** 10, seqlen_q=2 ** 20), fa2.FA2_ERR_UNSUPPORTED),
+])
+def test_ex_bad_arguments_rejected(lib, kw, code):
+    assert _ex(lib, **kw) == code
+
+
+def test_ex_stride_of_size_one_dimension_is_ignored(lib):
+    # batch = 1: an unaligned batch stride is never used, so the call gets past the
+    # stride checks and fails on the (deliberate) overlap of o with k instead
+    assert _ex(lib, q_strides=[3, 4096, 64], o=2 * A + 2048) == fa2.FA2_ERR_INVALID_ARG
+    assert _ex(lib, q_strides=[3, 4096, 64], batch=2, o=2 * A + 2048) == fa2.FA2_ERR_MISALIGNED
+
+
+def test_ex_bnhd_output_overlap_detected(lib):
+    # o as a [B, N, H, d] layout (row stride H*d, head stride d) reaching into lse
+    assert _ex(lib, o_strides=[8192, 64, 128], lse=4 * A + 16000) == fa2.FA2_ERR_INVALID_ARG
