@@ -92,3 +92,50 @@ def tiled_attention(Q, K, V, B_r: int, B_c: int, scale: float = 1.0, causal: boo
             O[i:i + B_r] = Ot / l[:, None]
         L[i:i + B_r] = m + np.log(l)
     return O, L
+
+
+def split_keys_attention(Q, K, V, scale: float, chunk: int, visible=None, merge_rescale: bool = True):
+    """Split-over-keys attention (the decoding regime) in numpy float64 -- test infrastructure only.
+
+    The keys are cut into chunks of ``chunk`` rows; for every query row each
+    chunk yields the online-softmax state of its visible keys on its own --
+    local maximum m_c (-inf when the chunk shows the row nothing), l_c =
+    sum exp(s - m_c) and O~_c = sum exp(s - m_c) v -- and the states are then
+    merged with the same rescaling step the tiled loop applies between key
+    tiles (Lesson 6.6, "Online softmax"; FlashAttention V2 in depth, section
+    3.2): M = max_c m_c, l = sum_c exp(m_c - M) l_c, O = sum_c exp(m_c - M)
+    O~_c / l, L = M + log l.  A row that sees no key gets O = 0, L = -inf.
+    ``visible`` is a boolean [N_q, N_k] mask (None: every key visible).
+    ``merge_rescale=False`` plants the slip of merging without the factors
+    exp(m_c - M), so tests can check that it breaks exactness.
+
+    Q [N_q, d], K [N_k, d], V [N_k, d_v]; returns O [N_q, d_v], L [N_q].
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    n_q, n_k = Q.shape[0], K.shape[0]
+    if visible is None:
+        visible = np.ones((n_q, n_k), dtype=bool)
+    states = []
+    for c0 in range(0, n_k, chunk):
+        S = scale * (Q @ K[c0:c0 + chunk].T)
+        S = np.where(visible[:, c0:c0 + chunk], S, -np.inf)
+        m = S.max(axis=1)
+        shift = np.where(np.isneginf(m), 0.0, m)
+        P = np.exp(S - shift[:, None])                 # exp(-inf) = 0 for hidden keys
+        states.append((m, P.sum(axis=1), P @ V[c0:c0 + chunk]))
+    M = np.max([s[0] for s in states], axis=0)
+    l = np.zeros(n_q)
+    Ot = np.zeros((n_q, V.shape[1]))
+    for m, lc, Oc in states:
+        if merge_rescale:
+            f = np.where(np.isneginf(m), 0.0, np.exp(m - np.where(np.isneginf(M), 0.0, M)))
+        else:
+            f = np.ones(n_q)
+        l += f * lc
+        Ot += f[:, None] * Oc
+    empty = ~(l > 0)
+    O = np.where(empty[:, None], 0.0, Ot / np.where(empty, 1.0, l)[:, None])
+    L = np.where(empty, -np.inf, M + np.log(np.where(empty, 1.0, l)))
+    return O, L
