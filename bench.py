@@ -60,6 +60,16 @@ def measured_peak():
         return 1900.0, "of fallback (1.9 PFLOP/s bf16)"
 
 
+def measured_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "of measured (copy bandwidth, MEASURED_PEAKS.json)"
+    except Exception:
+        return 6800.0, "of fallback (6.8 TB/s)"
+
+
 def recorded_traffic(workload: int):
     """DRAM bytes per launch from the committed ncu summary, if it matches this kernel source."""
     path = os.path.join(ROOT, "profiles", "traffic_per_launch.txt")
@@ -157,6 +167,26 @@ def oracle_sample(w: sy.Workload, q, k, v, target_s: float, rng, threads: int = 
     return done_flops, done_s, done_rows
 
 
+def oracle_sample_masked(w: sy.Workload, gen, q, k, v, target_s: float, rng, threads: int = 0):
+    """oracle_sample for the general options (band / prefix mask, N_k != N): random rows
+    through the oracle's sampled-row masked forward; flops 4*d per visible key."""
+    import oracle
+
+    BH, nq, nk = w.B * w.H, gen["seqlen_q"], gen["seqlen_k"]
+    vis = sy.visible_keys(nq, nk, gen["window_left"], gen["window_right"], gen["prefix"])
+    done_flops, done_s, done_rows = 0.0, 0.0, 0
+    while done_s < target_s:
+        bh = np.full(ORACLE_ROWS_PER_BATCH, int(rng.integers(0, BH)))
+        rows = rng.integers(0, nq, size=ORACLE_ROWS_PER_BATCH)
+        t0 = time.perf_counter()
+        oracle.attention_rows_masked(q, k, v, w.dtype, w.scale, bh, rows, window_left=gen["window_left"],
+                                     window_right=gen["window_right"], prefix_len=gen["prefix"], threads=threads)
+        done_s += time.perf_counter() - t0
+        done_flops += float(4.0 * w.d * vis[rows].sum())
+        done_rows += rows.size
+    return done_flops, done_s, done_rows
+
+
 def max_over_ranks(value: float, dist=None, device=None) -> float:
     """The maximum of `value` over every rank of the default process group
     (the value itself when there is no group)."""
@@ -181,20 +211,30 @@ def dist_env():
     return ws, rank, local
 
 
-def run_reference(args, w):
+def run_reference(args, w, gen=None):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
     import oracle
 
-    q, k, v = w.inputs()
+    if gen is not None and gen["varlen_seqs"]:
+        print(json.dumps({"impl": "reference", "unavailable": "the CPU oracle arm samples rows of unpacked "
+                          "problems only; run without --varlen-seqs"}), flush=True)
+        return 0
+    if gen is None:
+        q, k, v = w.inputs()
+        sample = lambda t, r: oracle_sample(w, q, k, v, t, r)
+    else:
+        q = sy.make_qkv(w.B, w.H, gen["seqlen_q"], w.d, w.dtype, w.seed(0), w.q_scale)[0]
+        _, k, v = sy.make_qkv(w.B, w.H, gen["seqlen_k"], w.d, w.dtype, w.seed(0) + 1)
+        sample = lambda t, r: oracle_sample_masked(w, gen, q, k, v, t, r)
     rng = np.random.default_rng(12345)
     per_step = max(0.5, min(4.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        oracle_sample(w, q, k, v, per_step / 4, rng)
+        sample(per_step / 4, rng)
     flops, secs, rows = 0.0, 0.0, 0
     for _ in range(args.steps):
-        f, s, r = oracle_sample(w, q, k, v, per_step, rng)
+        f, s, r = sample(per_step, rng)
         flops, secs, rows = flops + f, secs + s, rows + r
     value = flops / secs / 1e12
     cores = oracle.max_threads()
@@ -202,7 +242,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(w, args.gpus),
+        "data": "synthetic", "config": workload_config(w, args.gpus, gen),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": "%d random (head,row) rows of the workload, each step ~%.1f s of CPU work; "
                                    "flops counted 4*d per visible key" % (rows, per_step)},
@@ -212,12 +252,111 @@ def run_reference(args, w):
     return 0
 
 
-def workload_config(w: sy.Workload, n_gpus: int):
-    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
-            "dtype": "bf16" if w.dtype == sy.BF16 else "fp16", "causal": w.causal,
-            "scale": "1/sqrt(d)", "q_scale": w.q_scale,
-            "l2": "inputs (%.0f MB) larger than the 129 MB L2; no flush" % (3 * w.B * w.H * w.N * w.d * 2 / 1e6),
-            "parallelism": "replicas x%d" % n_gpus, "seed": w.seed(0)}
+def workload_config(w: sy.Workload, n_gpus: int, gen=None):
+    c = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+         "dtype": "bf16" if w.dtype == sy.BF16 else "fp16", "causal": w.causal,
+         "scale": "1/sqrt(d)", "q_scale": w.q_scale,
+         "l2": "inputs (%.0f MB) larger than the 129 MB L2; no flush" % (3 * w.B * w.H * w.N * w.d * 2 / 1e6),
+         "parallelism": "replicas x%d" % n_gpus, "seed": w.seed(0)}
+    if gen is not None:
+        c["workload"] = w.name + " " + gen["label"]
+        c["causal"] = None
+        c["mask"] = {k: gen[k] for k in ("window_left", "window_right", "prefix", "seqlen_k", "layout", "varlen_seqs")}
+        c["l2"] = "inputs (%.0f MB) vs the 129 MB L2; no flush" % (gen["input_bytes"] / 1e6)
+    return c
+
+
+def general_mask(args, w: sy.Workload):
+    """The general-forward options as one dict, or None when none is given."""
+    if (args.window_left is None and args.window_right is None and args.prefix == 0 and args.seqlen_k == 0
+            and args.layout == "bhnd" and args.varlen_seqs == 0 and args.decode_rows == 0):
+        return None
+    if args.decode_rows and (args.varlen_seqs or args.seqlen_k or args.layout != "bhnd"):
+        raise SystemExit("--decode-rows takes the workload's N as the key count; no --varlen-seqs/--seqlen-k/--layout")
+    wl = -1 if args.window_left is None else args.window_left
+    wr = (0 if w.causal else -1) if args.window_right is None else args.window_right
+    nk = args.seqlen_k or w.N
+    nq = args.decode_rows or w.N
+    if args.varlen_seqs and args.seqlen_k:
+        raise SystemExit("--varlen-seqs packs self-attention sequences (N_k = N_q); drop --seqlen-k")
+    label = "window(%d,%d)" % (wl, wr)
+    if args.prefix:
+        label += " prefix%d" % args.prefix
+    if nk != w.N:
+        label += " Nk%d" % nk
+    if args.layout != "bhnd":
+        label += " " + args.layout
+    if args.varlen_seqs:
+        label += " varlen%d" % args.varlen_seqs
+    if args.decode_rows:
+        label = "decode %d row%s vs %d keys " % (nq, "s" if nq > 1 else "", nk) + label
+    rows_q, rows_k = w.B * nq, w.B * nk    # per head
+    inputs = (rows_q + 2 * rows_k) * w.H * w.d * 2
+    return {"window_left": wl, "window_right": wr, "prefix": args.prefix, "seqlen_k": nk, "layout": args.layout,
+            "varlen_seqs": args.varlen_seqs, "decode_rows": args.decode_rows, "seqlen_q": nq, "label": label,
+            "input_bytes": inputs,
+            "bytes": inputs + rows_q * w.H * (w.d * 2 + 4)}
+
+
+def varlen_lengths(total: int, seqs: int, seed: int) -> np.ndarray:
+    """Seeded random sequence lengths (each >= 1) summing to total."""
+    rng = np.random.default_rng(seed)
+    cuts = np.sort(rng.choice(np.arange(1, total), size=seqs - 1, replace=False))
+    return np.diff(np.concatenate([[0], cuts, [total]])).astype(np.int64)
+
+
+def general_step(fa2, torch, w: sy.Workload, gen, dev, tdt, stream):
+    """Inputs, the timed fa2_fwd_ex call and its algorithmic FLOPs for the general options."""
+    wl, wr, pre = gen["window_left"], gen["window_right"], gen["prefix"]
+    to_dev = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(tdt).to(dev)
+    if gen["varlen_seqs"]:
+        T = w.B * w.N
+        lens = varlen_lengths(T, gen["varlen_seqs"], w.seed(0) + 7)
+        q_bits, k_bits, v_bits = sy.make_qkv(1, w.H, T, w.d, w.dtype, w.seed(0), w.q_scale)
+        q, k, v = (to_dev(x[0].transpose(1, 0, 2)) for x in (q_bits, k_bits, v_bits))   # [T, H, d]
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((w.H, T), dtype=torch.float32, device=dev)
+        vis = sum(int(sy.visible_keys(int(n), int(n), wl, wr, pre).sum()) for n in lens)
+        maxlen = int(lens.max())
+        gen["lengths"] = "min %d / median %d / max %d" % (lens.min(), int(np.median(lens)), maxlen)
+
+        def step():
+            fa2.fa2_fwd_ex(q, k, v, o, lse, scale=w.scale, window_left=wl, window_right=wr, prefix_len=pre,
+                           cu_seqlens_q=cu, cu_seqlens_k=cu, max_seqlen_q=maxlen, stream=stream)
+        flops = 4.0 * w.d * w.H * vis
+        return step, flops, None, None, None
+    nk = gen["seqlen_k"]
+    if gen["decode_rows"]:
+        nq = gen["seqlen_q"]
+        q_bits = sy.make_qkv(w.B, w.H, nq, w.d, w.dtype, w.seed(0), w.q_scale)[0]
+        _, k_bits, v_bits = sy.make_qkv(w.B, w.H, nk, w.d, w.dtype, w.seed(0) + 1)
+        q, k, v = (to_dev(x) for x in (q_bits, k_bits, v_bits))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, nq), dtype=torch.float32, device=dev)
+        ws = torch.empty(fa2.fa2_decode_workspace_bytes(q, k, v, window_left=wl, window_right=wr, prefix_len=pre),
+                         dtype=torch.uint8, device=dev)
+
+        def step():
+            fa2.fa2_decode(q, k, v, o, lse, workspace=ws, scale=w.scale, window_left=wl, window_right=wr,
+                           prefix_len=pre, stream=stream)
+        flops = 4.0 * w.d * w.B * w.H * float(sy.visible_keys(nq, nk, wl, wr, pre).sum())
+        return step, flops, q_bits, k_bits, v_bits
+    q_bits = sy.make_qkv(w.B, w.H, w.N, w.d, w.dtype, w.seed(0), w.q_scale)[0]
+    _, k_bits, v_bits = sy.make_qkv(w.B, w.H, nk, w.d, w.dtype, w.seed(0) + 1)
+    if gen["layout"] == "bnhd":   # [B, N, H, d] storage, passed as [B, H, N, d] views
+        q, k, v = (to_dev(x.transpose(0, 2, 1, 3)).transpose(1, 2) for x in (q_bits, k_bits, v_bits))
+        o = torch.empty((w.B, w.N, w.H, w.d), dtype=tdt, device=dev).transpose(1, 2)
+    else:
+        q, k, v = (to_dev(x) for x in (q_bits, k_bits, v_bits))
+        o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+
+    def step():
+        fa2.fa2_fwd_ex(q, k, v, o, lse, scale=w.scale, window_left=wl, window_right=wr, prefix_len=pre,
+                       stream=stream)
+    flops = 4.0 * w.d * w.B * w.H * float(sy.visible_keys(w.N, nk, wl, wr, pre).sum())
+    return step, flops, q_bits, k_bits, v_bits
 
 
 def launch_mode(args):
@@ -241,14 +380,28 @@ def main():
                     help="launch the timed steps one by one instead of replaying them from a CUDA graph")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (fa2_bwd) instead: 2.5x the forward FLOPs (five products)")
+    g = ap.add_argument_group("general forward (fa2_fwd_ex); FLOPs then count 4*d per visible (query, key) pair")
+    g.add_argument("--window-left", type=int, default=None, help="keys before the aligned one (-1: unbounded)")
+    g.add_argument("--window-right", type=int, default=None,
+                   help="keys after the aligned one (-1: unbounded; default 0 if the workload is causal)")
+    g.add_argument("--prefix", type=int, default=0, help="keys every query sees (prefix-LM)")
+    g.add_argument("--seqlen-k", type=int, default=0, help="N_k (default N); queries face the last N keys")
+    g.add_argument("--layout", choices=["bhnd", "bnhd"], default="bhnd", help="storage order of q, k, v, o")
+    g.add_argument("--varlen-seqs", type=int, default=0,
+                   help="pack the B*N query tokens as this many sequences of seeded random lengths")
+    g.add_argument("--decode-rows", type=int, default=0,
+                   help="time fa2_decode: this many query rows (<= 8) per (b, h) against the workload's N keys")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = sy.WORKLOADS[args.workload]
     if args.heads > 0:
         w = sy.Workload(w.index, w.B, args.heads, w.N, w.d, w.dtype, w.causal, w.q_scale)
+    gen = general_mask(args, w)
+    if gen is not None and args.backward:
+        ap.error("the general-forward options time the forward pass only")
     if args.impl == "reference":
-        return run_reference(args, w)
+        return run_reference(args, w, gen)
 
     import torch
 
@@ -277,6 +430,10 @@ def main():
 
     def step():
         fa2.fa2_fwd(q, k, v, o, lse, scale=w.scale, causal=w.causal, stream=stream)
+
+    flops = w.flops() * (2.5 if args.backward else 1.0)
+    if gen is not None:
+        step, flops, q_bits, k_bits, v_bits = general_step(fa2, torch, w, gen, dev, tdt, stream)
 
     if args.backward:
         with torch.cuda.stream(stream):
@@ -339,7 +496,6 @@ def main():
     if dist is not None:
         dist.barrier()
 
-    flops = w.flops() * (2.5 if args.backward else 1.0)
     value = job_throughput(flops, args.steps, ws, max_ms)
     avg_launch_ms = sum(kernel_ms) / len(kernel_ms)
     achieved = flops / (avg_launch_ms / 1e3) / 1e12
@@ -347,7 +503,16 @@ def main():
 
     e2e = None
     cpu = None
-    if rank == 0 and not args.kernel_only and not args.backward:
+    if rank == 0 and not args.kernel_only and gen is not None and ws == 1 and not args.no_cpu_baseline \
+            and q_bits is not None:
+        import oracle
+
+        f, s, rows = oracle_sample_masked(w, gen, q_bits, k_bits, v_bits, args.cpu_seconds,
+                                          np.random.default_rng(7))
+        cpu = {"value": f / s / 1e12, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+               "sample": "%d random (head,row) rows of the workload in %.1f s (fp64 oracle, OpenMP); "
+                         "flops counted 4*d per visible key" % (rows, s)}
+    if rank == 0 and not args.kernel_only and not args.backward and gen is None:
         # end to end through the host-buffer entry point: H2D of q, k, v and D2H of o, lse each step
         qh, kh, vh = (h.pin_memory() for h in host)
         oh = torch.empty(q.shape, dtype=tdt).pin_memory()
@@ -380,20 +545,32 @@ def main():
             "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == sy.BF16 else "fp16",
-            "data": "synthetic", "config": dict(workload_config(w, ws), launch=launch_mode(args)),
+            "data": "synthetic", "config": dict(workload_config(w, ws, gen), launch=launch_mode(args)),
             "pct_of_peak": 100.0 * value / ws / peak,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                         "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
+                         "frac": achieved / peak,
+                         "traffic": recorded_traffic(args.workload) if gen is None else None,
                          "peak_source": peak_note, "kernel": ("fa2_bwd_kernel" if args.backward else
                                     "fa2_fwd_pingpong_kernel" if w.d <= 128 else "fa2_fwd_dbuf_kernel"),
                          "avg_launch_ms": avg_launch_ms,
                          "algorithmic_flops_per_launch": flops,
-                         "algorithmic_bytes_per_launch": w.algorithmic_bytes() * (2 if args.backward else 1)},
+                         "algorithmic_bytes_per_launch": (w.algorithmic_bytes() * (2 if args.backward else 1)
+                                                          if gen is None else gen["bytes"])},
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                        "samples": clk["samples"]},
             "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": args.steps * (3 if args.backward else 1),
             "kernel_sha": kernel_source_hash(),
         }
+        if gen is not None and gen["decode_rows"]:
+            # HBM-bound: K and V read once dominate; roofline against the measured copy bandwidth
+            hbm, hbm_note = measured_hbm()
+            gbs = gen["bytes"] / (avg_launch_ms / 1e3) / 1e9
+            line["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                                "traffic": None, "peak_source": hbm_note,
+                                "kernel": "fa2_decode_kernel + fa2_decode_merge_kernel",
+                                "avg_launch_ms": avg_launch_ms, "algorithmic_bytes_per_launch": gen["bytes"],
+                                "algorithmic_flops_per_launch": flops}
+            line["gpu_launches"] = 2 * args.steps
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()

@@ -24,6 +24,7 @@ FA2_ERR_CUDA = 4
 FA2_ERR_DEVICE_TIMEOUT = 5
 FA2_ERR_SCRATCH_LIMIT = 6
 FA2_ERR_DEVICE_SEQLENS = 7
+FA2_DECODE_MAX_Q = 8
 FA2_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _lib = None
@@ -89,6 +90,10 @@ def load_library():
     lib.fa2_fwd_params_size.restype = sz
     lib.fa2_fwd_ex.argtypes = [ctypes.POINTER(Fa2FwdParams), vp]
     lib.fa2_fwd_ex.restype = ci
+    lib.fa2_decode.argtypes = [ctypes.POINTER(Fa2FwdParams), vp, sz, vp]
+    lib.fa2_decode.restype = ci
+    lib.fa2_decode_workspace_bytes.argtypes = [ctypes.POINTER(Fa2FwdParams)]
+    lib.fa2_decode_workspace_bytes.restype = sz
     if lib.fa2_fwd_params_size() != ctypes.sizeof(Fa2FwdParams):
         raise RuntimeError("fa2_fwd_params layout mismatch: library %d bytes, binding %d bytes"
                            % (lib.fa2_fwd_params_size(), ctypes.sizeof(Fa2FwdParams)))
@@ -151,23 +156,9 @@ def fa2_fwd(q, k, v, o=None, lse=None, scale=None, causal=False, stream=None):
     return o, lse
 
 
-def fa2_fwd_ex(q, k, v, o=None, lse=None, scale=None, window_left=-1, window_right=-1, prefix_len=0,
-               cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, stream=None):
-    """General forward (fa2_fwd_ex): strided views, N_q != N_k, band / prefix masks, packed batches.
-
-    Unpacked: q [B, H, N_q, d], k and v [B, H, N_k, d], any CUDA views whose
-    last dimension is contiguous (e.g. ``x.transpose(1, 2)`` of a [B, N, H, d]
-    tensor); o (default: new contiguous [B, H, N_q, d]) and lse (default: new
-    [B, H, N_q] float32) may be views too.
-
-    Packed (cu_seqlens_q and cu_seqlens_k, int32 CUDA [B + 1]): q [total_q, H, d],
-    k and v [total_k, H, d]; o [total_q, H, d] and lse [H, total_q] by default;
-    ``max_seqlen_q`` (default: total_q) bounds every sequence's query count.
-
-    Query i of a sequence sees key j iff j < prefix_len or
-    i + off - window_left <= j <= i + off + window_right, off = N_k - N_q
-    (-1 = unbounded).  causal is window (-1, 0).  Returns (o, lse).
-    """
+def _general_params(q, k, v, o, lse, scale, window_left, window_right, prefix_len, cu_seqlens_q, cu_seqlens_k,
+                    max_seqlen_q, max_seqlen_k):
+    """Marshal tensors into an Fa2FwdParams (allocating o and lse when not given)."""
     import torch
     packed = cu_seqlens_q is not None or cu_seqlens_k is not None
     if packed and (cu_seqlens_q is None or cu_seqlens_k is None):
@@ -194,8 +185,9 @@ def fa2_fwd_ex(q, k, v, o=None, lse=None, scale=None, window_left=-1, window_rig
             o = torch.empty_like(q, memory_format=torch.contiguous_format)
         if lse is None:
             lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
-        n_q = total_q if max_seqlen_q is None else int(max_seqlen_q)
-        p.batch, p.heads, p.seqlen_q, p.seqlen_k = B, H, n_q, 0
+        p.batch, p.heads = B, H
+        p.seqlen_q = total_q if max_seqlen_q is None else int(max_seqlen_q)
+        p.seqlen_k = total_k if max_seqlen_k is None else int(max_seqlen_k)
         p.total_q, p.total_k = total_q, total_k
         for name, t in (("q_strides", q), ("k_strides", k), ("v_strides", v), ("o_strides", o)):
             getattr(p, name)[:] = [0, t.stride(1), t.stride(0)]
@@ -222,9 +214,62 @@ def fa2_fwd_ex(q, k, v, o=None, lse=None, scale=None, window_left=-1, window_rig
     p.head_dim, p.dtype = d, _dtype_code(q)
     p.scale = 1.0 / float(d) ** 0.5 if scale is None else float(scale)
     p.window_left, p.window_right, p.prefix_len = int(window_left), int(window_right), int(prefix_len)
+    return p, o, lse
+
+
+def fa2_fwd_ex(q, k, v, o=None, lse=None, scale=None, window_left=-1, window_right=-1, prefix_len=0,
+               cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, stream=None):
+    """General forward (fa2_fwd_ex): strided views, N_q != N_k, band / prefix masks, packed batches.
+
+    Unpacked: q [B, H, N_q, d], k and v [B, H, N_k, d], any CUDA views whose
+    last dimension is contiguous (e.g. ``x.transpose(1, 2)`` of a [B, N, H, d]
+    tensor); o (default: new contiguous [B, H, N_q, d]) and lse (default: new
+    [B, H, N_q] float32) may be views too.
+
+    Packed (cu_seqlens_q and cu_seqlens_k, int32 CUDA [B + 1]): q [total_q, H, d],
+    k and v [total_k, H, d]; o [total_q, H, d] and lse [H, total_q] by default;
+    ``max_seqlen_q`` (default: total_q) bounds every sequence's query count.
+
+    Query i of a sequence sees key j iff j < prefix_len or
+    i + off - window_left <= j <= i + off + window_right, off = N_k - N_q
+    (-1 = unbounded).  causal is window (-1, 0).  Returns (o, lse).
+    """
+    p, o, lse = _general_params(q, k, v, o, lse, scale, window_left, window_right, prefix_len, cu_seqlens_q,
+                                cu_seqlens_k, max_seqlen_q, None)
     rc = load_library().fa2_fwd_ex(ctypes.byref(p), _stream_handle(stream, q.device))
     if rc:
         raise Fa2Error(rc, "fa2_fwd_ex")
+    return o, lse
+
+
+def fa2_decode_workspace_bytes(q, k, v, **kw) -> int:
+    """Workspace fa2_decode needs for these tensors and options (same keywords as fa2_decode)."""
+    p, _, _ = _general_params(q, k, v, kw.get("o"), kw.get("lse"), kw.get("scale"), kw.get("window_left", -1),
+                              kw.get("window_right", -1), kw.get("prefix_len", 0), kw.get("cu_seqlens_q"),
+                              kw.get("cu_seqlens_k"), kw.get("max_seqlen_q"), kw.get("max_seqlen_k"))
+    return int(load_library().fa2_decode_workspace_bytes(ctypes.byref(p)))
+
+
+def fa2_decode(q, k, v, o=None, lse=None, workspace=None, scale=None, window_left=-1, window_right=-1, prefix_len=0,
+               cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, stream=None):
+    """Decoding-regime forward (fa2_decode): at most FA2_DECODE_MAX_Q query rows per sequence.
+
+    Same tensors and options as fa2_fwd_ex; ``workspace`` (a CUDA uint8
+    tensor, allocated here when not given) holds the per-split partial
+    states; packed batches take ``max_seqlen_k`` (default: total_k), the
+    longest sequence's key count.  Returns (o, lse).
+    """
+    import torch
+    p, o, lse = _general_params(q, k, v, o, lse, scale, window_left, window_right, prefix_len, cu_seqlens_q,
+                                cu_seqlens_k, max_seqlen_q, max_seqlen_k)
+    lib = load_library()
+    need = int(lib.fa2_decode_workspace_bytes(ctypes.byref(p)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    rc = lib.fa2_decode(ctypes.byref(p), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                        _stream_handle(stream, q.device))
+    if rc:
+        raise Fa2Error(rc, "fa2_decode")
     return o, lse
 
 

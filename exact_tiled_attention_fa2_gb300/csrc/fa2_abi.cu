@@ -13,6 +13,7 @@
 
 #include "../../include/fa2.h"
 #include "fa2_common.cuh"
+#include "fa2_decode.cuh"
 #include "fa2_internal.h"
 
 namespace fa2 {
@@ -88,11 +89,12 @@ bool mergeable(long long heads, long long batch, const long long st[3]) {
 // Rows past `rows` read as zeros.  The stride of a dimension of size 1 never
 // addresses anything and is replaced by a valid placeholder.
 int encode_map_rows(CUtensorMap* m, const void* base, int d, long long rows, long long heads, long long batch,
-                    const long long st[3], int box_rows, bool bf16, bool merged) {
+                    const long long st[3], int box_rows, bool bf16, bool merged, int box_cols = 64,
+                    CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   const long long row_st = rows > 1 ? st[2] : d, head_st = heads > 1 ? st[1] : d, batch_st = batch > 1 ? st[0] : d;
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads, (cuuint64_t)batch};
   cuuint64_t strides[3] = {(cuuint64_t)row_st * 2, (cuuint64_t)head_st * 2, (cuuint64_t)batch_st * 2};
-  cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t box[4] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   cuuint32_t rank = 4;
   if (merged) {
@@ -102,8 +104,7 @@ int encode_map_rows(CUtensorMap* m, const void* base, int d, long long rows, lon
   }
   CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rank,
                         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA2_OK : FA2_ERR_CUDA;
 }
 
@@ -116,15 +117,38 @@ struct MapKey {
   long long strides[3][3];   // batch, head, row strides of each (elements)
 };
 
-// The tensor maps of the last forward call on this host thread: repeated
-// calls on the same buffers and shapes (the usual case in a loop) skip
-// re-encoding them.
+// The tensor maps of the last forward (and, separately, decode) call on this
+// host thread: repeated calls on the same buffers and shapes (the usual case
+// in a loop) skip re-encoding them.
 struct MapCache {
   bool valid = false;
   MapKey key;
   CUtensorMap tm_q, tm_k, tm_v;
 };
 thread_local MapCache t_maps;
+thread_local MapCache t_decode_maps;
+
+// K and V maps of the decode kernel: whole rows (d columns) x
+// decode_block_rows(d) rows per box, no swizzle (rows land contiguously).
+int cached_decode_maps(DecodeLaunchArgs& a, const MapKey& key) {
+  MapCache& c = t_decode_maps;
+  if (!(c.valid && std::memcmp(&c.key, &key, sizeof(MapKey)) == 0)) {
+    const bool bf16 = key.dtype == FA2_BF16;
+    CUtensorMap* maps[2] = {&c.tm_k, &c.tm_v};
+    c.valid = false;
+    for (int i = 0; i < 2; ++i) {
+      if (encode_map_rows(maps[i], key.ptr[i + 1], key.d, key.dims[i + 1][0], key.dims[i + 1][1],
+                          key.dims[i + 1][2], key.strides[i + 1], decode_block_rows(key.d), bf16, key.merged != 0,
+                          key.d, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return FA2_ERR_CUDA;
+    }
+    std::memcpy(&c.key, &key, sizeof(MapKey));
+    c.valid = true;
+  }
+  a.tm_k = c.tm_k;
+  a.tm_v = c.tm_v;
+  return FA2_OK;
+}
 
 int cached_maps(LaunchArgs& a, const MapKey& key) {
   MapCache& c = t_maps;
@@ -231,12 +255,10 @@ int check_stride(long long n, long long st, bool tma) {
   return FA2_OK;
 }
 
-int forward_checked(const fa2_fwd_params& a, cudaStream_t stream);
-
-// Validates the general forward arguments (no CUDA call), then launches.  A
-// batch whose (batch, head) strides merge in every tensor (batch stride =
-// H x head stride, as in contiguous [B,H,N,d]) runs as one batch of B*H heads.
-int forward(const fa2_fwd_params& a_in, cudaStream_t stream) {
+// A batch whose (batch, head) strides merge in every tensor (batch stride =
+// H x head stride, as in contiguous [B,H,N,d]) runs as one batch of B*H
+// heads: the kernels then need no division to find a CTA's batch.
+fa2_fwd_params fold_batches(const fa2_fwd_params& a_in) {
   fa2_fwd_params a = a_in;
   const bool packed = a.cu_seqlens_q != nullptr || a.cu_seqlens_k != nullptr;
   if (!packed && a.batch > 1 && a.heads > 1) {
@@ -248,10 +270,22 @@ int forward(const fa2_fwd_params& a_in, cudaStream_t stream) {
       a.batch = 1;
     }
   }
-  return forward_checked(a, stream);
+  return a;
 }
 
-int forward_checked(const fa2_fwd_params& a, cudaStream_t stream) {
+// Validated arguments turned into kernel parameters and map descriptions.
+struct Prepared {
+  KernelParams p;
+  MapKey key;            // q, k, v: pointers, dims, strides, rank
+  long long q_st[3];     // q strides (the decode kernel reads q directly)
+  bool band;             // a row's first visible key depends on the row
+};
+
+// Checks every argument (no CUDA call before they pass), then fills `out`;
+// `units_rows` is the query rows one CTA covers (sizes KernelParams.units).
+// `scratch` (optional): a further buffer the launch writes, which must overlap
+// none of the tensors.
+int prepare(const fa2_fwd_params& a, int units_rows, Prepared& out, const Extent* scratch = nullptr) {
   if (a.dtype != FA2_FP16 && a.dtype != FA2_BF16) return FA2_ERR_INVALID_ARG;
   if (a.batch < 1 || a.heads < 1 || a.seqlen_q < 1) return FA2_ERR_INVALID_ARG;
   if (!std::isfinite(a.scale) || !(a.scale > 0.f)) return FA2_ERR_INVALID_ARG;
@@ -266,8 +300,7 @@ int forward_checked(const fa2_fwd_params& a, cudaStream_t stream) {
   if (reinterpret_cast<uintptr_t>(a.lse) & 3u) return FA2_ERR_MISALIGNED;
   if (packed && ((reinterpret_cast<uintptr_t>(a.cu_seqlens_q) | reinterpret_cast<uintptr_t>(a.cu_seqlens_k)) & 3u))
     return FA2_ERR_MISALIGNED;
-  const TileGeometry g = tile_geometry(d);
-  const long long units = ((long long)a.seqlen_q + g.cta_rows - 1) / g.cta_rows;
+  const long long units = ((long long)a.seqlen_q + units_rows - 1) / units_rows;
   if ((long long)a.batch * a.heads * units > INT_MAX) return FA2_ERR_UNSUPPORTED;
 
   // tensor batch dimension (1 when packed: sequences are rows) and row counts
@@ -301,11 +334,16 @@ int forward_checked(const fa2_fwd_params& a, cudaStream_t stream) {
   if (overlap(e_o, e_l)) return FA2_ERR_INVALID_ARG;
   for (const Extent& in : ins)
     if (overlap(e_o, in) || overlap(e_l, in)) return FA2_ERR_INVALID_ARG;
+  if (scratch) {
+    if (overlap(*scratch, e_o) || overlap(*scratch, e_l)) return FA2_ERR_INVALID_ARG;
+    for (const Extent& in : ins)
+      if (overlap(*scratch, in)) return FA2_ERR_INVALID_ARG;
+  }
 
   DeviceState* ds = nullptr;
   int rc = device_state(&ds);
   if (rc) return rc;
-  MapKey key;
+  MapKey& key = out.key;
   std::memset(&key, 0, sizeof(key));
   if (cudaGetDevice(&key.dev) != cudaSuccess) return FA2_ERR_CUDA;
   key.dtype = a.dtype;
@@ -322,11 +360,9 @@ int forward_checked(const fa2_fwd_params& a, cudaStream_t stream) {
   key.merged = 1;
   for (int t = 0; t < 3; ++t)
     if (!mergeable(a.heads, tb, st_in[t])) key.merged = 0;
-  LaunchArgs la;
-  std::memset(&la, 0, sizeof(la));
-  rc = cached_maps(la, key);
-  if (rc) return rc;
-  KernelParams& p = la.p;
+  for (int i = 0; i < 3; ++i) out.q_st[i] = st_in[0][i];
+  KernelParams& p = out.p;
+  std::memset(&p, 0, sizeof(p));
   p.o = a.o;
   p.lse = a.lse;
   p.status = ds->status;
@@ -349,14 +385,104 @@ int forward_checked(const fa2_fwd_params& a, cudaStream_t stream) {
   p.window_right = a.window_right;
   p.prefix = a.prefix_len;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  out.band = a.window_left >= 0 || a.prefix_len > 0;
+  return FA2_OK;
+}
+
+// Validates the general forward arguments (no CUDA call before they pass),
+// then launches the tiled kernel for the head dim.
+int forward(const fa2_fwd_params& a_in, cudaStream_t stream) {
+  const fa2_fwd_params a = fold_batches(a_in);
+  Prepared pr;
+  int rc = prepare(a, tile_geometry(a.head_dim).cta_rows, pr);
+  if (rc) return rc;
+  LaunchArgs la;
+  std::memset(&la, 0, sizeof(la));
+  rc = cached_maps(la, pr.key);
+  if (rc) return rc;
+  la.p = pr.p;
   la.bf16 = a.dtype == FA2_BF16;
-  la.band = a.window_left >= 0 || a.prefix_len > 0;
+  la.band = pr.band;
   la.stream = stream;
   int e = 0;
-  switch (d) {
+  switch (a.head_dim) {
     case 64: e = launch_fwd_d64(la); break;
     case 128: e = launch_fwd_d128(la); break;
     default: e = launch_fwd_d256(la); break;
+  }
+  return e == 0 ? FA2_OK : FA2_ERR_CUDA;
+}
+
+// Key splits of the decode path: enough CTAs for two on each of the 152 SMs
+// of a GB300 (independent of the device, so the workspace size is too), no
+// split shorter than kDecodeMinChunk keys, chunks a multiple of a stage.
+constexpr long long kDecodeTargetCtas = 2 * 152;
+constexpr long long kDecodeMinChunk = 256;
+
+struct DecodePlan {
+  int splits, chunk;
+  size_t ws_o_bytes, ws_ml_bytes;
+};
+
+// 0, or a status: N_q <= FA2_DECODE_MAX_Q, plus the plan for these sizes.
+int decode_plan(const fa2_fwd_params& a, DecodePlan& out) {
+  if (a.seqlen_q < 1 || a.seqlen_q > FA2_DECODE_MAX_Q) return FA2_ERR_UNSUPPORTED;
+  if (a.seqlen_k < 1 || a.batch < 1 || a.heads < 1) return FA2_ERR_INVALID_ARG;
+  if (a.head_dim != 64 && a.head_dim != 128 && a.head_dim != 256) return FA2_ERR_UNSUPPORTED;
+  const long long bh = (long long)a.batch * a.heads;
+  const long long nk = a.seqlen_k;
+  const long long block = decode_block_rows(a.head_dim);
+  long long splits = kDecodeTargetCtas / bh;
+  const long long useful = (nk + kDecodeMinChunk - 1) / kDecodeMinChunk;
+  if (splits > useful) splits = useful;
+  if (splits < 1) splits = 1;
+  long long chunk = (nk + splits - 1) / splits;
+  chunk = (chunk + block - 1) / block * block;
+  splits = (nk + chunk - 1) / chunk;
+  if (bh * splits > INT_MAX || bh * a.seqlen_q > INT_MAX) return FA2_ERR_UNSUPPORTED;
+  out.splits = (int)splits;
+  out.chunk = (int)chunk;
+  const size_t slots = (size_t)bh * (size_t)a.seqlen_q * (size_t)splits;
+  out.ws_o_bytes = align256(slots * (size_t)a.head_dim * 4);
+  out.ws_ml_bytes = align256(slots * 2 * 4);
+  return FA2_OK;
+}
+
+int decode(const fa2_fwd_params& a_in, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  const fa2_fwd_params a = fold_batches(a_in);
+  DecodePlan plan;
+  int rc = decode_plan(a, plan);
+  if (rc) return rc;
+  if (!workspace) return FA2_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA2_ERR_MISALIGNED;
+  if (workspace_bytes < plan.ws_o_bytes + plan.ws_ml_bytes) return FA2_ERR_INVALID_ARG;
+  // the workspace is written by the kernels: it must overlap none of the tensors
+  const Extent ew{workspace, plan.ws_o_bytes + plan.ws_ml_bytes};
+  Prepared pr;
+  rc = prepare(a, FA2_DECODE_MAX_Q, pr, &ew);
+  if (rc) return rc;
+  const bool packed = a.cu_seqlens_q != nullptr;
+  DecodeLaunchArgs la;
+  std::memset(&la, 0, sizeof(la));
+  rc = cached_decode_maps(la, pr.key);
+  if (rc) return rc;
+  la.p.q = a.q;
+  la.p.q_bs = packed ? 0 : pr.q_st[0];
+  la.p.q_hs = pr.q_st[1];
+  la.p.q_rs = pr.q_st[2];
+  la.p.ws_o = static_cast<float*>(workspace);
+  la.p.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.ws_o_bytes);
+  la.p.splits = plan.splits;
+  la.p.chunk = plan.chunk;
+  la.p.f = pr.p;
+  la.p.f.n_k = a.seqlen_k;   // packed: the longest sequence's key count the plan covers
+  la.bf16 = a.dtype == FA2_BF16;
+  la.stream = stream;
+  int e = 0;
+  switch (a.head_dim) {
+    case 64: e = launch_decode_d64(la); break;
+    case 128: e = launch_decode_d128(la); break;
+    default: e = launch_decode_d256(la); break;
   }
   return e == 0 ? FA2_OK : FA2_ERR_CUDA;
 }
@@ -369,6 +495,18 @@ extern "C" size_t fa2_fwd_params_size(void) { return sizeof(fa2_fwd_params); }
 extern "C" int fa2_fwd_ex(const fa2_fwd_params* params, void* stream) {
   if (!params) return FA2_ERR_INVALID_ARG;
   return forward(*params, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t fa2_decode_workspace_bytes(const fa2_fwd_params* params) {
+  if (!params) return 0;
+  DecodePlan plan;
+  if (decode_plan(fold_batches(*params), plan)) return 0;
+  return plan.ws_o_bytes + plan.ws_ml_bytes;
+}
+
+extern "C" int fa2_decode(const fa2_fwd_params* params, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!params) return FA2_ERR_INVALID_ARG;
+  return decode(*params, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,

@@ -25,6 +25,8 @@ enum WaitSite : uint32_t {
   kSiteEpilogueO = 9,
   kSiteDrain = 10,
   kSiteSelfTest = 11,
+  kSiteDecodeFull = 12,
+  kSiteDecodeMerge = 13,
 };
 
 // Wait for the phase of `bar` with the given parity for at most `limit_ns`;

@@ -1,0 +1,416 @@
+// fa2_decode.cuh -- forward pass for a few query rows against many keys (the
+// decoding regime: one new token, or a handful, attending to a long cache).
+//
+// With N_q <= 8 rows per sequence there is no query tile to fill a tensor
+// core, and the step is bound by reading K and V from HBM once: each key
+// costs 4 d bytes (16-bit K and V) against 4 d FLOPs per query row.  So the
+// keys of each (batch, head) are split into chunks, one CTA per chunk,
+// enough CTAs to cover every SM twice, and each chunk is reduced on CUDA
+// cores to the online-softmax state of every query row -- local maximum m,
+// l = sum 2^(s - m), O~ = sum 2^(s - m) v -- which a second kernel merges
+// with the same rescaling step the tiled loop applies between key tiles:
+// M = max m_c, l = sum 2^(m_c - M) l_c, O = sum 2^(m_c - M) O~_c / l (Lesson
+// 6.6, "Online softmax"; FlashAttention V2 in depth, section 3.2).  Lesson
+// 6.6 ("Common misconceptions") names this regime as needing its own kernel.
+//
+// Per CTA: a TMA warp streams [BLOCK x d] boxes of K and V through a 3-stage
+// shared-memory ring; four compute warps each take BLOCK/4 keys of a stage.
+// A key row is spread over d/8 lanes (16 bytes each), so a lane keeps only
+// its 8 elements of each query row in registers; the partial dot products
+// are summed across those lanes with xor shuffles.  The running maximum is
+// raised only past a 2^8 margin (as in the tiled kernels), so rescaling
+// O~ is rare.  At the end the per-lane-group states are merged through the
+// (then idle) stage buffers and written to the caller's workspace.
+#pragma once
+
+#include "fa2_common.cuh"
+
+namespace fa2 {
+
+struct DecodeParams {
+  const void* q;                 // query rows, 16-bit
+  long long q_bs, q_hs, q_rs;    // q strides in elements (head-dim stride 1)
+  float* ws_o;                   // [B*H][n_q][splits][d] partial O~
+  float* ws_ml;                  // [B*H][n_q][splits][2] partial (m, l), exp2 domain
+  int splits;                    // key chunks per (b, h)
+  int chunk;                     // keys per chunk (a multiple of the stage size)
+  KernelParams f;                // outputs, offsets, sizes, mask, scale (as the tiled kernels)
+};
+
+struct DecodeLaunchArgs {
+  CUtensorMap tm_k, tm_v;        // boxes of d columns x BLOCK rows, no swizzle
+  DecodeParams p;
+  bool bf16;
+  cudaStream_t stream;
+};
+
+constexpr int kDecodeMaxRows = 8;  // FA2_DECODE_MAX_Q
+constexpr float kRescaleDecodeLog2 = 8.0f;   // raise the running maximum only past a 2^8 margin
+
+template <int D_>
+struct DecodeConfig {
+  static constexpr int D = D_;
+  static constexpr int G = D / 8;                      // lanes per key row (16 bytes each)
+  static constexpr int KPW = 32 / G;                   // keys a warp takes per step
+  static constexpr int WARPS = 4;                      // compute warps
+  static constexpr int TMA_WARP = WARPS;
+  static constexpr int THREADS = (WARPS + 1) * 32;
+  static constexpr int BLOCK = decode_block_rows(D);   // keys per stage
+  static constexpr int KEYS_PER_WARP = BLOCK / WARPS;
+  static constexpr int STEPS = KEYS_PER_WARP / KPW;    // steps per warp per stage
+  static constexpr int STAGES = 3;
+  static constexpr int GROUPS = WARPS * KPW;           // lane groups in the CTA, each with its own state
+  static constexpr uint32_t TILE_BYTES = BLOCK * D * 2;
+  static constexpr uint32_t OFF_K = 0;
+  static constexpr uint32_t OFF_V = STAGES * TILE_BYTES;
+  static constexpr uint32_t OFF_BAR = 2 * STAGES * TILE_BYTES;
+  static constexpr uint32_t NUM_BARS = 2 * STAGES + 2;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 128;   // + alignment slack
+  // merge area (reuses the stage buffers once every stage is consumed)
+  static constexpr uint32_t MERGE_O_BYTES = GROUPS * kDecodeMaxRows * D * 4;
+  static constexpr uint32_t MERGE_ML_BYTES = GROUPS * kDecodeMaxRows * 2 * 4;
+  static_assert(KEYS_PER_WARP % KPW == 0, "keys per warp");
+  static_assert(MERGE_O_BYTES + MERGE_ML_BYTES <= 2 * STAGES * TILE_BYTES, "merge area");
+  static_assert(2 * SMEM_BYTES <= 232448, "two CTAs per SM");
+};
+
+enum : int {
+  DC_FULL = 0,                   // + stage: K and V of the stage landed
+  DC_EMPTY = 3,                  // + stage: four compute warps are done with it
+  DC_DONE = 6,                   // every compute warp has finished reading stages
+  DC_MERGED = 7,                 // every lane group's state is in the merge area
+};
+
+template <bool BF16>
+__device__ __forceinline__ void unpack8(const uint4& u, float* x) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = unpack2<BF16>(w[i]);
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+// The chunk of keys [c0, c1) one CTA reduces, within a sequence, clipped to
+// the keys some query row sees; false if empty.
+__device__ __forceinline__ bool decode_range(const KeyMask& km, int n_q, int split, int chunk, int& c0, int& c1) {
+  int lo, end;
+  if (!km.tile_range<true>(0, n_q - 1, lo, end)) return false;
+  c0 = max(lo, split * chunk);
+  c1 = min(end, min(km.n_k, (split + 1) * chunk));
+  return c1 > c0;
+}
+
+template <int NQ, class C, bool BF16>
+__device__ __forceinline__ void dc_compute(const DecodeParams& dp, const SeqInfo& seq, const KeyMask& km, int n_q,
+                                           int c0, int c1, uint32_t sbase, uint32_t bar0, volatile int* abort_flag,
+                                           int warp, int lane, float* st_m, float* st_l, float* st_o) {
+  const KernelParams& p = dp.f;
+  const int g = lane / C::G;            // lane group within the warp (its key of a step)
+  const int e0 = (lane % C::G) * 8;     // this lane's 8 elements of a row
+  // this lane's slice of every query row, in the exp2 domain
+  float q[NQ][8];
+#pragma unroll
+  for (int r = 0; r < NQ; ++r) {
+    if (r < n_q) {
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(dp.q) +
+                           2 * ((long long)seq.b * dp.q_bs + (long long)seq.h * dp.q_hs +
+                                (long long)(seq.row0_q + r) * dp.q_rs + e0);
+      unpack8<BF16>(*reinterpret_cast<const uint4*>(src), q[r]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) q[r][e] *= p.scale_log2;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) q[r][e] = 0.f;
+    }
+  }
+  // rows past n_q repeat the last row's band (they are computed, never stored)
+  int row_lo[NQ], row_hi[NQ];
+#pragma unroll
+  for (int r = 0; r < NQ; ++r) {
+    row_lo[r] = km.row_lo(min(r, n_q - 1));
+    row_hi[r] = km.row_hi(min(r, n_q - 1));
+  }
+  // a stage needs no per-key mask when it ends before c1 and every row sees all of it
+  const int lo_last = km.row_lo(n_q - 1);
+  const int hi_first = km.row_hi(0);
+  float m[NQ], l[NQ], o[NQ][8];
+#pragma unroll
+  for (int r = 0; r < NQ; ++r) {
+    m[r] = -INFINITY;
+    l[r] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[r][e] = 0.f;
+  }
+  const int nblk = (c1 - c0 + C::BLOCK - 1) / C::BLOCK;
+  bool ok = true;
+  for (int b = 0; b < nblk; ++b) {
+    const int s = b % C::STAGES;
+    ok = wait_or_abort(bar0 + 8u * (DC_FULL + s), (uint32_t)(b / C::STAGES) & 1, abort_flag, p.status,
+                       kSiteDecodeFull);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    const int kb0 = c0 + b * C::BLOCK;
+    const int kb1 = kb0 + C::BLOCK;
+    const bool full = kb1 <= c1 && (kb1 <= km.pre_end || (kb0 >= lo_last && kb1 - 1 <= hi_first));
+    const uint32_t sK = sbase + C::OFF_K + s * C::TILE_BYTES;
+    const uint32_t sV = sbase + C::OFF_V + s * C::TILE_BYTES;
+#pragma unroll 2
+    for (int step = 0; step < C::STEPS; ++step) {
+      const int kl = warp * C::KEYS_PER_WARP + step * C::KPW + g;   // key within the stage
+      const int key = kb0 + kl;
+      float kx[8];
+      unpack8<BF16>(lds128(sK + kl * (C::D * 2) + e0 * 2), kx);
+      float sc[NQ];
+#pragma unroll
+      for (int r = 0; r < NQ; ++r) {
+        float a = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a = fmaf(q[r][e], kx[e], a);
+#pragma unroll
+        for (int off = C::G / 2; off >= 1; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+        sc[r] = a;
+      }
+      if (!full) {
+#pragma unroll
+        for (int r = 0; r < NQ; ++r) {
+          const bool vis = key < c1 && (key < km.pre_end || (key >= row_lo[r] && key <= row_hi[r]));
+          if (!vis) sc[r] = -INFINITY;
+        }
+      }
+      float vx[8];
+      unpack8<BF16>(lds128(sV + kl * (C::D * 2) + e0 * 2), vx);
+#pragma unroll
+      for (int r = 0; r < NQ; ++r) {
+        if (sc[r] > m[r] + kRescaleDecodeLog2) {   // raise the maximum (rare after the first key)
+          const float alpha = ex2_approx(m[r] - sc[r]);   // 0 when m was -inf
+          m[r] = sc[r];
+          l[r] *= alpha;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[r][e] *= alpha;
+        }
+        const float pr = ex2_approx(sc[r] - (m[r] == -INFINITY ? 0.f : m[r]));   // 0 for a hidden key
+        l[r] += pr;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[r][e] = fmaf(pr, vx[e], o[r][e]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar0 + 8u * (DC_EMPTY + s));
+  }
+  // every stage consumed: the stage buffers become the merge area
+  if (lane == 0) mbar_arrive(bar0 + 8u * DC_DONE);
+  if (ok) ok = wait_or_abort(bar0 + 8u * DC_DONE, 0, abort_flag, p.status, kSiteDecodeMerge);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok) return;
+  const int grp = warp * C::KPW + g;
+#pragma unroll
+  for (int r = 0; r < NQ; ++r) {
+    if (lane % C::G == 0) {
+      st_m[grp * kDecodeMaxRows + r] = m[r];
+      st_l[grp * kDecodeMaxRows + r] = l[r];
+    }
+    float4* dst = reinterpret_cast<float4*>(st_o + ((size_t)grp * kDecodeMaxRows + r) * C::D + e0);
+    dst[0] = make_float4(o[r][0], o[r][1], o[r][2], o[r][3]);
+    dst[1] = make_float4(o[r][4], o[r][5], o[r][6], o[r][7]);
+  }
+}
+
+// Merge the CTA's lane-group states and write its partial for every query row.
+template <class C>
+__device__ __forceinline__ void dc_write_partial(const DecodeParams& dp, int bh, int split, int n_q, const float* st_m,
+                                                 const float* st_l, const float* st_o, bool empty, int tid) {
+  for (int idx = tid; idx < n_q * C::D; idx += C::WARPS * 32) {
+    const int r = idx / C::D, c = idx - r * C::D;
+    float M = -INFINITY, L = 0.f, O = 0.f;
+    if (!empty) {
+#pragma unroll
+      for (int gi = 0; gi < C::GROUPS; ++gi) M = fmaxf(M, st_m[gi * kDecodeMaxRows + r]);
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int gi = 0; gi < C::GROUPS; ++gi) {
+          const float mg = st_m[gi * kDecodeMaxRows + r];
+          const float f = mg == -INFINITY ? 0.f : ex2_approx(mg - M);
+          L = fmaf(f, st_l[gi * kDecodeMaxRows + r], L);
+          O = fmaf(f, st_o[((size_t)gi * kDecodeMaxRows + r) * C::D + c], O);
+        }
+      }
+    }
+    const size_t slot = ((size_t)bh * dp.f.n_q + r) * dp.splits + split;
+    dp.ws_o[slot * C::D + c] = O;
+    if (c == 0) {
+      dp.ws_ml[slot * 2] = M;
+      dp.ws_ml[slot * 2 + 1] = L;
+    }
+  }
+}
+
+// Eight query rows keep 8 x 8 elements of q and O~ per lane in registers:
+// that instantiation runs one CTA per SM with the whole register file.
+template <int D, bool BF16, int NQ>
+__global__ void __launch_bounds__(DecodeConfig<D>::THREADS, NQ >= 8 ? 1 : 2)
+    fa2_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                      const DecodeParams dp) {
+  using C = DecodeConfig<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((128u - (raw_addr & 127u)) & 127u);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC);
+  const int warp = (int)(threadIdx.x >> 5);
+  const int lane = (int)(threadIdx.x & 31);
+  const KernelParams& p = dp.f;
+
+  const int bh = (int)blockIdx.x / dp.splits;
+  const int split = (int)blockIdx.x - bh * dp.splits;
+  SeqInfo seq;
+  if (!seq_info(p, bh, seq)) return;
+  if (seq.n_k > dp.splits * dp.chunk) {   // a packed sequence longer than the split plan covers
+    if (threadIdx.x == 0 && split == 0) atomicOr(p.status, kStatusBadSeqlens);
+    return;
+  }
+  const int n_q = seq.n_q;
+  if (n_q == 0) return;
+  const KeyMask km = key_mask(p, seq);
+  int c0 = 0, c1 = 0;
+  const bool empty = !decode_range(km, n_q, split, dp.chunk, c0, c1);
+  const int nblk = empty ? 0 : (c1 - c0 + C::BLOCK - 1) / C::BLOCK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar0 + 8u * (DC_FULL + s), 1);
+      mbar_init(bar0 + 8u * (DC_EMPTY + s), C::WARPS);
+    }
+    mbar_init(bar0 + 8u * DC_DONE, C::WARPS);
+    mbar_init(bar0 + 8u * DC_MERGED, C::WARPS);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::TMA_WARP && lane == 0) {
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  __syncthreads();
+
+  float* st_o = reinterpret_cast<float*>(smem);
+  float* st_m = reinterpret_cast<float*>(smem + C::MERGE_O_BYTES);
+  float* st_l = st_m + C::GROUPS * kDecodeMaxRows;
+
+  if (warp == C::TMA_WARP) {
+    if (lane == 0) {
+      const int hb = seq.b * p.heads + seq.h;
+      const bool merged = p.merged_bh != 0;
+      int last_use[C::STAGES];
+      for (int s = 0; s < C::STAGES; ++s) last_use[s] = -1;
+      for (int b = 0; b < nblk; ++b) {
+        const int s = b % C::STAGES;
+        const int w = b / C::STAGES;
+        if (w > 0 &&
+            !wait_or_abort(bar0 + 8u * (DC_EMPTY + s), (uint32_t)(w - 1) & 1, abort_flag, p.status, kSiteProducerEmpty))
+          break;
+        const int row = seq.row0_k + c0 + b * C::BLOCK;
+        mbar_arrive_expect_tx(bar0 + 8u * (DC_FULL + s), 2 * C::TILE_BYTES);
+        tma_load_rows(sbase + C::OFF_K + s * C::TILE_BYTES, &tm_k, merged, 0, row, seq.h, seq.b, hb,
+                      bar0 + 8u * (DC_FULL + s));
+        tma_load_rows(sbase + C::OFF_V + s * C::TILE_BYTES, &tm_v, merged, 0, row, seq.h, seq.b, hb,
+                      bar0 + 8u * (DC_FULL + s));
+        last_use[s] = w;
+      }
+      for (int s = 0; s < C::STAGES; ++s)
+        if (last_use[s] >= 0) wait_drain(bar0 + 8u * (DC_FULL + s), (uint32_t)last_use[s] & 1, p.status);
+    }
+    return;   // the producer takes no part in the merge (no block-wide barrier follows)
+  }
+  dc_compute<NQ, C, BF16>(dp, seq, km, n_q, c0, c1, sbase, bar0, abort_flag, warp, lane, st_m, st_l, st_o);
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar0 + 8u * DC_MERGED);
+  bool ok = wait_or_abort(bar0 + 8u * DC_MERGED, 0, abort_flag, p.status, kSiteDecodeMerge);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok || *abort_flag) return;
+  dc_write_partial<C>(dp, bh, split, n_q, st_m, st_l, st_o, empty, (int)threadIdx.x);
+}
+
+// One block per (b*h, query row): merge the row's partials, store O and LSE.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(128)
+    fa2_decode_merge_kernel(const DecodeParams dp) {
+  const KernelParams& p = dp.f;
+  const int bh = (int)blockIdx.x / p.n_q;
+  const int r = (int)blockIdx.x - bh * p.n_q;
+  SeqInfo seq;
+  if (!seq_info(p, bh, seq)) return;   // the decode kernel has already reported it
+  if (r >= seq.n_q || seq.n_k > dp.splits * dp.chunk) return;
+  const size_t slot0 = ((size_t)bh * p.n_q + r) * dp.splits;
+  float M = -INFINITY;
+  for (int s = 0; s < dp.splits; ++s) M = fmaxf(M, dp.ws_ml[(slot0 + s) * 2]);
+  float L = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < dp.splits; ++s) {
+      const float ms = dp.ws_ml[(slot0 + s) * 2];
+      if (ms != -INFINITY) L = fmaf(ex2_approx(ms - M), dp.ws_ml[(slot0 + s) * 2 + 1], L);
+    }
+  }
+  const bool empty = !(L > 0.f);
+  const float inv_l = empty ? 0.f : 1.f / L;
+  uint8_t* o_row = reinterpret_cast<uint8_t*>(p.o) +
+                   2 * ((long long)seq.b * p.o_bs + (long long)seq.h * p.o_hs + (long long)(seq.row0_q + r) * p.o_rs);
+  for (int c = 2 * (int)threadIdx.x; c < D; c += 2 * (int)blockDim.x) {
+    float a0 = 0.f, a1 = 0.f;
+    if (!empty) {
+      for (int s = 0; s < dp.splits; ++s) {
+        const float ms = dp.ws_ml[(slot0 + s) * 2];
+        if (ms == -INFINITY) continue;
+        const float f = ex2_approx(ms - M);
+        const float2 v = *reinterpret_cast<const float2*>(dp.ws_o + (slot0 + s) * D + c);
+        a0 = fmaf(f, v.x, a0);
+        a1 = fmaf(f, v.y, a1);
+      }
+    }
+    *reinterpret_cast<uint32_t*>(o_row + 2 * c) = empty ? 0u : pack2<BF16>(a0 * inv_l, a1 * inv_l);
+  }
+  if (threadIdx.x == 0)
+    p.lse[(long long)seq.b * p.l_bs + (long long)seq.h * p.l_hs + seq.row0_q + r] =
+        empty ? -INFINITY : (M + log2f(L)) * 0.6931471805599453f;
+}
+
+template <int D, bool BF16, int NQ>
+int launch_decode_nq(const DecodeLaunchArgs& a) {
+  using C = DecodeConfig<D>;
+  auto kern = fa2_decode_kernel<D, BF16, NQ>;
+  static std::atomic<unsigned long long> configured{0};
+  const int e = once_per_device(configured, [&]() -> int {
+    return (int)cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
+  });
+  if (e != 0) return e;
+  const long long blocks = (long long)a.p.f.bh * a.p.splits;
+  kern<<<(unsigned)blocks, C::THREADS, C::SMEM_BYTES, a.stream>>>(a.tm_k, a.tm_v, a.p);
+  cudaError_t r = cudaGetLastError();
+  if (r != cudaSuccess) return (int)r;
+  fa2_decode_merge_kernel<D, BF16><<<(unsigned)((long long)a.p.f.bh * a.p.f.n_q), 128, 0, a.stream>>>(a.p);
+  return (int)cudaGetLastError();
+}
+
+template <int D, bool BF16>
+int launch_decode_dtype(const DecodeLaunchArgs& a) {
+  const int n = a.p.f.n_q;
+  if (n <= 1) return launch_decode_nq<D, BF16, 1>(a);
+  if (n <= 2) return launch_decode_nq<D, BF16, 2>(a);
+  if (n <= 4) return launch_decode_nq<D, BF16, 4>(a);
+  return launch_decode_nq<D, BF16, 8>(a);
+}
+
+template <int D>
+int launch_decode_dispatch(const DecodeLaunchArgs& a) {
+  return a.bf16 ? launch_decode_dtype<D, true>(a) : launch_decode_dtype<D, false>(a);
+}
+
+}  // namespace fa2

@@ -94,6 +94,10 @@ struct TileGeometry {
 
 TileGeometry tile_geometry(int d);
 
+// Key rows per pipeline stage of the decode kernel (the box height of its
+// K/V tensor maps).
+constexpr int decode_block_rows(int d) { return d == 256 ? 32 : 64; }
+
 // One-time per-device set-up of a kernel instantiation (attributes, checks):
 // `setup` runs until it succeeds once on a device; devices >= 64 run it on
 // every call.
@@ -112,5 +116,10 @@ inline int once_per_device(std::atomic<unsigned long long>& done, F&& setup) {
 int launch_fwd_d64(const LaunchArgs& a);
 int launch_fwd_d128(const LaunchArgs& a);
 int launch_fwd_d256(const LaunchArgs& a);
+
+struct DecodeLaunchArgs;
+int launch_decode_d64(const DecodeLaunchArgs& a);
+int launch_decode_d128(const DecodeLaunchArgs& a);
+int launch_decode_d256(const DecodeLaunchArgs& a);
 
 }  // namespace fa2

@@ -150,6 +150,24 @@ class Workload:
         return make_qkv(self.B, self.H, self.N, self.d, self.dtype, self.seed(run), self.q_scale)
 
 
+def visible_keys(Nq: int, Nk: int, window_left: int = -1, window_right: int = -1, prefix: int = 0) -> np.ndarray:
+    """Keys each query row sees under the band / prefix mask (int64 [Nq]).
+
+    Query i is aligned with key i + Nk - Nq and sees key j < Nk iff j < prefix
+    or i + off - window_left <= j <= i + off + window_right (-1 = unbounded):
+    the count is |[0, prefix) U [lo_i, hi_i]| clipped to [0, Nk).  Used to
+    count algorithmic FLOPs (4 d per visible key) of masked problems.
+    """
+    i = np.arange(Nq, dtype=np.int64)
+    off = Nk - Nq
+    lo = np.zeros(Nq, np.int64) if window_left < 0 else np.clip(i + off - window_left, 0, Nk)
+    hi = np.full(Nq, Nk - 1, np.int64) if window_right < 0 else np.clip(i + off + window_right, -1, Nk - 1)
+    band = np.maximum(hi - lo + 1, 0)
+    pre = min(max(prefix, 0), Nk)
+    overlap = np.where(band > 0, np.maximum(np.minimum(hi + 1, pre) - lo, 0), 0)
+    return band + pre - overlap
+
+
 # The five synthetic workloads: a tiny single-tile case, a short-sequence d=64
 # batch, a causal d=128 batch, the long-context causal batch-1 case, and a
 # ragged d=256 case with sharpened queries.

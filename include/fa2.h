@@ -157,6 +157,36 @@ size_t fa2_fwd_params_size(void);
  */
 int fa2_fwd_ex(const fa2_fwd_params* params, void* stream);
 
+/* Query rows per sequence fa2_decode takes. */
+#define FA2_DECODE_MAX_Q 8
+
+/*
+ * fa2_decode -- the forward pass for few query rows against many keys (the
+ * decoding regime: a new token, or up to FA2_DECODE_MAX_Q of them, attending
+ * to a long key/value cache).  Lesson 6.6 ("Common misconceptions") notes
+ * that single-row decoding needs its own kernel: with one query row there is
+ * no tile to fill a tensor core and the step is bound by reading K and V.
+ * The keys of each (batch, head) are split into chunks reduced by separate
+ * CTAs to online-softmax states (m, l, O~) that a second kernel merges with
+ * the rescaling step of the tiled loop (Lesson 6.6, "Online softmax").
+ *
+ * Arguments as fa2_fwd_ex (same struct, masks, strides and packed batches),
+ * with seqlen_q <= FA2_DECODE_MAX_Q (FA2_ERR_UNSUPPORTED otherwise; packed:
+ * every sequence's query count) and seqlen_k the key count (packed: the
+ * longest sequence's key count -- it sizes the split grid, which covers at
+ * least that many keys; a sequence with more keys than the grid covers is
+ * left unwritten and reported as FA2_ERR_DEVICE_SEQLENS).
+ * `workspace`: device, >= fa2_decode_workspace_bytes(params) bytes, 256-byte
+ * aligned, owned by the caller, overlapping no tensor; it holds fp32 partial
+ * states and is written before it is read.  Asynchronous on `stream`; two
+ * kernel launches.  Deterministic.
+ */
+int fa2_decode(const fa2_fwd_params* params, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace fa2_decode needs for these sizes (0 if they are invalid); it does
+ * not depend on the device. */
+size_t fa2_decode_workspace_bytes(const fa2_fwd_params* params);
+
 /*
  * fa2_fwd_host -- the same forward pass on HOST buffers, end to end.
  *

@@ -192,3 +192,46 @@ def test_ex_stride_of_size_one_dimension_is_ignored(lib):
 def test_ex_bnhd_output_overlap_detected(lib):
     # o as a [B, N, H, d] layout (row stride H*d, head stride d) reaching into lse
     assert _ex(lib, o_strides=[8192, 64, 128], lse=4 * A + 16000) == fa2.FA2_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- fa2_decode argument checks
+
+
+def _decode(lib, ws=9 * A, ws_bytes=1 << 20, **kw):
+    kw = dict(dict(seqlen_q=1), **kw)
+    return lib.fa2_decode(ctypes.byref(_params(**kw)), ws, ws_bytes, None)
+
+
+def test_decode_workspace_plan_is_device_independent(lib):
+    # B1 H32 N_k 16384 d128: 304 // 32 = 9 splits of ceil(16384 / 9) = 1821 -> 1856 keys (a multiple
+    # of the 64-key stage); 288 slots x (128 + 2) floats, each array 256-byte aligned
+    p = _params(batch=1, heads=32, seqlen_q=1, seqlen_k=16384, head_dim=128)
+    assert lib.fa2_decode_workspace_bytes(ctypes.byref(p)) == 288 * 128 * 4 + 2304
+    # more heads than two per SM: one split each; short caches: no split below 256 keys
+    p = _params(batch=4, heads=128, seqlen_q=2, seqlen_k=1000, head_dim=64)
+    assert lib.fa2_decode_workspace_bytes(ctypes.byref(p)) == 512 * 2 * 64 * 4 + 512 * 2 * 8
+    p = _params(batch=1, heads=2, seqlen_q=1, seqlen_k=600, head_dim=256)
+    slots = 2 * 3   # ceil(600 / 256) = 3 splits of 224 keys
+    assert lib.fa2_decode_workspace_bytes(ctypes.byref(p)) == (slots * 256 * 4 + 255) // 256 * 256 + 256
+    assert lib.fa2_decode_workspace_bytes(ctypes.byref(_params(seqlen_q=9))) == 0
+    assert lib.fa2_decode_workspace_bytes(None) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(seqlen_q=9), fa2.FA2_ERR_UNSUPPORTED),
+    (dict(seqlen_q=0), fa2.FA2_ERR_UNSUPPORTED),
+    (dict(head_dim=96), fa2.FA2_ERR_UNSUPPORTED),
+    (dict(ws=0), fa2.FA2_ERR_INVALID_ARG),
+    (dict(ws=9 * A + 128), fa2.FA2_ERR_MISALIGNED),
+    (dict(ws_bytes=100), fa2.FA2_ERR_INVALID_ARG),
+    (dict(window_left=-3), fa2.FA2_ERR_INVALID_ARG),
+    (dict(k_strides=[8192, 4096, 60]), fa2.FA2_ERR_MISALIGNED),
+    (dict(ws=4 * A), fa2.FA2_ERR_INVALID_ARG),                      # workspace over o
+    (dict(ws=A), fa2.FA2_ERR_INVALID_ARG),                          # workspace over q
+])
+def test_decode_bad_arguments_rejected(lib, kw, code):
+    assert _decode(lib, **kw) == code
+
+
+def test_decode_null_params(lib):
+    assert lib.fa2_decode(None, 9 * A, 1 << 20, None) == fa2.FA2_ERR_INVALID_ARG

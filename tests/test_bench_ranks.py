@@ -46,3 +46,33 @@ def test_single_process_defaults():
 
     assert bench.max_over_ranks(12.5) == 12.5
     assert bench.job_throughput(1e12, 5, 1, 1000.0) == pytest.approx(5.0)
+
+
+def test_general_options_parse_and_count():
+    """The general-forward bench options: mask defaults follow the workload,
+    packed lengths are seeded, positive and sum to the token count."""
+    sys.path.insert(0, ROOT)
+    import argparse
+
+    import numpy as np
+
+    import bench
+    from exact_tiled_attention_fa2_gb300 import synthetic as sy
+
+    w = sy.WORKLOADS[4]
+    ns = dict(window_left=None, window_right=None, prefix=0, seqlen_k=0, layout="bhnd", varlen_seqs=0, decode_rows=0)
+    assert bench.general_mask(argparse.Namespace(**ns), w) is None
+    g = bench.general_mask(argparse.Namespace(**dict(ns, window_left=4095)), w)
+    assert (g["window_left"], g["window_right"], g["seqlen_k"]) == (4095, 0, w.N)   # causal workload: right edge 0
+    g = bench.general_mask(argparse.Namespace(**dict(ns, seqlen_k=20000)), w)
+    assert g["seqlen_k"] == 20000 and "Nk20000" in g["label"]
+    lens = bench.varlen_lengths(1 << 16, 37, 5)
+    assert lens.sum() == 1 << 16 and lens.min() >= 1 and lens.size == 37
+    np.testing.assert_array_equal(lens, bench.varlen_lengths(1 << 16, 37, 5))
+    # a 4096-key window on a causal N=16384 problem: every row past the first 4095 sees 4096 keys
+    vis = sy.visible_keys(16384, 16384, 4095, 0, 0)
+    assert vis.sum() == sum(range(1, 4097)) + (16384 - 4096) * 4096
+    g = bench.general_mask(argparse.Namespace(**dict(ns, decode_rows=1)), w)
+    assert g["seqlen_q"] == 1 and g["seqlen_k"] == w.N and g["label"].startswith("decode 1 row vs 16384 keys")
+    # one causal row facing the last of N keys sees all of them: K + V read once dominate the bytes
+    assert g["input_bytes"] == (1 + 2 * w.N) * w.H * w.d * 2

@@ -1,5 +1,6 @@
 """The seeded input generator: deterministic, N(0,1)-distributed, correctly rounded."""
 import numpy as np
+import pytest
 import torch
 
 from exact_tiled_attention_fa2_gb300 import synthetic as sy
@@ -45,3 +46,17 @@ def test_q_scale_only_touches_q():
     np.testing.assert_array_equal(v1, v3)
     raw = sy.normals_f32(3, 0, 64)
     np.testing.assert_array_equal(q3.reshape(-1), sy.f32_to_bits(raw * np.float32(3.0), sy.FP16))
+
+
+@pytest.mark.parametrize("Nq,Nk,wl,wr,pre", [(7, 7, -1, -1, 0), (7, 7, -1, 0, 0), (5, 12, 2, 1, 0), (12, 5, -1, 0, 0),
+                                             (20, 20, 3, 0, 4), (20, 20, 0, 0, 25), (9, 30, 0, -1, 2)])
+def test_visible_keys_matches_brute_force(Nq, Nk, wl, wr, pre):
+    off = Nk - Nq
+    want = []
+    for i in range(Nq):
+        n = 0
+        for j in range(Nk):
+            band = (wl < 0 or j >= i + off - wl) and (wr < 0 or j <= i + off + wr)
+            n += (j < pre) or band
+        want.append(n)
+    np.testing.assert_array_equal(sy.visible_keys(Nq, Nk, wl, wr, pre), want)
