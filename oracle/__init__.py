@@ -72,6 +72,15 @@ def _load():
                                                      ctypes.c_double, i64, i64, i64, pi64, pi64, i64, pd, pd,
                                                      ctypes.c_int]
         lib.oracle_attention_rows_masked.restype = ctypes.c_int
+        lib.oracle_attention_fwd_masked_f64.argtypes = [pd, pd, pd, i64, i64, i64, i64, i64, ctypes.c_double, i64, i64,
+                                                        i64, pd, pd]
+        lib.oracle_attention_fwd_masked_f64.restype = ctypes.c_int
+        lib.oracle_attention_bwd_masked_f64.argtypes = [pd, pd, pd, pd, i64, i64, i64, i64, i64, ctypes.c_double, i64,
+                                                        i64, i64, pd, pd, pd, pd, ctypes.c_int]
+        lib.oracle_attention_bwd_masked_f64.restype = ctypes.c_int
+        lib.oracle_attention_bwd_masked.argtypes = [p16, p16, p16, p16, ctypes.c_int, i64, i64, i64, i64, i64,
+                                                    ctypes.c_double, i64, i64, i64, pd, pd, pd, pd, ctypes.c_int]
+        lib.oracle_attention_bwd_masked.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -238,3 +247,58 @@ def attention_rows_masked(q, k, v, dtype: int, scale: float, bh_idx, row_idx, wi
     if rc:
         raise ValueError("oracle_attention_rows_masked failed (%d)" % rc)
     return o, lse
+
+
+def attention_fwd_masked_f64(q, k, v, scale: float, window_left: int = -1, window_right: int = -1,
+                             prefix_len: int = 0):
+    """attention_fwd_masked on float64 inputs q [B,H,Nq,d], k, v [B,H,Nk,d]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    o = np.empty((B, H, Nq, d))
+    lse = np.empty((B, H, Nq))
+    rc = _load().oracle_attention_fwd_masked_f64(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
+                                                 _ptr(v, ctypes.c_double), B, H, Nq, Nk, d, float(scale),
+                                                 int(window_left), int(window_right), int(prefix_len),
+                                                 _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double))
+    if rc:
+        raise ValueError("oracle_attention_fwd_masked_f64 failed (%d)" % rc)
+    return o, lse
+
+
+def _bwd_masked_out(B, H, Nq, Nk, d):
+    return (np.empty((B, H, Nq, d)), np.empty((B, H, Nk, d)), np.empty((B, H, Nk, d)), np.empty((B, H, Nq)))
+
+
+def attention_bwd_masked_f64(q, k, v, dout, scale: float, window_left: int = -1, window_right: int = -1,
+                             prefix_len: int = 0, threads: int = 0):
+    """Gradients (dQ, dK, dV, D) of the masked forward for upstream dout, float64 inputs."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    dq, dk, dv, delta = _bwd_masked_out(B, H, Nq, Nk, d)
+    rc = _load().oracle_attention_bwd_masked_f64(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
+                                                 _ptr(v, ctypes.c_double), _ptr(dout, ctypes.c_double), B, H, Nq, Nk,
+                                                 d, float(scale), int(window_left), int(window_right),
+                                                 int(prefix_len), _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double),
+                                                 _ptr(dv, ctypes.c_double), _ptr(delta, ctypes.c_double), int(threads))
+    if rc:
+        raise ValueError("oracle_attention_bwd_masked_f64 failed (%d)" % rc)
+    return dq, dk, dv, delta
+
+
+def attention_bwd_masked(q, k, v, dout, dtype: int, scale: float, window_left: int = -1, window_right: int = -1,
+                         prefix_len: int = 0, threads: int = 0):
+    """Masked-backward gradients from 16-bit bit patterns (q, dout [B,H,Nq,d]; k, v [B,H,Nk,d]), float64."""
+    q, k, v, dout = _bits(q), _bits(k), _bits(v), _bits(dout)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    dq, dk, dv, delta = _bwd_masked_out(B, H, Nq, Nk, d)
+    rc = _load().oracle_attention_bwd_masked(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
+                                             _ptr(v, ctypes.c_uint16), _ptr(dout, ctypes.c_uint16), int(dtype), B, H,
+                                             Nq, Nk, d, float(scale), int(window_left), int(window_right),
+                                             int(prefix_len), _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double),
+                                             _ptr(dv, ctypes.c_double), _ptr(delta, ctypes.c_double), int(threads))
+    if rc:
+        raise ValueError("oracle_attention_bwd_masked failed (%d)" % rc)
+    return dq, dk, dv, delta

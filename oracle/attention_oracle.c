@@ -534,6 +534,163 @@ int oracle_attention_rows_masked(const uint16_t* q, const uint16_t* k, const uin
   return nomem ? ORACLE_ERR_NOMEM : ORACLE_OK;
 }
 
+/* ------------------------------------------------------------------ masked backward */
+
+/*
+ * Gradients of the masked forward above (FlashAttention V2 in depth,
+ * section 7: P = softmax over the visible keys, dV = P^T dO, dP = dO V^T,
+ * D_i = rowsum(dO_i o O_i) = sum_j P_ij dP_ij, dS = P o (dP - D),
+ * dQ = scale dS K, dK = scale dS^T Q), for one (b,h) slice of float64 data:
+ * q, dout [Nq,d], k, v [Nk,d].  Hidden pairs contribute nothing; a row that
+ * sees no key has dQ = 0 and D = 0; a key no row sees has dK = dV = 0.
+ */
+static int masked_bwd_slice(const double* q, const double* k, const double* v, const double* dout, int64_t Nq,
+                            int64_t Nk, int64_t d, double scale, int64_t wl, int64_t wr, int64_t prefix,
+                            double* dq, double* dk, double* dv, double* delta) {
+  const int64_t off = Nk - Nq;
+  double* m = (double*)malloc(sizeof(double) * (size_t)Nq);
+  double* l = (double*)malloc(sizeof(double) * (size_t)Nq);
+  if (!m || !l) { free(m); free(l); return ORACLE_ERR_NOMEM; }
+  int nomem = 0;
+  /* rows: m_i, l_i, D_i, dQ_i */
+#pragma omp parallel reduction(| : nomem)
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)Nk);
+    if (!s) {
+      nomem = 1;
+    } else {
+#pragma omp for schedule(dynamic, 4)
+      for (int64_t i = 0; i < Nq; ++i) {
+        const double* qi = q + i * d;
+        const double* doi = dout + i * d;
+        double mi = -INFINITY;
+        for (int64_t j = 0; j < Nk; ++j) {
+          if (!key_visible(i, j, off, wl, wr, prefix)) continue;
+          double acc = 0.0;
+          for (int64_t c = 0; c < d; ++c) acc += qi[c] * k[j * d + c];
+          s[j] = scale * acc;
+          if (s[j] > mi) mi = s[j];
+        }
+        for (int64_t c = 0; c < d; ++c) dq[i * d + c] = 0.0;
+        m[i] = mi;
+        l[i] = 0.0;
+        delta[i] = 0.0;
+        if (mi == -INFINITY) continue;
+        double li = 0.0;
+        for (int64_t j = 0; j < Nk; ++j)
+          if (key_visible(i, j, off, wl, wr, prefix)) li += exp(s[j] - mi);
+        double di = 0.0;
+        for (int64_t j = 0; j < Nk; ++j) {
+          if (!key_visible(i, j, off, wl, wr, prefix)) continue;
+          double dp = 0.0;
+          for (int64_t c = 0; c < d; ++c) dp += doi[c] * v[j * d + c];
+          di += exp(s[j] - mi) / li * dp;
+        }
+        for (int64_t j = 0; j < Nk; ++j) {
+          if (!key_visible(i, j, off, wl, wr, prefix)) continue;
+          double dp = 0.0;
+          for (int64_t c = 0; c < d; ++c) dp += doi[c] * v[j * d + c];
+          const double ds = exp(s[j] - mi) / li * (dp - di);
+          for (int64_t c = 0; c < d; ++c) dq[i * d + c] += scale * ds * k[j * d + c];
+        }
+        l[i] = li;
+        delta[i] = di;
+      }
+    }
+    free(s);
+  }
+  if (nomem) { free(m); free(l); return ORACLE_ERR_NOMEM; }
+  /* keys: dK_j, dV_j over the rows that see key j */
+#pragma omp parallel for schedule(dynamic, 4)
+  for (int64_t j = 0; j < Nk; ++j) {
+    for (int64_t c = 0; c < d; ++c) { dk[j * d + c] = 0.0; dv[j * d + c] = 0.0; }
+    for (int64_t i = 0; i < Nq; ++i) {
+      if (!key_visible(i, j, off, wl, wr, prefix) || m[i] == -INFINITY) continue;
+      double sij = 0.0, dpij = 0.0;
+      for (int64_t c = 0; c < d; ++c) {
+        sij += q[i * d + c] * k[j * d + c];
+        dpij += dout[i * d + c] * v[j * d + c];
+      }
+      const double pij = exp(scale * sij - m[i]) / l[i];
+      const double ds = pij * (dpij - delta[i]);
+      for (int64_t c = 0; c < d; ++c) {
+        dv[j * d + c] += pij * dout[i * d + c];
+        dk[j * d + c] += scale * ds * q[i * d + c];
+      }
+    }
+  }
+  free(m);
+  free(l);
+  return ORACLE_OK;
+}
+
+static int masked_f64_args_ok(const double* q, const double* k, const double* v, int64_t B, int64_t H, int64_t Nq,
+                              int64_t Nk, int64_t d, double scale, int64_t prefix_len) {
+  if (!q || !k || !v) return 0;
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1 || !isfinite(scale) || prefix_len < 0) return 0;
+  return 1;
+}
+
+/* The masked forward on float64 inputs q [B,H,Nq,d], k, v [B,H,Nk,d]. */
+int oracle_attention_fwd_masked_f64(const double* q, const double* k, const double* v, int64_t B, int64_t H,
+                                    int64_t Nq, int64_t Nk, int64_t d, double scale, int64_t window_left,
+                                    int64_t window_right, int64_t prefix_len, double* o_out, double* lse_out) {
+  if (!masked_f64_args_ok(q, k, v, B, H, Nq, Nk, d, scale, prefix_len) || !o_out || !lse_out) return ORACLE_ERR_ARG;
+  double* srow = (double*)malloc(sizeof(double) * (size_t)Nk);
+  if (!srow) return ORACLE_ERR_NOMEM;
+  for (int64_t bh = 0; bh < B * H; ++bh)
+    for (int64_t i = 0; i < Nq; ++i)
+      masked_row(q + (bh * Nq + i) * d, k + bh * Nk * d, v + bh * Nk * d, i, Nq, Nk, d, scale, window_left,
+                 window_right, prefix_len, srow, o_out + (bh * Nq + i) * d, lse_out + bh * Nq + i);
+  free(srow);
+  return ORACLE_OK;
+}
+
+/* Masked backward on float64 inputs: dq, dout [B,H,Nq,d]; dk, dv [B,H,Nk,d]; delta [B,H,Nq]. */
+int oracle_attention_bwd_masked_f64(const double* q, const double* k, const double* v, const double* dout, int64_t B,
+                                    int64_t H, int64_t Nq, int64_t Nk, int64_t d, double scale, int64_t window_left,
+                                    int64_t window_right, int64_t prefix_len, double* dq, double* dk, double* dv,
+                                    double* delta, int threads) {
+  if (!masked_f64_args_ok(q, k, v, B, H, Nq, Nk, d, scale, prefix_len) || !dout || !dq || !dk || !dv || !delta)
+    return ORACLE_ERR_ARG;
+#ifdef _OPENMP
+  if (threads > 0) omp_set_num_threads(threads);
+#else
+  (void)threads;
+#endif
+  for (int64_t bh = 0; bh < B * H; ++bh) {
+    const int64_t oq = bh * Nq * d, ok = bh * Nk * d;
+    int rc = masked_bwd_slice(q + oq, k + ok, v + ok, dout + oq, Nq, Nk, d, scale, window_left, window_right,
+                              prefix_len, dq + oq, dk + ok, dv + ok, delta + bh * Nq);
+    if (rc) return rc;
+  }
+  return ORACLE_OK;
+}
+
+/* Masked backward on 16-bit inputs (widened exactly first). */
+int oracle_attention_bwd_masked(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout,
+                                int dtype, int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, double scale,
+                                int64_t window_left, int64_t window_right, int64_t prefix_len, double* dq,
+                                double* dk, double* dv, double* delta, int threads) {
+  if (!masked_args_ok(q, k, v, dtype, B, H, Nq, Nk, d, scale, prefix_len) || !dout) return ORACLE_ERR_ARG;
+  const int64_t nq = B * H * Nq * d, nk = B * H * Nk * d;
+  double* buf = (double*)malloc(sizeof(double) * (size_t)(2 * nq + 2 * nk));
+  if (!buf) return ORACLE_ERR_NOMEM;
+  double *bq = buf, *bdo = buf + nq, *bk = buf + 2 * nq, *bv = buf + 2 * nq + nk;
+  for (int64_t x = 0; x < nq; ++x) {
+    bq[x] = widen(q[x], dtype);
+    bdo[x] = widen(dout[x], dtype);
+  }
+  for (int64_t x = 0; x < nk; ++x) {
+    bk[x] = widen(k[x], dtype);
+    bv[x] = widen(v[x], dtype);
+  }
+  int rc = oracle_attention_bwd_masked_f64(bq, bk, bv, bdo, B, H, Nq, Nk, d, scale, window_left, window_right,
+                                           prefix_len, dq, dk, dv, delta, threads);
+  free(buf);
+  return rc;
+}
+
 /* Threads OpenMP will use (1 without OpenMP); reported by the CPU baseline. */
 int oracle_max_threads(void) {
 #ifdef _OPENMP
