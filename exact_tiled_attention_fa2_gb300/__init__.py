@@ -48,6 +48,16 @@ class Fa2FwdParams(ctypes.Structure):
     ]
 
 
+class Fa2BwdParams(ctypes.Structure):
+    """Mirror of ``fa2_bwd_params`` in include/fa2.h."""
+
+    _fields_ = [
+        ("fwd", Fa2FwdParams),
+        ("dout", ctypes.c_void_p), ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
 class Fa2Error(RuntimeError):
     """A nonzero fa2_status returned through the C ABI."""
 
@@ -94,6 +104,10 @@ def load_library():
     lib.fa2_decode.restype = ci
     lib.fa2_decode_workspace_bytes.argtypes = [ctypes.POINTER(Fa2FwdParams)]
     lib.fa2_decode_workspace_bytes.restype = sz
+    lib.fa2_bwd_ex.argtypes = [ctypes.POINTER(Fa2BwdParams), vp]
+    lib.fa2_bwd_ex.restype = ci
+    lib.fa2_bwd_ex_workspace_bytes.argtypes = [ctypes.POINTER(Fa2FwdParams)]
+    lib.fa2_bwd_ex_workspace_bytes.restype = sz
     if lib.fa2_fwd_params_size() != ctypes.sizeof(Fa2FwdParams):
         raise RuntimeError("fa2_fwd_params layout mismatch: library %d bytes, binding %d bytes"
                            % (lib.fa2_fwd_params_size(), ctypes.sizeof(Fa2FwdParams)))
@@ -298,6 +312,41 @@ def fa2_bwd(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, workspace=None, sc
                                  int(bool(causal)), _dtype_code(q), _stream_handle(stream, q.device))
     if rc:
         raise Fa2Error(rc, "fa2_bwd")
+    return dq, dk, dv
+
+
+def fa2_bwd_ex(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, workspace=None, scale=None, window_left=-1,
+               window_right=-1, prefix_len=0, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None,
+               max_seqlen_k=None, stream=None):
+    """Gradients (dq, dk, dv) of fa2_fwd_ex (same tensors and options; o, lse its outputs).
+
+    dout has o's layout; dq, dk, dv default to new tensors shaped like q, k,
+    v (contiguous) and may be views.  Packed batches take ``max_seqlen_k``
+    (default: total_k), the longest sequence's key count.  head dim 64 or 128.
+    """
+    import torch
+    p = Fa2BwdParams()
+    fp, _, _ = _general_params(q, k, v, o, lse, scale, window_left, window_right, prefix_len, cu_seqlens_q,
+                               cu_seqlens_k, max_seqlen_q, max_seqlen_k)
+    p.fwd = fp
+    if dout.shape != o.shape or dout.stride() != o.stride() or dout.dtype != o.dtype:
+        raise ValueError("dout must have o's shape, strides and dtype")
+    like = lambda t: torch.empty_strided(t.shape, t.stride(), dtype=t.dtype, device=t.device)
+    dq = like(q) if dq is None else dq
+    dk = like(k) if dk is None else dk
+    dv = like(v) if dv is None else dv
+    for g, t, name in ((dq, q, "dq"), (dk, k, "dk"), (dv, v, "dv")):
+        if g.shape != t.shape or g.stride() != t.stride() or g.dtype != t.dtype:
+            raise ValueError("%s must have the shape, strides and dtype of its primal tensor" % name)
+    lib = load_library()
+    if workspace is None:
+        workspace = torch.empty(max(int(lib.fa2_bwd_ex_workspace_bytes(ctypes.byref(fp))), 256), dtype=torch.uint8,
+                                device=q.device)
+    p.dout, p.dq, p.dk, p.dv = dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr()
+    p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    rc = lib.fa2_bwd_ex(ctypes.byref(p), _stream_handle(stream, q.device))
+    if rc:
+        raise Fa2Error(rc, "fa2_bwd_ex")
     return dq, dk, dv
 
 

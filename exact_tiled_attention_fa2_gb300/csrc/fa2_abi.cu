@@ -185,20 +185,6 @@ int encode_map(CUtensorMap* m, const void* base, int bh, int n, int d, int rows,
   return r == CUDA_SUCCESS ? FA2_OK : FA2_ERR_CUDA;
 }
 
-// fp32 [B*H, N, d] view of the dQ accumulator; boxes of 32 columns x 32 rows
-// (one warp's rows and a 128-byte column block), 128-byte swizzle, for TMA
-// reduce-add.  Rows past N are clipped.
-int encode_dq_map(CUtensorMap* m, void* base, int bh, int n, int d) {
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)n * (cuuint64_t)d * 4};
-  cuuint32_t box[3] = {32, 32, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? FA2_OK : FA2_ERR_CUDA;
-}
-
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
   uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + nb && y < x + na;
@@ -769,6 +755,150 @@ __global__ void selftest_wait_timeout_kernel(uint32_t* status, uint64_t limit_ns
 
 }  // namespace fa2
 
+namespace fa2 {
+namespace {
+
+// fp32 (d, rows, B*H) view of the dQ accumulator; boxes of 32 columns x 32
+// rows (one warp's rows and a 128-byte column block), 128-byte swizzle, for
+// TMA reduce-add.  Rows past `rows` are clipped.
+int encode_dq_accum_map(CUtensorMap* m, void* base, long long slices, long long rows, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)slices};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)rows * (cuuint64_t)d * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA2_OK : FA2_ERR_CUDA;
+}
+
+struct BwdPlan {
+  long long slices, rows_q;   // (tensor batch x heads) slices and query rows per slice
+  int num_k_tiles;
+  size_t accum_bytes, delta_bytes;
+};
+
+int bwd_plan(const fa2_fwd_params& a, BwdPlan& out) {
+  if (a.head_dim != 64 && a.head_dim != 128) return FA2_ERR_UNSUPPORTED;
+  if (a.batch < 1 || a.heads < 1 || a.seqlen_q < 1 || a.seqlen_k < 1) return FA2_ERR_INVALID_ARG;
+  const bool packed = a.cu_seqlens_q != nullptr;
+  if (packed && a.total_q < 1) return FA2_ERR_INVALID_ARG;
+  out.slices = (long long)(packed ? 1 : a.batch) * a.heads;
+  out.rows_q = packed ? a.total_q : a.seqlen_q;
+  const long long tiles = ((long long)a.seqlen_k + 127) / 128;
+  if ((long long)a.batch * a.heads * tiles > INT_MAX) return FA2_ERR_UNSUPPORTED;
+  out.num_k_tiles = (int)tiles;
+  const size_t rows = (size_t)out.slices * (size_t)out.rows_q;
+  out.accum_bytes = align256(rows * (size_t)a.head_dim * 4);
+  out.delta_bytes = align256(rows * 4);
+  return FA2_OK;
+}
+
+int backward(const fa2_bwd_params& bp, cudaStream_t stream) {
+  fa2_bwd_params b = bp;
+  b.fwd = fold_batches(bp.fwd);
+  const fa2_fwd_params& a = b.fwd;
+  BwdPlan plan;
+  int rc = bwd_plan(a, plan);
+  if (rc) return rc;
+  if (!b.dout || !b.dq || !b.dk || !b.dv || !b.workspace) return FA2_ERR_INVALID_ARG;
+  if (misaligned(b.dout) || misaligned(b.dq) || misaligned(b.dk) || misaligned(b.dv)) return FA2_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(b.workspace) & 255u) return FA2_ERR_MISALIGNED;
+  if (b.workspace_bytes < plan.accum_bytes + plan.delta_bytes) return FA2_ERR_INVALID_ARG;
+  // byte ranges: every written buffer overlaps no input and no other output
+  const bool packed = a.cu_seqlens_q != nullptr || a.cu_seqlens_k != nullptr;
+  const long long tb = packed ? 1 : a.batch;
+  const long long dq_dims[3] = {tb, a.heads, packed ? a.total_q : a.seqlen_q};
+  const long long dk_dims[3] = {tb, a.heads, packed ? a.total_k : a.seqlen_k};
+  long long st[4][3];
+  const int64_t* src[4] = {a.q_strides, a.k_strides, a.v_strides, a.o_strides};
+  for (int t = 0; t < 4; ++t)
+    for (int i = 0; i < 3; ++i) st[t][i] = (long long)src[t][i];
+  for (int i = 0; i < 3; ++i) {   // the stride checks prepare() repeats, needed here for the extents
+    if (check_stride(dq_dims[i], st[0][i], true) || check_stride(dk_dims[i], st[1][i], true) ||
+        check_stride(dk_dims[i], st[2][i], true) || check_stride(dq_dims[i], st[3][i], true))
+      return FA2_ERR_INVALID_ARG;
+  }
+  const long long l_st[3] = {packed ? 0 : (long long)a.lse_strides[0], (long long)a.lse_strides[1], 1};
+  const int d = a.head_dim;
+  const Extent outs[4] = {extent(b.dq, dq_dims, st[0], d, 2), extent(b.dk, dk_dims, st[1], d, 2),
+                          extent(b.dv, dk_dims, st[2], d, 2),
+                          Extent{b.workspace, plan.accum_bytes + plan.delta_bytes}};
+  const Extent ins[6] = {extent(a.q, dq_dims, st[0], d, 2),   extent(a.k, dk_dims, st[1], d, 2),
+                         extent(a.v, dk_dims, st[2], d, 2),   extent(a.o, dq_dims, st[3], d, 2),
+                         extent(a.lse, dq_dims, l_st, 1, 4), extent(b.dout, dq_dims, st[3], d, 2)};
+  for (int i = 0; i < 4; ++i) {
+    for (const Extent& in : ins)
+      if (overlap(outs[i], in)) return FA2_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 4; ++j)
+      if (overlap(outs[i], outs[j])) return FA2_ERR_INVALID_ARG;
+  }
+  Prepared pr;
+  rc = prepare(a, 128, pr);
+  if (rc) return rc;
+  // one map rank for every tensor the kernel loads: merge (batch, head) only
+  // when q, k, v and dout all allow it
+  if (!mergeable(a.heads, tb, st[3])) {
+    pr.key.merged = 0;
+    pr.p.merged_bh = 0;
+  }
+  BwdLaunchArgs la;
+  std::memset(&la, 0, sizeof(la));
+  LaunchArgs fl;
+  std::memset(&fl, 0, sizeof(fl));
+  rc = cached_maps(fl, pr.key);
+  if (rc) return rc;
+  la.tm_q = fl.tm_q;
+  la.tm_k = fl.tm_k;
+  la.tm_v = fl.tm_v;
+  const bool bf16 = a.dtype == FA2_BF16;
+  if (encode_map_rows(&la.tm_do, b.dout, d, dq_dims[2], a.heads, tb, st[3], 128, bf16, pr.key.merged != 0))
+    return FA2_ERR_CUDA;
+  uint8_t* w = static_cast<uint8_t*>(b.workspace);
+  if (encode_dq_accum_map(&la.tm_dq, w, plan.slices, plan.rows_q, d)) return FA2_ERR_CUDA;
+  BwdParams& p = la.p;
+  p.f = pr.p;
+  p.f.n_k = a.seqlen_k;   // packed: the longest sequence's key count the grid covers
+  p.q = a.q;
+  p.dout = b.dout;
+  p.dq = b.dq;
+  p.dk = b.dk;
+  p.dv = b.dv;
+  p.dq_accum = reinterpret_cast<float*>(w);
+  p.delta = reinterpret_cast<float*>(w + plan.accum_bytes);
+  p.q_bs = packed ? 0 : st[0][0];
+  p.q_hs = st[0][1];
+  p.q_rs = st[0][2];
+  p.k_bs = packed ? 0 : st[1][0];
+  p.k_hs = st[1][1];
+  p.k_rs = st[1][2];
+  p.v_bs = packed ? 0 : st[2][0];
+  p.v_hs = st[2][1];
+  p.v_rs = st[2][2];
+  p.slices = plan.slices;
+  p.num_k_tiles = plan.num_k_tiles;
+  p.scale = a.scale;
+  la.bf16 = bf16;
+  la.stream = stream;
+  const int e = (d == 64) ? launch_bwd_d64(la) : launch_bwd_d128(la);
+  return e == 0 ? FA2_OK : FA2_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace fa2
+
+extern "C" size_t fa2_bwd_ex_workspace_bytes(const fa2_fwd_params* fwd) {
+  if (!fwd) return 0;
+  BwdPlan plan;
+  if (bwd_plan(fold_batches(*fwd), plan)) return 0;
+  return plan.accum_bytes + plan.delta_bytes;
+}
+
+extern "C" int fa2_bwd_ex(const fa2_bwd_params* params, void* stream) {
+  if (!params) return FA2_ERR_INVALID_ARG;
+  return backward(*params, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" size_t fa2_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
   const size_t rows = (size_t)B * H * (size_t)N;
@@ -781,57 +911,44 @@ extern "C" int fa2_bwd(const void* q, const void* k, const void* v, const void* 
   int rc = check_shape(B, H, N, d, scale, causal, dtype);
   if (rc) return rc;
   if (d != 64 && d != 128) return FA2_ERR_UNSUPPORTED;
-  const void* ptrs[11] = {q, k, v, o, lse, dout, dq, dk, dv, workspace, nullptr};
-  for (int i = 0; i < 10; ++i)
-    if (!ptrs[i]) return FA2_ERR_INVALID_ARG;
-  for (int i = 0; i < 10; ++i)
-    if (misaligned(ptrs[i])) return FA2_ERR_MISALIGNED;
-  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA2_ERR_MISALIGNED;
-  if (workspace_bytes < fa2_bwd_workspace_bytes(B, H, N, d)) return FA2_ERR_INVALID_ARG;
-  const size_t rows = (size_t)B * H * (size_t)N;
-  const size_t tb = rows * (size_t)d * 2, lb = rows * 4, wb = fa2_bwd_workspace_bytes(B, H, N, d);
-  // every written buffer (dq, dk, dv, workspace) overlaps no input and no other output
-  const void* outs[4] = {dq, dk, dv, workspace};
-  const size_t out_bytes[4] = {tb, tb, tb, wb};
-  const void* ins[6] = {q, k, v, o, lse, dout};
-  const size_t in_bytes[6] = {tb, tb, tb, tb, lb, tb};
-  for (int a = 0; a < 4; ++a) {
-    for (int b = 0; b < 6; ++b)
-      if (ranges_overlap(outs[a], out_bytes[a], ins[b], in_bytes[b])) return FA2_ERR_INVALID_ARG;
-    for (int b = a + 1; b < 4; ++b)
-      if (ranges_overlap(outs[a], out_bytes[a], outs[b], out_bytes[b])) return FA2_ERR_INVALID_ARG;
+  const void* ptrs[10] = {q, k, v, o, lse, dout, dq, dk, dv, workspace};
+  for (const void* ptr : ptrs)
+    if (!ptr) return FA2_ERR_INVALID_ARG;
+  for (const void* ptr : ptrs)
+    if (misaligned(ptr)) return FA2_ERR_MISALIGNED;
+  fa2_bwd_params b;
+  std::memset(&b, 0, sizeof(b));
+  fa2_fwd_params& a = b.fwd;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = const_cast<void*>(o);
+  a.lse = const_cast<float*>(lse);
+  a.batch = B;
+  a.heads = H;
+  a.seqlen_q = N;
+  a.seqlen_k = N;
+  a.head_dim = d;
+  a.dtype = dtype;
+  a.scale = scale;
+  a.window_left = -1;
+  a.window_right = causal ? 0 : -1;
+  const long long row = d, head = (long long)N * d, batch = (long long)H * N * d;
+  int64_t* st[4] = {a.q_strides, a.k_strides, a.v_strides, a.o_strides};
+  for (int64_t* s : st) {
+    s[0] = batch;
+    s[1] = head;
+    s[2] = row;
   }
-  DeviceState* ds = nullptr;
-  rc = device_state(&ds);
-  if (rc) return rc;
-  const bool bf16 = dtype == FA2_BF16;
-  const int bh = B * H;
-  BwdLaunchArgs a;
-  std::memset(&a, 0, sizeof(a));
-  if (encode_map(&a.tm_q, q, bh, N, d, 128, bf16) || encode_map(&a.tm_k, k, bh, N, d, 128, bf16) ||
-      encode_map(&a.tm_v, v, bh, N, d, 128, bf16) || encode_map(&a.tm_do, dout, bh, N, d, 128, bf16))
-    return FA2_ERR_CUDA;
-  uint8_t* w = static_cast<uint8_t*>(workspace);
-  if (encode_dq_map(&a.tm_dq, w, bh, N, d)) return FA2_ERR_CUDA;
-  a.p.dq_accum = reinterpret_cast<float*>(w);
-  a.p.delta = reinterpret_cast<float*>(w + align256(rows * (size_t)d * 4));
-  a.p.lse = lse;
-  a.p.dk = dk;
-  a.p.dv = dv;
-  a.p.status = ds->status;
-  a.p.n = N;
-  a.p.bh = bh;
-  a.p.num_tiles = (N + 127) / 128;
-  a.p.scale = scale;
-  a.p.scale_log2 = scale * 1.4426950408889634f;
-  a.o = o;
-  a.dout = dout;
-  a.dq = dq;
-  a.bf16 = bf16;
-  a.causal = causal != 0;
-  a.stream = static_cast<cudaStream_t>(stream);
-  const int e = (d == 64) ? launch_bwd_d64(a) : launch_bwd_d128(a);
-  return e == 0 ? FA2_OK : FA2_ERR_CUDA;
+  a.lse_strides[0] = (long long)H * N;
+  a.lse_strides[1] = N;
+  b.dout = dout;
+  b.dq = dq;
+  b.dk = dk;
+  b.dv = dv;
+  b.workspace = workspace;
+  b.workspace_bytes = workspace_bytes;
+  return backward(b, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fa2_selftest_wait_timeout(int limit_us, void* stream) {

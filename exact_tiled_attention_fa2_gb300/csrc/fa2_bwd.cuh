@@ -33,6 +33,13 @@
 // dQ, dK, dV); warp 8 owns TMEM and issues every MMA; warp 9 drives TMA.
 // Every mbarrier wait is bounded (fa2_common.cuh), and each barrier is waited
 // phase by phase, never more than one phase away from its waiter.
+//
+// Masks, lengths and layouts are those of the forward pass (KeyMask): a key
+// tile visits only the query tiles whose rows see one of its keys -- both
+// band edges are non-decreasing in the row, so those rows form one interval
+// -- and in a tile some pair of which is hidden, a key row keeps the query
+// columns [clo, chi] it is seen by (P = 0 elsewhere).  A key tile no row
+// sees stores dK = dV = 0.
 #pragma once
 
 #include "fa2_fwd_pingpong.cuh"
@@ -86,17 +93,22 @@ struct BwdCtx {
   uint32_t bar0, sK, sV, sQ, sDO, sDS, tmem;
   volatile int* abort_flag;
   uint32_t* status;
-  int bh, n, j0, i0, niter;   // key tile start row, first query tile, number of query tiles
+  SeqInfo seq;
+  int hb;           // batch * H + head: the merged map coordinate and the workspace slice
+  bool merged;      // 3-D maps (batch and head merged) or 4-D
+  int j0;           // first key of the tile (within the sequence)
+  int i0, niter;    // first query tile visited and how many
   __device__ __forceinline__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
 };
 
 template <class C>
 __device__ __forceinline__ void bwd_producer(const BwdCtx& t, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                              const CUtensorMap* tm_v, const CUtensorMap* tm_do) {
+  const int h = t.seq.h, b = t.seq.b;
   mbar_arrive_expect_tx(t.bar(BB_KV), 2 * C::TILE_BYTES);
   for (int kb = 0; kb < C::D / 64; ++kb) {
-    tma_load_3d(t.sK + kb * (C::T * 128), tm_k, kb * 64, t.j0, t.bh, t.bar(BB_KV));
-    tma_load_3d(t.sV + kb * (C::T * 128), tm_v, kb * 64, t.j0, t.bh, t.bar(BB_KV));
+    tma_load_rows(t.sK + kb * (C::T * 128), tm_k, t.merged, kb * 64, t.seq.row0_k + t.j0, h, b, t.hb, t.bar(BB_KV));
+    tma_load_rows(t.sV + kb * (C::T * 128), tm_v, t.merged, kb * 64, t.seq.row0_k + t.j0, h, b, t.hb, t.bar(BB_KV));
   }
   int loaded = 0;
   for (int it = 0; it < t.niter; ++it) {
@@ -104,11 +116,13 @@ __device__ __forceinline__ void bwd_producer(const BwdCtx& t, const CUtensorMap*
     if (u > 0 && !wait_or_abort(t.bar(BB_QEMPTY + s), (uint32_t)(u - 1) & 1, t.abort_flag, t.status,
                                 kSiteProducerEmpty))
       break;
-    const int q0 = (t.i0 + it) * C::T;
+    const int row = t.seq.row0_q + (t.i0 + it) * C::T;
     mbar_arrive_expect_tx(t.bar(BB_Q + s), 2 * C::TILE_BYTES);
     for (int kb = 0; kb < C::D / 64; ++kb) {
-      tma_load_3d(t.sQ + s * C::TILE_BYTES + kb * (C::T * 128), tm_q, kb * 64, q0, t.bh, t.bar(BB_Q + s));
-      tma_load_3d(t.sDO + s * C::TILE_BYTES + kb * (C::T * 128), tm_do, kb * 64, q0, t.bh, t.bar(BB_Q + s));
+      tma_load_rows(t.sQ + s * C::TILE_BYTES + kb * (C::T * 128), tm_q, t.merged, kb * 64, row, h, b, t.hb,
+                    t.bar(BB_Q + s));
+      tma_load_rows(t.sDO + s * C::TILE_BYTES + kb * (C::T * 128), tm_do, t.merged, kb * 64, row, h, b, t.hb,
+                    t.bar(BB_Q + s));
     }
     loaded = it + 1;
   }
@@ -182,35 +196,86 @@ __device__ __forceinline__ void bwd_mma(const BwdCtx& t) {
   wait_drain(t.bar(BB_EXIT), 0, t.status);
 }
 
-template <class C, bool BF16, bool CAUSAL>
-__device__ __forceinline__ void bwd_elementwise(const BwdCtx& t, const BwdParams& p, uint8_t* smem, int warp,
-                                                int lane, const CUtensorMap* tm_dq) {
-  const int h = warp >> 2;                 // warpgroup: query columns [64h, 64h + 64)
+// Queries [lo, hi] (within the sequence, clipped to [0, n_q)) that see key
+// `key`; lo > hi when none does.
+__device__ __forceinline__ void queries_of_key(const KeyMask& km, int n_q, int key, int& lo, int& hi) {
+  if (key >= km.n_k) {
+    lo = 1;
+    hi = 0;
+    return;
+  }
+  long long a = 0, b = n_q - 1;
+  if (key >= km.pre_end) {
+    if (km.wr >= 0) a = max(a, (long long)key - km.off - km.wr);
+    if (km.wl >= 0) b = min(b, (long long)key - km.off + km.wl);
+  }
+  if (a > b) {
+    lo = 1;
+    hi = 0;
+    return;
+  }
+  lo = (int)a;
+  hi = (int)b;
+}
+
+// Query rows [lo, hi] that see some key of [j0, j1] (j0 < n_k <= ...): every
+// row when the tile starts inside the prefix, else the rows whose band meets
+// the tile, [j0 - off - wr, j1 - off + wl] clipped to [0, n_q); lo > hi when
+// there are none.
+__device__ __forceinline__ void queries_of_tile(const KeyMask& km, int n_q, int j0, int j1, int& lo, int& hi) {
+  long long a = 0, b = n_q - 1;
+  if (j0 >= km.pre_end) {
+    if (km.wr >= 0) a = max(a, (long long)j0 - km.off - km.wr);
+    if (km.wl >= 0) b = min(b, (long long)j1 - km.off + km.wl);
+  }
+  if (a > b) {
+    lo = 1;
+    hi = 0;
+    return;
+  }
+  lo = (int)a;
+  hi = (int)b;
+}
+
+template <class C, bool BF16>
+__device__ __forceinline__ void bwd_elementwise(const BwdCtx& t, const BwdParams& p, const KeyMask& km, uint8_t* smem,
+                                                int warp, int lane, const CUtensorMap* tm_dq) {
+  const KernelParams& f = p.f;
+  const int wg = warp >> 2;                // warpgroup: query columns [64 wg, 64 wg + 64)
   const int quad = warp & 3;
   const int r = quad * 32 + lane;          // TMEM lane: key row (S^T, dP^T, dK, dV) or query row (dQ_i)
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-  const uint32_t tS = t.tmem + lane_off + C::TMEM_S + 64 * h;
-  const uint32_t tDP = t.tmem + lane_off + C::TMEM_DP + 64 * h;
-  uint8_t* ds_row = smem + C::OFF_DS + h * (C::T * 128) + r * 128;     // this key's row of dS^T, block h
-  uint8_t* dq_stage = smem + C::OFF_DQ + warp * C::DQ_WARP_BYTES;         // this warp's dQ boxes
+  const uint32_t tS = t.tmem + lane_off + C::TMEM_S + 64 * wg;
+  const uint32_t tDP = t.tmem + lane_off + C::TMEM_DP + 64 * wg;
+  uint8_t* ds_row = smem + C::OFF_DS + wg * (C::T * 128) + r * 128;     // this key's row of dS^T, block wg
+  uint8_t* dq_stage = smem + C::OFF_DQ + warp * C::DQ_WARP_BYTES;          // this warp's dQ boxes
+  const int n_q = t.seq.n_q;
   const int key = t.j0 + r;
-  const float sl2 = p.scale_log2;
+  int key_qlo, key_qhi;                    // the queries this key row is seen by
+  queries_of_key(km, n_q, key, key_qlo, key_qhi);
+  // every (key, query) pair of a 128 x 64 block is visible iff the block's
+  // last key is seen from its first query on and its first key up to its last
+  int last_qlo, last_qhi, first_qlo, first_qhi;
+  queries_of_key(km, n_q, t.j0 + C::T - 1, last_qlo, last_qhi);
+  queries_of_key(km, n_q, t.j0, first_qlo, first_qhi);
+  const float sl2 = f.scale_log2;
   const float scale = p.scale;
+  const long long lse_base = (long long)t.seq.b * f.l_bs + (long long)t.seq.h * f.l_hs + t.seq.row0_q;
+  const long long d_base = (long long)t.hb * f.total_q + t.seq.row0_q;
   bool ok = true;
   for (int it = 0; it < t.niter; ++it) {
     const uint32_t ph = (uint32_t)it & 1;
-    const int q0 = (t.i0 + it) * C::T + 64 * h;   // first query of this warpgroup's columns
+    const int q0 = (t.i0 + it) * C::T + 64 * wg;   // first query of this warpgroup's columns
     // L (exp2 domain) and D of the 64 queries: lane c holds queries c and
     // c + 32, every lane takes each value by shuffle (warp-local, so no
     // barrier spans warps that might abandon the tile)
     float l_lo, l_hi, d_lo, d_hi;
     {
       const int qa = q0 + lane, qb = q0 + lane + 32;
-      const size_t base = (size_t)t.bh * t.n;
-      l_lo = (qa < t.n) ? p.lse[base + qa] * 1.4426950408889634f : INFINITY;
-      l_hi = (qb < t.n) ? p.lse[base + qb] * 1.4426950408889634f : INFINITY;
-      d_lo = (qa < t.n) ? p.delta[base + qa] : 0.f;
-      d_hi = (qb < t.n) ? p.delta[base + qb] : 0.f;
+      l_lo = (qa < n_q) ? f.lse[lse_base + qa] * 1.4426950408889634f : INFINITY;
+      l_hi = (qb < n_q) ? f.lse[lse_base + qb] * 1.4426950408889634f : INFINITY;
+      d_lo = (qa < n_q) ? p.delta[d_base + qa] : 0.f;
+      d_hi = (qb < n_q) ? p.delta[d_base + qb] : 0.f;
     }
 
     ok = wait_or_abort(t.bar(BB_S), ph, t.abort_flag, t.status, kSiteSoftmaxS);
@@ -222,14 +287,20 @@ __device__ __forceinline__ void bwd_elementwise(const BwdCtx& t, const BwdParams
     tmem_ld_32x32b_x32(tS + 32, sr + 32);
     tmem_ld_wait_x32(sr);
     tmem_ld_wait_x32(sr + 32);
-    // a key row sees query q when key < N, q < N and (causal) key <= q
-    const bool full = (t.j0 + C::T <= t.n) && (q0 + 64 <= t.n) && (!CAUSAL || t.j0 + C::T - 1 <= q0);
+    const bool full = last_qlo <= q0 && first_qhi >= q0 + 63 && last_qlo <= last_qhi && first_qlo <= first_qhi;
     float pv[64];
 #pragma unroll
     for (int c = 0; c < 64; ++c) {
       const float lq = __shfl_sync(0xffffffffu, c < 32 ? l_lo : l_hi, c & 31);
-      const float x = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lq));
-      pv[c] = (full || (key < t.n && (!CAUSAL || key <= q0 + c))) ? x : 0.f;   // q >= N: L = inf gives 0
+      pv[c] = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lq));
+    }
+    // hidden pairs (and rows without keys) give 0; a separate pass that only
+    // blocks some pair of which is hidden run
+    if (!full) {
+      const int clo = key_qlo - q0, chi = key_qhi - q0;   // visible columns of this key row
+#pragma unroll
+      for (int c = 0; c < 64; ++c)
+        if (!(c >= clo && c <= chi)) pv[c] = 0.f;
     }
     uint32_t pk[32];
 #pragma unroll
@@ -274,10 +345,12 @@ __device__ __forceinline__ void bwd_elementwise(const BwdCtx& t, const BwdParams
     // dQ_i rows: lane = query row of tile i; this warpgroup adds d/2 columns.
     // Copy them to registers and free the TMEM columns at once, then stage
     // them in this warp's shared-memory boxes (128-byte swizzle) and let TMA
-    // add the boxes to the fp32 accumulator asynchronously.
+    // add the boxes to the fp32 accumulator asynchronously.  Rows past the
+    // sequence add zeros (their dS columns are 0).
     uint32_t dq[C::D / 2];
 #pragma unroll
-    for (int c = 0; c < C::D / 2; c += 32) tmem_ld_32x32b_x32(t.tmem + lane_off + C::TMEM_DP + (C::D / 2) * h + c, dq + c);
+    for (int c = 0; c < C::D / 2; c += 32)
+      tmem_ld_32x32b_x32(t.tmem + lane_off + C::TMEM_DP + (C::D / 2) * wg + c, dq + c);
 #pragma unroll
     for (int c = 0; c < C::D / 2; c += 32) tmem_ld_wait_x32(dq + c);
     tc_fence_before();
@@ -296,36 +369,46 @@ __device__ __forceinline__ void bwd_elementwise(const BwdCtx& t, const BwdParams
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      const int y = (t.i0 + it) * C::T + quad * 32;   // rows past N are clipped by the reduce
+      const int y = t.seq.row0_q + (t.i0 + it) * C::T + quad * 32;   // rows past the tensor are clipped
 #pragma unroll
       for (int b = 0; b < C::D / 64; ++b)
-        tma_reduce_add_3d(tm_dq, smem_u32(dq_stage + b * 4096), (C::D / 2) * h + 32 * b, y, t.bh);
+        tma_reduce_add_3d(tm_dq, smem_u32(dq_stage + b * 4096), (C::D / 2) * wg + 32 * b, y, t.hb);
       bulk_commit_group();
     }
   }
   if (lane == 0) bulk_wait_all();   // this warp's reduce-adds performed before the CTA exits
   __syncwarp();
-  if (ok) {
+  if (ok && t.niter > 0) {
     ok = wait_or_abort(t.bar(BB_END), 0, t.abort_flag, t.status, kSiteDrain);
     ok = __all_sync(0xffffffffu, ok);
   }
   if (!ok) return;
   tc_fence_after();
-  // dV_j and dK_j rows (lane = key row): d/2 columns per warpgroup
-  const size_t row_off = ((size_t)t.bh * t.n + (size_t)key) * C::D + (C::D / 2) * h;
+  // dV_j and dK_j rows (lane = key row): d/2 columns per warpgroup; zero when
+  // no query row sees the tile
+  const long long col0 = (C::D / 2) * wg;
 #pragma unroll 1
   for (int which = 0; which < 2; ++which) {
-    const uint32_t base = t.tmem + lane_off + (which ? C::TMEM_DK : C::TMEM_DV) + (C::D / 2) * h;
-    uint8_t* out = reinterpret_cast<uint8_t*>(which ? p.dk : p.dv) + row_off * 2;
+    const uint32_t base = t.tmem + lane_off + (which ? C::TMEM_DK : C::TMEM_DV) + (C::D / 2) * wg;
+    uint8_t* out = reinterpret_cast<uint8_t*>(which ? p.dk : p.dv) +
+                   2 * (which ? (long long)t.seq.b * p.k_bs + (long long)t.seq.h * p.k_hs +
+                                    (long long)(t.seq.row0_k + key) * p.k_rs + col0
+                              : (long long)t.seq.b * p.v_bs + (long long)t.seq.h * p.v_hs +
+                                    (long long)(t.seq.row0_k + key) * p.v_rs + col0);
 #pragma unroll 1
     for (int c = 0; c < C::D / 2; c += 32) {
-      uint32_t o[32];
-      tmem_ld_32x32b_x32(base + c, o);
-      tmem_ld_wait_x32(o);
       uint32_t pk16[16];
+      if (t.niter > 0) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(base + c, o);
+        tmem_ld_wait_x32(o);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) pk16[i] = pack2<BF16>(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
-      if (key < t.n) {
+        for (int i = 0; i < 16; ++i) pk16[i] = pack2<BF16>(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk16[i] = 0u;
+      }
+      if (key < t.seq.n_k) {
         uint4* dst4 = reinterpret_cast<uint4*>(out + c * 2);
 #pragma unroll
         for (int i = 0; i < 4; ++i) dst4[i] = make_uint4(pk16[4 * i], pk16[4 * i + 1], pk16[4 * i + 2], pk16[4 * i + 3]);
@@ -334,7 +417,7 @@ __device__ __forceinline__ void bwd_elementwise(const BwdCtx& t, const BwdParams
   }
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16>
 __global__ void __launch_bounds__(384, 1)
     fa2_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -348,8 +431,32 @@ __global__ void __launch_bounds__(384, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   const int warp = (int)(threadIdx.x >> 5);
   const int lane = (int)(threadIdx.x & 31);
+  const KernelParams& f = p.f;
 
   BwdCtx t;
+  int bh, unit;
+  unit_of_block((int)blockIdx.x, f.bh, p.num_k_tiles, bh, unit);
+  // The whole CTA leaves together, before any set-up, when its sequence is
+  // malformed, has more keys than the grid covers, or ends before this tile.
+  if (!seq_info(f, bh, t.seq)) return;
+  if (t.seq.n_k > p.num_k_tiles * C::T) {
+    if (threadIdx.x == 0 && unit == 0) atomicOr(f.status, kStatusBadSeqlens);
+    return;
+  }
+  // the key tiles with the most query tiles (the first ones, under a causal
+  // mask) start first
+  const int jt = p.num_k_tiles - 1 - unit;
+  t.j0 = jt * C::T;
+  if (t.j0 >= t.seq.n_k) return;
+  const KeyMask km = key_mask(f, t.seq);
+  {
+    int r_lo, r_hi;
+    queries_of_tile(km, t.seq.n_q, t.j0, min(t.j0 + C::T, t.seq.n_k) - 1, r_lo, r_hi);
+    t.i0 = r_lo <= r_hi ? r_lo / C::T : 0;
+    t.niter = r_lo <= r_hi ? r_hi / C::T - t.i0 + 1 : 0;
+  }
+  t.hb = t.seq.b * f.heads + t.seq.h;
+  t.merged = f.merged_bh != 0;
   t.bar0 = sbase + C::OFF_BAR;
   t.sK = sbase + C::OFF_K;
   t.sV = sbase + C::OFF_V;
@@ -357,15 +464,7 @@ __global__ void __launch_bounds__(384, 1)
   t.sDO = sbase + C::OFF_DO;
   t.sDS = sbase + C::OFF_DS;
   t.abort_flag = abort_flag;
-  t.status = p.status;
-  t.n = p.n;
-  int unit;
-  unit_of_block((int)blockIdx.x, p.bh, p.num_tiles, t.bh, unit);
-  // the key tiles with the most query tiles (the first ones, when causal) start first
-  const int jt = p.num_tiles - 1 - unit;
-  t.j0 = jt * C::T;
-  t.i0 = CAUSAL ? jt : 0;
-  t.niter = p.num_tiles - t.i0;
+  t.status = f.status;
 
   if (threadIdx.x == 0) {
     mbar_init(t.bar(BB_KV), 1);
@@ -400,12 +499,12 @@ __global__ void __launch_bounds__(384, 1)
   t.tmem = *tmem_slot;
 
   if (warp == C::TMA_WARP) {
-    if (lane == 0) bwd_producer<C>(t, &tm_q, &tm_k, &tm_v, &tm_do);
+    if (lane == 0 && t.niter > 0) bwd_producer<C>(t, &tm_q, &tm_k, &tm_v, &tm_do);
   } else if (warp == C::MMA_WARP) {
-    if (lane == 0) bwd_mma<C, BF16>(t);
+    if (lane == 0 && t.niter > 0) bwd_mma<C, BF16>(t);
     __syncwarp();
   } else if (warp < 8) {
-    bwd_elementwise<C, BF16, CAUSAL>(t, p, smem, warp, lane, &tm_dq);
+    bwd_elementwise<C, BF16>(t, p, km, smem, warp, lane, &tm_dq);
   }
   tc_fence_before();
   __syncthreads();
@@ -415,78 +514,88 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-// D_i = rowsum(dO_i o O_i) in fp32, and the row's fp32 dQ accumulator zeroed.
-// D/8 threads per row, 8 elements (16 bytes) each.
+// D_i = rowsum(dO_i o O_i) in fp32, and the row's fp32 dQ accumulator zeroed,
+// for every row of every (batch, head) slice (packed: every row of the
+// packed tensors).  D/8 threads per row, 8 elements (16 bytes) each.
 template <int D, bool BF16>
-__global__ void fa2_bwd_preprocess_kernel(const void* __restrict__ o, const void* __restrict__ dout,
-                                          float* __restrict__ delta, float* __restrict__ dq_accum, long long rows) {
+__global__ void fa2_bwd_preprocess_kernel(const BwdParams p) {
   constexpr int TPR = D / 8;
+  const KernelParams& f = p.f;
+  const long long rows = p.slices * f.total_q;
   const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long row = g / TPR;
   const int part = (int)(g % TPR);
   float acc = 0.f;
   if (row < rows) {
-    const size_t off = (size_t)row * D + (size_t)part * 8;
-    const uint4 a = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(o) + off);
-    const uint4 b = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(dout) + off);
-    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+    // a row index fits in 32 bits (2^31 rows of d >= 64 would not fit in memory)
+    const int hb = (int)row / f.total_q, i = (int)row - hb * f.total_q;
+    const int b = hb / f.heads, h = hb - b * f.heads;
+    const long long off = (long long)b * f.o_bs + (long long)h * f.o_hs + (long long)i * f.o_rs + (long long)part * 8;
+    const uint4 a = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(f.o) + off);
+    const uint4 c = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.dout) + off);
+    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, cv[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 x = unpack2<BF16>(av[i]), y = unpack2<BF16>(bv[i]);
+    for (int k = 0; k < 4; ++k) {
+      const float2 x = unpack2<BF16>(av[k]), y = unpack2<BF16>(cv[k]);
       acc = fmaf(x.x, y.x, acc);
       acc = fmaf(x.y, y.y, acc);
     }
-    float4* z = reinterpret_cast<float4*>(dq_accum + off);
+    float4* z = reinterpret_cast<float4*>(p.dq_accum + row * D + (long long)part * 8);
     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
   for (int m = TPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-  if (row < rows && part == 0) delta[row] = acc;
+  if (row < rows && part == 0) const_cast<float*>(p.delta)[row] = acc;
 }
 
-// 16-bit dQ from the fp32 accumulator, 8 elements per thread.
-template <bool BF16>
-__global__ void fa2_bwd_dq_convert_kernel(const float* __restrict__ acc, void* __restrict__ dq, long long n8) {
+// 16-bit dQ (q's layout) from the fp32 accumulator, 8 elements per thread.
+template <int D, bool BF16>
+__global__ void fa2_bwd_dq_convert_kernel(const BwdParams p) {
+  const KernelParams& f = p.f;
+  const long long n8 = p.slices * f.total_q * (D / 8);
   const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= n8) return;
-  const float4 a = reinterpret_cast<const float4*>(acc)[2 * g];
-  const float4 b = reinterpret_cast<const float4*>(acc)[2 * g + 1];
-  reinterpret_cast<uint4*>(dq)[g] =
-      make_uint4(pack2<BF16>(a.x, a.y), pack2<BF16>(a.z, a.w), pack2<BF16>(b.x, b.y), pack2<BF16>(b.z, b.w));
+  const long long row = g / (D / 8);
+  const int part = (int)(g % (D / 8));
+  const int hb = (int)row / f.total_q, i = (int)row - hb * f.total_q;   // rows fit in 32 bits
+  const int b = hb / f.heads, h = hb - b * f.heads;
+  const float4 a = reinterpret_cast<const float4*>(p.dq_accum)[2 * g];
+  const float4 c = reinterpret_cast<const float4*>(p.dq_accum)[2 * g + 1];
+  uint16_t* dst = reinterpret_cast<uint16_t*>(p.dq) + (long long)b * p.q_bs + (long long)h * p.q_hs +
+                  (long long)i * p.q_rs + (long long)part * 8;
+  *reinterpret_cast<uint4*>(dst) =
+      make_uint4(pack2<BF16>(a.x, a.y), pack2<BF16>(a.z, a.w), pack2<BF16>(c.x, c.y), pack2<BF16>(c.z, c.w));
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16>
 int launch_bwd(const BwdLaunchArgs& a) {
   using C = BwdConfig<D>;
-  const long long rows = (long long)a.p.bh * a.p.n;
+  const long long rows = a.p.slices * a.p.f.total_q;   // every row of every (batch, head) slice
   {
     const long long threads = rows * (D / 8);
-    const unsigned blocks = (unsigned)((threads + 255) / 256);
-    fa2_bwd_preprocess_kernel<D, BF16><<<blocks, 256, 0, a.stream>>>(a.o, a.dout, const_cast<float*>(a.p.delta),
-                                                                     a.p.dq_accum, rows);
+    fa2_bwd_preprocess_kernel<D, BF16><<<(unsigned)((threads + 255) / 256), 256, 0, a.stream>>>(a.p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;
   }
-  auto kern = fa2_bwd_kernel<D, BF16, CAUSAL>;
+  auto kern = fa2_bwd_kernel<D, BF16>;
   static std::atomic<unsigned long long> configured{0};
   int e = once_per_device(configured, [&]() -> int {
     return (int)cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
   });
   if (e != 0) return e;
-  kern<<<(unsigned)(a.p.bh * a.p.num_tiles), C::THREADS, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v,
-                                                                                     a.tm_do, a.tm_dq, a.p);
+  kern<<<(unsigned)((long long)a.p.f.bh * a.p.num_k_tiles), C::THREADS, C::SMEM_BYTES, a.stream>>>(
+      a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq, a.p);
   e = (int)cudaGetLastError();
   if (e != 0) return e;
-  const long long n8 = rows * D / 8;
-  fa2_bwd_dq_convert_kernel<BF16><<<(unsigned)((n8 + 255) / 256), 256, 0, a.stream>>>(a.p.dq_accum, a.dq, n8);
+  const long long n8 = rows * (D / 8);
+  fa2_bwd_dq_convert_kernel<D, BF16><<<(unsigned)((n8 + 255) / 256), 256, 0, a.stream>>>(a.p);
   return (int)cudaGetLastError();
 }
 
 template <int D>
 int launch_bwd_dispatch(const BwdLaunchArgs& a) {
-  if (a.bf16) return a.causal ? launch_bwd<D, true, true>(a) : launch_bwd<D, true, false>(a);
-  return a.causal ? launch_bwd<D, false, true>(a) : launch_bwd<D, false, false>(a);
+  return a.bf16 ? launch_bwd<D, true>(a) : launch_bwd<D, false>(a);
 }
 
 }  // namespace fa2

@@ -54,29 +54,32 @@ struct LaunchArgs {
   cudaStream_t stream;
 };
 
+// Backward-pass arguments the kernels read.  Sequence offsets, strides and
+// sizes follow KernelParams (`f`): dout has o's layout, dq q's, dk k's and dv
+// v's.  Per (tensor batch, head) slice hb = b*H + h the workspace holds D
+// [hb][rows_q] and the fp32 dQ accumulator [hb][rows_q][d], rows_q = f.total_q.
 struct BwdParams {
-  const float* lse;    // [B,H,N] forward logsumexp (natural log)
-  const float* delta;  // [B,H,N] D_i = rowsum(dO_i o O_i), from the preprocess kernel
-  float* dq_accum;     // [B,H,N,d] fp32, zeroed by the preprocess kernel
-  void* dk;            // [B,H,N,d] 16-bit outputs
+  KernelParams f;       // o and lse are the forward's outputs here (read)
+  const void* q;        // read by the preprocess (nothing) and the kernels via maps
+  const void* dout;
+  void* dq;
+  void* dk;
   void* dv;
-  uint32_t* status;
-  int n;
-  int bh;
-  int num_tiles;       // ceil(N / 128): key tiles = query tiles
+  const float* delta;   // D_i = rowsum(dO_i o O_i), from the preprocess kernel
+  float* dq_accum;      // zeroed by the preprocess kernel
+  long long q_bs, q_hs, q_rs;   // q (= dq) strides
+  long long k_bs, k_hs, k_rs;   // k (= dk) strides
+  long long v_bs, v_hs, v_rs;   // v (= dv) strides
+  long long slices;     // (tensor batch) x heads: 1 x H for packed batches, B x H otherwise
+  int num_k_tiles;      // key tiles per (b, h), from the longest key sequence
   float scale;
-  float scale_log2;
 };
 
 struct BwdLaunchArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // boxes of 64 columns x 128 rows
   CUtensorMap tm_dq;                    // fp32 dQ accumulator, boxes of 32 columns x 32 rows
   BwdParams p;
-  const void* o;       // forward output, for D
-  const void* dout;    // upstream gradient
-  void* dq;            // 16-bit dQ output
   bool bf16;
-  bool causal;
   cudaStream_t stream;
 };
 

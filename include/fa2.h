@@ -283,6 +283,38 @@ int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const fl
 size_t fa2_bwd_workspace_bytes(int B, int H, int N, int d);
 
 /*
+ * fa2_bwd_params / fa2_bwd_ex -- gradients of fa2_fwd_ex: the same masks
+ * (band, prefix), unequal query / key lengths, strided layouts and packed
+ * batches.  `fwd` holds the forward call's arguments (q, k, v; o and lse
+ * are the forward's outputs and are read here); the gradients share the
+ * layouts of their primal tensors: dout and dq/dk/dv use o's, q's, k's and
+ * v's strides.  head_dim 64 or 128 (FA2_ERR_UNSUPPORTED otherwise).  Packed
+ * batches: fwd.seqlen_k is the longest sequence's key count (it sizes the
+ * grid; a sequence with more keys is left unwritten and reported as
+ * FA2_ERR_DEVICE_SEQLENS), and rows of dq outside every sequence are set to
+ * zero.  A key no query row sees gets dK = dV = 0; a query row that sees no
+ * key gets dQ = 0.
+ *
+ * `workspace`: device, >= fa2_bwd_ex_workspace_bytes(&fwd) bytes, 256-byte
+ * aligned: the fp32 dQ accumulator and D per row of every (batch, head)
+ * slice, written before read.  dq, dk, dv and the workspace overlap no input
+ * and no other output.  Asynchronous on `stream` (three kernels); dQ is
+ * accumulated with fp32 reduce-adds, so its last bits may vary between runs.
+ */
+typedef struct fa2_bwd_params {
+  fa2_fwd_params fwd;
+  const void* dout;       /* device, o's layout, 16-byte aligned */
+  void* dq;               /* device, q's layout, written */
+  void* dk;               /* device, k's layout, written */
+  void* dv;               /* device, v's layout, written */
+  void* workspace;
+  size_t workspace_bytes;
+} fa2_bwd_params;
+
+size_t fa2_bwd_ex_workspace_bytes(const fa2_fwd_params* fwd);
+int fa2_bwd_ex(const fa2_bwd_params* params, void* stream);
+
+/*
  * fa2_selftest_wait_timeout -- exercises the kernels' failure path without a
  * GPU fault: launches one CTA whose single wait, made through the same
  * bounded-wait routine every forward-kernel wait uses, is on an mbarrier that

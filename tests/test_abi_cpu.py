@@ -235,3 +235,42 @@ def test_decode_bad_arguments_rejected(lib, kw, code):
 
 def test_decode_null_params(lib):
     assert lib.fa2_decode(None, 9 * A, 1 << 20, None) == fa2.FA2_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- fa2_bwd_ex argument checks
+
+
+def _bwd(lib, dout=6 * A, dq=7 * A, dk=8 * A, dv=9 * A, ws=10 * A, ws_bytes=1 << 20, **kw):
+    b = fa2.Fa2BwdParams()
+    b.fwd = _params(**kw)
+    b.dout, b.dq, b.dk, b.dv, b.workspace, b.workspace_bytes = dout, dq, dk, dv, ws, ws_bytes
+    return lib.fa2_bwd_ex(ctypes.byref(b), None)
+
+
+def test_bwd_ex_workspace_plan(lib):
+    # [1, 2, 64, 64]: fp32 accumulator 2 x 64 x 64 x 4 bytes + D 2 x 64 x 4 bytes (256-byte aligned)
+    assert lib.fa2_bwd_ex_workspace_bytes(ctypes.byref(_params())) == 32768 + 512
+    assert lib.fa2_bwd_ex_workspace_bytes(ctypes.byref(_params(head_dim=256))) == 0
+    assert lib.fa2_bwd_ex_workspace_bytes(None) == 0
+    # the contiguous entry point asks for the same amount
+    assert fa2.fa2_bwd_workspace_bytes(1, 2, 64, 64) == 32768 + 512
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim=256), fa2.FA2_ERR_UNSUPPORTED),
+    (dict(dq=0), fa2.FA2_ERR_INVALID_ARG),
+    (dict(dout=6 * A + 8), fa2.FA2_ERR_MISALIGNED),
+    (dict(ws=10 * A + 64), fa2.FA2_ERR_MISALIGNED),
+    (dict(ws_bytes=1000), fa2.FA2_ERR_INVALID_ARG),
+    (dict(dq=A + 512), fa2.FA2_ERR_INVALID_ARG),           # dq over q
+    (dict(dk=6 * A), fa2.FA2_ERR_INVALID_ARG),             # dk over dout
+    (dict(dv=7 * A + 1024), fa2.FA2_ERR_INVALID_ARG),      # dv over dq
+    (dict(ws=8 * A), fa2.FA2_ERR_INVALID_ARG),             # workspace over dk
+    (dict(window_left=-7), fa2.FA2_ERR_INVALID_ARG),
+])
+def test_bwd_ex_bad_arguments_rejected(lib, kw, code):
+    assert _bwd(lib, **kw) == code
+
+
+def test_bwd_ex_null_params(lib):
+    assert lib.fa2_bwd_ex(None, None) == fa2.FA2_ERR_INVALID_ARG
