@@ -298,6 +298,29 @@ def general_mask(args, w: sy.Workload):
             "bytes": inputs + rows_q * w.H * (w.d * 2 + 4)}
 
 
+def backward_step(fa2, torch, w: sy.Workload, forward_step, q, k, v, o, lse, stream, **opts):
+    """Run the forward once, then return the timed fa2_bwd_ex call for a seeded dout of o's layout."""
+    import ctypes
+
+    with torch.cuda.stream(stream):
+        forward_step()
+    stream.synchronize()
+    g = torch.Generator(device="cpu").manual_seed(w.seed(0) + 500)
+    dout = torch.empty_strided(o.shape, o.stride(), dtype=o.dtype, device=o.device)
+    dout.copy_(torch.randn(o.shape, generator=g).to(o.dtype))
+    like = lambda t: torch.empty_strided(t.shape, t.stride(), dtype=t.dtype, device=t.device)
+    dq, dk, dv = like(q), like(k), like(v)
+    p, _, _ = fa2._general_params(q, k, v, o, lse, w.scale, opts.get("window_left", -1), opts.get("window_right", -1),
+                                  opts.get("prefix_len", 0), opts.get("cu_seqlens_q"), opts.get("cu_seqlens_k"),
+                                  opts.get("max_seqlen_q"), opts.get("max_seqlen_k"))
+    need = int(fa2.load_library().fa2_bwd_ex_workspace_bytes(ctypes.byref(p)))
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+
+    def step():
+        fa2.fa2_bwd_ex(q, k, v, o, lse, dout, dq, dk, dv, workspace=ws, scale=w.scale, stream=stream, **opts)
+    return step
+
+
 def varlen_lengths(total: int, seqs: int, seed: int) -> np.ndarray:
     """Seeded random sequence lengths (each >= 1) summing to total."""
     rng = np.random.default_rng(seed)
@@ -305,8 +328,9 @@ def varlen_lengths(total: int, seqs: int, seed: int) -> np.ndarray:
     return np.diff(np.concatenate([[0], cuts, [total]])).astype(np.int64)
 
 
-def general_step(fa2, torch, w: sy.Workload, gen, dev, tdt, stream):
-    """Inputs, the timed fa2_fwd_ex call and its algorithmic FLOPs for the general options."""
+def general_step(fa2, torch, w: sy.Workload, gen, dev, tdt, stream, backward=False):
+    """Inputs, the timed call (fa2_fwd_ex / fa2_decode, or fa2_bwd_ex after one forward) and
+    its algorithmic FLOPs (the backward: 2.5x the forward's) for the general options."""
     wl, wr, pre = gen["window_left"], gen["window_right"], gen["prefix"]
     to_dev = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(tdt).to(dev)
     if gen["varlen_seqs"]:
@@ -325,6 +349,11 @@ def general_step(fa2, torch, w: sy.Workload, gen, dev, tdt, stream):
             fa2.fa2_fwd_ex(q, k, v, o, lse, scale=w.scale, window_left=wl, window_right=wr, prefix_len=pre,
                            cu_seqlens_q=cu, cu_seqlens_k=cu, max_seqlen_q=maxlen, stream=stream)
         flops = 4.0 * w.d * w.H * vis
+        if backward:
+            step = backward_step(fa2, torch, w, step, q, k, v, o, lse, stream, window_left=wl, window_right=wr,
+                                 prefix_len=pre, cu_seqlens_q=cu, cu_seqlens_k=cu, max_seqlen_q=maxlen,
+                                 max_seqlen_k=maxlen)
+            flops *= 2.5
         return step, flops, None, None, None
     nk = gen["seqlen_k"]
     if gen["decode_rows"]:
@@ -356,6 +385,10 @@ def general_step(fa2, torch, w: sy.Workload, gen, dev, tdt, stream):
         fa2.fa2_fwd_ex(q, k, v, o, lse, scale=w.scale, window_left=wl, window_right=wr, prefix_len=pre,
                        stream=stream)
     flops = 4.0 * w.d * w.B * w.H * float(sy.visible_keys(w.N, nk, wl, wr, pre).sum())
+    if backward:
+        step = backward_step(fa2, torch, w, step, q, k, v, o, lse, stream, window_left=wl, window_right=wr,
+                             prefix_len=pre)
+        flops *= 2.5
     return step, flops, q_bits, k_bits, v_bits
 
 
@@ -398,8 +431,8 @@ def main():
     if args.heads > 0:
         w = sy.Workload(w.index, w.B, args.heads, w.N, w.d, w.dtype, w.causal, w.q_scale)
     gen = general_mask(args, w)
-    if gen is not None and args.backward:
-        ap.error("the general-forward options time the forward pass only")
+    if gen is not None and args.backward and gen["decode_rows"]:
+        ap.error("--decode-rows times the forward pass only")
     if args.impl == "reference":
         return run_reference(args, w, gen)
 
@@ -433,9 +466,9 @@ def main():
 
     flops = w.flops() * (2.5 if args.backward else 1.0)
     if gen is not None:
-        step, flops, q_bits, k_bits, v_bits = general_step(fa2, torch, w, gen, dev, tdt, stream)
+        step, flops, q_bits, k_bits, v_bits = general_step(fa2, torch, w, gen, dev, tdt, stream, args.backward)
 
-    if args.backward:
+    if args.backward and gen is None:
         with torch.cuda.stream(stream):
             step()
         stream.synchronize()
@@ -554,8 +587,8 @@ def main():
                                     "fa2_fwd_pingpong_kernel" if w.d <= 128 else "fa2_fwd_dbuf_kernel"),
                          "avg_launch_ms": avg_launch_ms,
                          "algorithmic_flops_per_launch": flops,
-                         "algorithmic_bytes_per_launch": (w.algorithmic_bytes() * (2 if args.backward else 1)
-                                                          if gen is None else gen["bytes"])},
+                         "algorithmic_bytes_per_launch": (w.algorithmic_bytes() if gen is None else gen["bytes"]) *
+                                                         (2 if args.backward else 1)},
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                        "samples": clk["samples"]},
             "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": args.steps * (3 if args.backward else 1),
