@@ -112,9 +112,9 @@ int encode_map_rows(CUtensorMap* m, const void* base, int d, long long rows, lon
 // that whole-struct comparison is exact.
 struct MapKey {
   int dev, dtype, d, merged;
-  const void* ptr[3];        // q, k, v
-  long long dims[3][3];      // rows, heads, batch of each
-  long long strides[3][3];   // batch, head, row strides of each (elements)
+  const void* ptr[4];        // q, k, v, o
+  long long dims[4][3];      // rows, heads, batch of each
+  long long strides[4][3];   // batch, head, row strides of each (elements)
 };
 
 // The tensor maps of the last forward (and, separately, decode) call on this
@@ -123,7 +123,7 @@ struct MapKey {
 struct MapCache {
   bool valid = false;
   MapKey key;
-  CUtensorMap tm_q, tm_k, tm_v;
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;
 };
 thread_local MapCache t_maps;
 thread_local MapCache t_decode_maps;
@@ -155,11 +155,12 @@ int cached_maps(LaunchArgs& a, const MapKey& key) {
   if (!(c.valid && std::memcmp(&c.key, &key, sizeof(MapKey)) == 0)) {
     const bool bf16 = key.dtype == FA2_BF16;
     const TileGeometry g = tile_geometry(key.d);
-    CUtensorMap* maps[3] = {&c.tm_q, &c.tm_k, &c.tm_v};
+    CUtensorMap* maps[4] = {&c.tm_q, &c.tm_k, &c.tm_v, &c.tm_o};
+    const int rows[4] = {g.q_rows, g.kv_rows, g.kv_rows, 32};   // o: one warp's 32 rows per box
     c.valid = false;
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < 4; ++i) {
       if (encode_map_rows(maps[i], key.ptr[i], key.d, key.dims[i][0], key.dims[i][1], key.dims[i][2],
-                          key.strides[i], i == 0 ? g.q_rows : g.kv_rows, bf16, key.merged != 0))
+                          key.strides[i], rows[i], bf16, key.merged != 0))
         return FA2_ERR_CUDA;
     }
     std::memcpy(&c.key, &key, sizeof(MapKey));
@@ -168,21 +169,8 @@ int cached_maps(LaunchArgs& a, const MapKey& key) {
   a.tm_q = c.tm_q;
   a.tm_k = c.tm_k;
   a.tm_v = c.tm_v;
+  a.tm_o = c.tm_o;
   return FA2_OK;
-}
-
-// [B*H, N, d] view of a contiguous [B,H,N,d] tensor; boxes of 64 columns x
-// `rows` rows, 128-byte swizzle (the backward kernels' maps).
-int encode_map(CUtensorMap* m, const void* base, int bh, int n, int d, int rows, bool bf16) {
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)n * (cuuint64_t)d * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? FA2_OK : FA2_ERR_CUDA;
 }
 
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
@@ -334,18 +322,20 @@ int prepare(const fa2_fwd_params& a, int units_rows, Prepared& out, const Extent
   if (cudaGetDevice(&key.dev) != cudaSuccess) return FA2_ERR_CUDA;
   key.dtype = a.dtype;
   key.d = d;
-  const void* ptrs[3] = {a.q, a.k, a.v};
-  for (int t = 0; t < 3; ++t) {
-    const long long* dims = t == 0 ? dq : dk;
+  const void* ptrs[4] = {a.q, a.k, a.v, a.o};
+  for (int t = 0; t < 4; ++t) {
+    const long long* dims = (t == 0 || t == 3) ? dq : dk;
     key.ptr[t] = ptrs[t];
     key.dims[t][0] = dims[2];  // rows, heads, batch
     key.dims[t][1] = dims[1];
     key.dims[t][2] = dims[0];
-    for (int i = 0; i < 3; ++i) key.strides[t][i] = st_in[t][i];
+    for (int i = 0; i < 3; ++i) key.strides[t][i] = t < 3 ? st_in[t][i] : o_st[i];
   }
+  // one map rank for every tensor: merge (batch, head) only when q, k, v and
+  // o all allow it (the backward's dout shares o's strides)
   key.merged = 1;
-  for (int t = 0; t < 3; ++t)
-    if (!mergeable(a.heads, tb, st_in[t])) key.merged = 0;
+  for (int t = 0; t < 4; ++t)
+    if (!mergeable(a.heads, tb, key.strides[t])) key.merged = 0;
   for (int i = 0; i < 3; ++i) out.q_st[i] = st_in[0][i];
   KernelParams& p = out.p;
   std::memset(&p, 0, sizeof(p));
@@ -365,6 +355,7 @@ int prepare(const fa2_fwd_params& a, int units_rows, Prepared& out, const Extent
   p.total_k = (int)rows_k;
   p.heads = a.heads;
   p.merged_bh = key.merged;
+  p.tma_o = packed ? 0 : 1;   // packed: a box would spill into the next sequence's rows
   p.bh = a.batch * a.heads;
   p.units = (int)units;
   p.window_left = a.window_left;
@@ -836,12 +827,6 @@ int backward(const fa2_bwd_params& bp, cudaStream_t stream) {
   Prepared pr;
   rc = prepare(a, 128, pr);
   if (rc) return rc;
-  // one map rank for every tensor the kernel loads: merge (batch, head) only
-  // when q, k, v and dout all allow it
-  if (!mergeable(a.heads, tb, st[3])) {
-    pr.key.merged = 0;
-    pr.p.merged_bh = 0;
-  }
   BwdLaunchArgs la;
   std::memset(&la, 0, sizeof(la));
   LaunchArgs fl;

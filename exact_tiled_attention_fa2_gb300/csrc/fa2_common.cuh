@@ -196,6 +196,16 @@ __device__ __forceinline__ void tma_load_rows(uint32_t dst, const CUtensorMap* m
     tma_load_4d(dst, map, x, row, h, b, bar);
 }
 
+// Stores one 64-column box of rows (the map's box height) of head h, batch b
+// from shared memory, whichever rank the map has; tracked by a bulk group.
+__device__ __forceinline__ void tma_store_rows(const CUtensorMap* map, bool merged, uint32_t src, int x, int row, int h,
+                                               int b, int hb) {
+  if (merged)
+    tma_store_3d(map, src, x, row, hb);
+  else
+    tma_store_4d(map, src, x, row, h, b);
+}
+
 // One (batch, head) slice: where its rows start in the tensors and how long
 // it is.  Packed batches read their offsets from cu_q / cu_k.
 struct SeqInfo {
@@ -284,6 +294,61 @@ __device__ __forceinline__ void store_row(const KernelParams& p, const SeqInfo& 
   if (valid)
     p.lse[(long long)s.b * p.l_bs + (long long)s.h * p.l_hs + s.row0_q + row] =
         empty ? -INFINITY : (m_run + log2f(l_run)) * 0.6931471805599453f;
+}
+
+// Epilogue through shared memory: row r (0..127) of a tile's O = O~ / l,
+// rounded to 16 bits, into sO -- D/64 blocks of 128 rows x 128 bytes with the
+// 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r mod 8)), the
+// layout a TMA store of 32-row boxes reads -- and its LSE straight to global
+// memory.  A row that sees no key gets O = 0 and LSE = -inf.
+template <int D, bool BF16>
+__device__ __forceinline__ void stage_row(const KernelParams& p, const SeqInfo& s, int row, int r, uint32_t sO,
+                                          uint32_t tO, float m_run, float l_run) {
+  const bool empty = !(l_run > 0.f);
+  const float inv_l = empty ? 0.f : 1.f / l_run;
+#pragma unroll 1
+  for (int c = 0; c < D; c += 32) {
+    uint32_t o[32];
+    tmem_ld_32x32b_x32(tO + c, o);
+    tmem_ld_wait_x32(o);
+    uint32_t packed[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      packed[i] = empty ? 0u : pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+    const uint32_t row_base = sO + (uint32_t)(c / 64) * (128u * 128u) + (uint32_t)r * 128u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int chunk = (c % 64) / 8 + i;
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(row_base + (uint32_t)((chunk ^ (r & 7)) * 16)),
+                   "r"(packed[4 * i]), "r"(packed[4 * i + 1]), "r"(packed[4 * i + 2]), "r"(packed[4 * i + 3])
+                   : "memory");
+    }
+  }
+  if (row < s.n_q)
+    p.lse[(long long)s.b * p.l_bs + (long long)s.h * p.l_hs + s.row0_q + row] =
+        empty ? -INFINITY : (m_run + log2f(l_run)) * 0.6931471805599453f;
+}
+
+// One warp's 32 staged rows (rows 32 quad .. 32 quad + 31 of the tile whose
+// first row is q0) to global memory by TMA; rows past the tensor are clipped
+// (unpacked batches only: a packed sequence's tail would reach the next one).
+// The warp waits until the stores have completed.
+template <int D>
+__device__ __forceinline__ void store_staged_rows(const CUtensorMap* tm_o, const KernelParams& p, const SeqInfo& s,
+                                                  uint32_t sO, int q0, int quad, int lane) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    const bool merged = p.merged_bh != 0;
+    const int hb = s.b * p.heads + s.h;
+#pragma unroll
+    for (int kb = 0; kb < D / 64; ++kb)
+      tma_store_rows(tm_o, merged, sO + (uint32_t)kb * (128u * 128u) + (uint32_t)quad * (32u * 128u), kb * 64,
+                     s.row0_q + q0 + quad * 32, s.h, s.b, hb);
+    bulk_commit_group();
+    bulk_wait_all();
+  }
+  __syncwarp();
 }
 
 // Rows of a query tile that see no key at all: O = 0, LSE = -inf, without

@@ -208,7 +208,7 @@ __device__ __forceinline__ void db_mma(const DbufCtx& t) {
 
 template <class C, bool BF16, bool BAND>
 __device__ __forceinline__ void db_softmax(const DbufCtx& t, const KernelParams& p, const CtaFacts* facts, int warp,
-                                           int lane) {
+                                           int lane, const CUtensorMap* tm_o) {
   const int quad = warp & 3;
   const int r = quad * 32 + lane;
   const int row = t.q0 + r;
@@ -297,7 +297,13 @@ __device__ __forceinline__ void db_softmax(const DbufCtx& t, const KernelParams&
   }
   if (!ok) return;
   tc_fence_after();
-  store_row<C::D, BF16>(p, facts->seq, row, tO, m_run, l_run);
+  if (p.tma_o) {
+    // the Q buffer is free: the last S product completed before DB_OLAST
+    stage_row<C::D, BF16>(p, facts->seq, row, r, t.sQ, tO, m_run, l_run);
+    store_staged_rows<C::D>(tm_o, p, facts->seq, t.sQ, t.q0, quad, lane);
+  } else {
+    store_row<C::D, BF16>(p, facts->seq, row, tO, m_run, l_run);
+  }
 }
 
 // BAND: the first key a query row sees may depend on the row (a bounded left
@@ -305,7 +311,8 @@ __device__ __forceinline__ void db_softmax(const DbufCtx& t, const KernelParams&
 template <int D, bool BF16, bool BAND>
 __global__ void __launch_bounds__(192, 1)
     fa2_fwd_dbuf_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const KernelParams p) {
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                        const KernelParams p) {
   using C = DbufConfig<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -371,6 +378,7 @@ __global__ void __launch_bounds__(192, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
   }
   if (warp == C::MMA_WARP) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -387,7 +395,7 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) db_mma<C, BF16>(t);
     __syncwarp();
   } else {
-    db_softmax<C, BF16, BAND>(t, p, facts, warp, lane);
+    db_softmax<C, BF16, BAND>(t, p, facts, warp, lane, &tm_o);
   }
   tc_fence_before();
   __syncthreads();
@@ -408,7 +416,7 @@ int launch_fwd_dbuf(const LaunchArgs& a) {
   if (e != 0) return e;
   static_assert(C::BR == 128, "query rows per CTA: tile_geometry(d).cta_rows sizes the grid");
   dim3 grid((unsigned)(a.p.bh * a.p.units));
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.p);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
   return (int)cudaGetLastError();
 }
 

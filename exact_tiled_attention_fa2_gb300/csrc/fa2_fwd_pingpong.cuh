@@ -275,7 +275,7 @@ __device__ __forceinline__ void pp_p_chunk(const uint32_t* sr, int ch, uint32_t 
 
 template <class C, bool BF16, bool BAND>
 __device__ __forceinline__ void pp_softmax(const PairCtx& t, const KernelParams& p, const CtaFacts* facts, int q,
-                                           int warp, int lane) {
+                                           int warp, int lane, const CUtensorMap* tm_o) {
   const int nkv = q ? t.nkv[1] : t.nkv[0];   // selects, not a runtime-indexed local array
   const int q0 = q ? t.q0[1] : t.q0[0];
   const int kt0 = t.kv0 + (q ? t.first[1] : t.first[0]);
@@ -361,7 +361,14 @@ __device__ __forceinline__ void pp_softmax(const PairCtx& t, const KernelParams&
   }
   if (!ok) return;
   tc_fence_after();
-  store_row<C::D, BF16>(p, facts->seq, row, tO, m_run, l_run);
+  if (p.tma_o) {
+    // the tile's Q buffer is free: its last S product completed before PB_O
+    const uint32_t sO = t.sQ + (uint32_t)q * C::Q_BYTES;
+    stage_row<C::D, BF16>(p, facts->seq, row, r, sO, tO, m_run, l_run);
+    store_staged_rows<C::D>(tm_o, p, facts->seq, sO, q0, quad, lane);
+  } else {
+    store_row<C::D, BF16>(p, facts->seq, row, tO, m_run, l_run);
+  }
 }
 
 // BAND: the first key a query row sees may depend on the row (a bounded left
@@ -370,7 +377,8 @@ __device__ __forceinline__ void pp_softmax(const PairCtx& t, const KernelParams&
 template <int D, bool BF16, bool BAND>
 __global__ void __launch_bounds__(384, 1)
     fa2_fwd_pingpong_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                            const __grid_constant__ CUtensorMap tm_v, const KernelParams p) {
+                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                            const KernelParams p) {
   using C = PingPongConfig<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -455,6 +463,7 @@ __global__ void __launch_bounds__(384, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
   }
   if (warp == C::MMA_WARP) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -475,7 +484,7 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else {
     regs_increase<C::REGS_SOFTMAX>();
-    pp_softmax<C, BF16, BAND>(t, p, facts, warp >> 2, warp, lane);
+    pp_softmax<C, BF16, BAND>(t, p, facts, warp >> 2, warp, lane, &tm_o);
   }
   tc_fence_before();
   __syncthreads();
@@ -502,7 +511,7 @@ int launch_fwd_pingpong(const LaunchArgs& a) {
   if (e != 0) return e;
   static_assert(C::NQ * C::BR == 256, "query rows per CTA: tile_geometry(d).cta_rows sizes the grid");
   dim3 grid((unsigned)(a.p.bh * a.p.units));
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.p);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
   return (int)cudaGetLastError();
 }
 

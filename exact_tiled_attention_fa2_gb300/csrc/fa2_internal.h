@@ -34,6 +34,7 @@ struct KernelParams {
   int total_k;        // packed: rows of k/v (bound for cu_k); else n_k
   int heads;          // H
   int merged_bh;      // 1: the tensor maps are 3-D (d, rows, B*H), coordinate b*H + h; 0: 4-D
+  int tma_o;          // 1: O is staged in shared memory and written by TMA stores (unpacked batches)
   int bh;             // B * H
   int units;          // query units (tiles or tile pairs) per (b, h), from n_q
   int window_left;    // key j visible to query i iff i+off-wl <= j <= i+off+wr
@@ -48,6 +49,7 @@ constexpr uint32_t kStatusBadSeqlens = 2u;
 
 struct LaunchArgs {
   CUtensorMap tm_q, tm_k, tm_v;  // (d, rows, B*H) or (d, rows, H, B) maps, boxes of 64 columns
+  CUtensorMap tm_o;              // the same view of o, boxes of 64 columns x 32 rows (one warp's rows)
   KernelParams p;
   bool bf16;
   bool band;  // window_left >= 0 or prefix > 0: a row's first visible key depends on the row
