@@ -17,9 +17,11 @@
 // shared-memory ring; four compute warps each take BLOCK/4 keys of a stage.
 // A key row is spread over d/8 lanes (16 bytes each), so a lane keeps only
 // its 8 elements of each query row in registers; the partial dot products
-// are summed across those lanes with xor shuffles.  The running maximum is
-// raised only past a 2^8 margin (as in the tiled kernels), so rescaling
-// O~ is rare.  At the end the per-lane-group states are merged through the
+// of all rows are summed across those lanes by a reduce-scatter that leaves
+// each lane the score of one row, whose online-softmax state that lane keeps
+// (one exponential per lane per key); p then goes back to every lane for
+// its part of O~.  The running maximum is raised only past a 2^8 margin (as
+// in the tiled kernels), so rescaling O~ is rare.  At the end the per-lane-group states are merged through the
 // (then idle) stage buffers and written to the caller's workspace.
 #pragma once
 
@@ -109,47 +111,85 @@ __device__ __forceinline__ bool decode_range(const KeyMask& km, int n_q, int spl
   return c1 > c0;
 }
 
+// Lane (within its group of G) that owns query row r after dc_reduce_scatter.
+template <int NQ, int G>
+__device__ __forceinline__ constexpr int dc_owner(int r) {
+  int li = 0;
+  for (int rd = 0, w = NQ; w > 1; ++rd, w >>= 1)
+    if ((r / (w / 2)) & 1) li += G >> (rd + 1);   // which half of the current rows r lies in
+  return li;
+}
+
+// Sum partial dot products over the G lanes of a group so that each lane ends
+// with the full sum for one row (lanes own rows in halving steps: a lane keeps
+// one half of the rows and passes the other half to its partner, then the
+// last lanes sharing a row add up): log2(G) shuffles instead of NQ log2(G).
+// Returns the lane's row; v[0] holds its sum.
+template <int NQ, int G>
+__device__ __forceinline__ int dc_reduce_scatter(float* v, int li) {
+  int own = 0;
+#pragma unroll
+  for (int rd = 0, w = NQ; w > 1; ++rd, w >>= 1) {
+    const int mask = G >> (rd + 1);
+    const bool upper = (li & mask) != 0;
+    const int half = w / 2;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+    }
+    if (upper) own += half;
+  }
+#pragma unroll
+  for (int mask = G / NQ / 2; mask >= 1; mask >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], mask);
+  return own;
+}
+
 template <int NQ, class C, bool BF16>
 __device__ __forceinline__ void dc_compute(const DecodeParams& dp, const SeqInfo& seq, const KeyMask& km, int n_q,
                                            int c0, int c1, uint32_t sbase, uint32_t bar0, volatile int* abort_flag,
                                            int warp, int lane, float* st_m, float* st_l, float* st_o) {
+  static_assert(NQ <= C::G, "one row per lane after the reduce-scatter");
   const KernelParams& p = dp.f;
   const int g = lane / C::G;            // lane group within the warp (its key of a step)
-  const int e0 = (lane % C::G) * 8;     // this lane's 8 elements of a row
-  // this lane's slice of every query row, in the exp2 domain
-  float q[NQ][8];
+  const int li = lane % C::G;           // lane within the group
+  const int gbase = g * C::G;
+  const int e0 = li * 8;                // this lane's 8 elements of a row
+  // this lane's slice of every query row (exp2 domain), as fp32 pairs
+  float2 q[NQ][4];
 #pragma unroll
   for (int r = 0; r < NQ; ++r) {
+    float x[8];
     if (r < n_q) {
       const uint8_t* src = reinterpret_cast<const uint8_t*>(dp.q) +
                            2 * ((long long)seq.b * dp.q_bs + (long long)seq.h * dp.q_hs +
                                 (long long)(seq.row0_q + r) * dp.q_rs + e0);
-      unpack8<BF16>(*reinterpret_cast<const uint4*>(src), q[r]);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) q[r][e] *= p.scale_log2;
+      unpack8<BF16>(*reinterpret_cast<const uint4*>(src), x);
     } else {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) q[r][e] = 0.f;
+      for (int e = 0; e < 8; ++e) x[e] = 0.f;
     }
-  }
-  // rows past n_q repeat the last row's band (they are computed, never stored)
-  int row_lo[NQ], row_hi[NQ];
 #pragma unroll
-  for (int r = 0; r < NQ; ++r) {
-    row_lo[r] = km.row_lo(min(r, n_q - 1));
-    row_hi[r] = km.row_hi(min(r, n_q - 1));
+    for (int e = 0; e < 4; ++e) q[r][e] = make_float2(x[2 * e] * p.scale_log2, x[2 * e + 1] * p.scale_log2);
   }
+  // the row this lane owns after the reduce-scatter, and that row's band;
+  // rows past n_q repeat the last row's band (computed, never stored)
+  int own = 0;   // as dc_reduce_scatter assigns it (it depends on the lane only)
+#pragma unroll
+  for (int rd = 0, w = NQ; w > 1; ++rd, w >>= 1)
+    if (li & (C::G >> (rd + 1))) own += w / 2;
+  const int own_row = min(own, n_q - 1);
+  const int own_lo = km.row_lo(own_row), own_hi = km.row_hi(own_row);
   // a stage needs no per-key mask when it ends before c1 and every row sees all of it
   const int lo_last = km.row_lo(n_q - 1);
   const int hi_first = km.row_hi(0);
-  float m[NQ], l[NQ], o[NQ][8];
+  float m = -INFINITY, l = 0.f;   // the owned row's state (exp2 domain)
+  float2 o[NQ][4];                 // every row's 8 output elements of this lane
 #pragma unroll
-  for (int r = 0; r < NQ; ++r) {
-    m[r] = -INFINITY;
-    l[r] = 0.f;
+  for (int r = 0; r < NQ; ++r)
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[r][e] = 0.f;
-  }
+    for (int e = 0; e < 4; ++e) o[r][e] = make_float2(0.f, 0.f);
   const int nblk = (c1 - c0 + C::BLOCK - 1) / C::BLOCK;
   bool ok = true;
   for (int b = 0; b < nblk; ++b) {
@@ -167,40 +207,64 @@ __device__ __forceinline__ void dc_compute(const DecodeParams& dp, const SeqInfo
     for (int step = 0; step < C::STEPS; ++step) {
       const int kl = warp * C::KEYS_PER_WARP + step * C::KPW + g;   // key within the stage
       const int key = kb0 + kl;
-      float kx[8];
-      unpack8<BF16>(lds128(sK + kl * (C::D * 2) + e0 * 2), kx);
-      float sc[NQ];
+      const uint4 kr = lds128(sK + kl * (C::D * 2) + e0 * 2);
+      const float2 k0 = unpack2<BF16>(kr.x), k1 = unpack2<BF16>(kr.y), k2 = unpack2<BF16>(kr.z),
+                   k3 = unpack2<BF16>(kr.w);
+      float v[NQ];
 #pragma unroll
       for (int r = 0; r < NQ; ++r) {
-        float a = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) a = fmaf(q[r][e], kx[e], a);
-#pragma unroll
-        for (int off = C::G / 2; off >= 1; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-        sc[r] = a;
+        float2 a = __fmul2_rn(q[r][0], k0);
+        a = __ffma2_rn(q[r][1], k1, a);
+        a = __ffma2_rn(q[r][2], k2, a);
+        a = __ffma2_rn(q[r][3], k3, a);
+        v[r] = a.x + a.y;
       }
+      dc_reduce_scatter<NQ, C::G>(v, li);
+      float sc = v[0];   // the owned row's score for this key
       if (!full) {
+        const bool vis = key < c1 && (key < km.pre_end || (key >= own_lo && key <= own_hi));
+        if (!vis) sc = -INFINITY;
+      }
+      // raise the maximum past a 2^8 margin (rare after the first key): every
+      // lane then rescales its elements of the rows whose owners raised (with
+      // one row every lane holds that row's state and rescales on its own)
+      const bool raise = sc > m + kRescaleDecodeLog2;
+      if (NQ == 1) {
+        if (raise) {
+          const float alpha = ex2_approx(m - sc);   // 0 when m was -inf
+          m = sc;
+          l *= alpha;
+          const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[0][e] = __fmul2_rn(o[0][e], a2);
+        }
+      } else if (__any_sync(0xffffffffu, raise)) {
+        const float alpha = raise ? ex2_approx(m - sc) : 1.f;   // 0 when m was -inf
+        if (raise) {
+          m = sc;
+          l *= alpha;
+        }
 #pragma unroll
         for (int r = 0; r < NQ; ++r) {
-          const bool vis = key < c1 && (key < km.pre_end || (key >= row_lo[r] && key <= row_hi[r]));
-          if (!vis) sc[r] = -INFINITY;
+          const float ar = __shfl_sync(0xffffffffu, alpha, gbase + dc_owner<NQ, C::G>(r));
+          const float2 a2 = make_float2(ar, ar);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[r][e] = __fmul2_rn(o[r][e], a2);
         }
       }
-      float vx[8];
-      unpack8<BF16>(lds128(sV + kl * (C::D * 2) + e0 * 2), vx);
+      const float pown = ex2_approx(sc - (m == -INFINITY ? 0.f : m));   // 0 for a hidden key
+      l += pown;
+      const uint4 vr = lds128(sV + kl * (C::D * 2) + e0 * 2);
+      const float2 v0 = unpack2<BF16>(vr.x), v1 = unpack2<BF16>(vr.y), v2 = unpack2<BF16>(vr.z),
+                   v3 = unpack2<BF16>(vr.w);
 #pragma unroll
       for (int r = 0; r < NQ; ++r) {
-        if (sc[r] > m[r] + kRescaleDecodeLog2) {   // raise the maximum (rare after the first key)
-          const float alpha = ex2_approx(m[r] - sc[r]);   // 0 when m was -inf
-          m[r] = sc[r];
-          l[r] *= alpha;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o[r][e] *= alpha;
-        }
-        const float pr = ex2_approx(sc[r] - (m[r] == -INFINITY ? 0.f : m[r]));   // 0 for a hidden key
-        l[r] += pr;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[r][e] = fmaf(pr, vx[e], o[r][e]);
+        const float pr = NQ == 1 ? pown : __shfl_sync(0xffffffffu, pown, gbase + dc_owner<NQ, C::G>(r));
+        const float2 p2 = make_float2(pr, pr);
+        o[r][0] = __ffma2_rn(p2, v0, o[r][0]);
+        o[r][1] = __ffma2_rn(p2, v1, o[r][1]);
+        o[r][2] = __ffma2_rn(p2, v2, o[r][2]);
+        o[r][3] = __ffma2_rn(p2, v3, o[r][3]);
       }
     }
     __syncwarp();
@@ -212,15 +276,15 @@ __device__ __forceinline__ void dc_compute(const DecodeParams& dp, const SeqInfo
   ok = __all_sync(0xffffffffu, ok);
   if (!ok) return;
   const int grp = warp * C::KPW + g;
+  if (li == dc_owner<NQ, C::G>(own)) {   // one lane per owned row writes its state
+    st_m[grp * kDecodeMaxRows + own] = m;
+    st_l[grp * kDecodeMaxRows + own] = l;
+  }
 #pragma unroll
   for (int r = 0; r < NQ; ++r) {
-    if (lane % C::G == 0) {
-      st_m[grp * kDecodeMaxRows + r] = m[r];
-      st_l[grp * kDecodeMaxRows + r] = l[r];
-    }
     float4* dst = reinterpret_cast<float4*>(st_o + ((size_t)grp * kDecodeMaxRows + r) * C::D + e0);
-    dst[0] = make_float4(o[r][0], o[r][1], o[r][2], o[r][3]);
-    dst[1] = make_float4(o[r][4], o[r][5], o[r][6], o[r][7]);
+    dst[0] = make_float4(o[r][0].x, o[r][0].y, o[r][1].x, o[r][1].y);
+    dst[1] = make_float4(o[r][2].x, o[r][2].y, o[r][3].x, o[r][3].y);
   }
 }
 
@@ -253,10 +317,11 @@ __device__ __forceinline__ void dc_write_partial(const DecodeParams& dp, int bh,
   }
 }
 
-// Eight query rows keep 8 x 8 elements of q and O~ per lane in registers:
-// that instantiation runs one CTA per SM with the whole register file.
+// Two CTAs per SM for every row count: with eight rows (8 x 8 elements of q
+// and O~ per lane) that costs a few spilled registers but hides twice the
+// latency, which measured faster than one CTA per SM with none.
 template <int D, bool BF16, int NQ>
-__global__ void __launch_bounds__(DecodeConfig<D>::THREADS, NQ >= 8 ? 1 : 2)
+__global__ void __launch_bounds__(DecodeConfig<D>::THREADS, 2)
     fa2_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                       const DecodeParams dp) {
   using C = DecodeConfig<D>;
