@@ -435,7 +435,9 @@ __global__ void __launch_bounds__(384, 1)
 
   BwdCtx t;
   int bh, unit;
-  unit_of_block((int)blockIdx.x, f.bh, p.num_k_tiles, bh, unit);
+  // heads in groups of 4: a key tile re-streams the Q and dO tiles of every
+  // query tile it visits, and 4 heads' worth stay in L2 better than 8 (measured)
+  unit_of_block((int)blockIdx.x, f.bh, p.num_k_tiles, bh, unit, 4);
   // The whole CTA leaves together, before any set-up, when its sequence is
   // malformed, has more keys than the grid covers, or ends before this tile.
   if (!seq_info(f, bh, t.seq)) return;

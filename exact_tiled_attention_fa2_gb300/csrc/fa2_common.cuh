@@ -364,27 +364,29 @@ __device__ __forceinline__ void store_empty_row(const KernelParams& p, const Seq
 }
 
 // Order of work units over a 1-D grid of (B*H) x units blocks.  Heads go in
-// groups of kHeadGroup; inside a group the units run from the last (the one
+// groups of `group`; inside a group the units run from the last (the one
 // with the most key tiles under a causal mask) to the first, heads
 // interleaved.  So the CTAs resident at a time share the K/V of about
 // kHeadGroup heads in L2, and causal work is launched longest first within
 // each group, whose short tail overlaps the next group's long units.
-constexpr int kHeadGroup = 8;
+constexpr int kHeadGroup = 8;   // forward kernels (measured: 4 and 16 lose on the long causal workload,
+                                // a group sized to span two waves lost 10 % on B4 H16 N4096)
 
-__device__ __forceinline__ void unit_of_block(int block, int bh_total, int units, int& bh, int& unit) {
-  const int full_groups = bh_total / kHeadGroup;
-  const int per_group = kHeadGroup * units;
+__device__ __forceinline__ void unit_of_block(int block, int bh_total, int units, int& bh, int& unit,
+                                              int group = kHeadGroup) {
+  const int full_groups = bh_total / group;
+  const int per_group = group * units;
   int g, size, r;
   if (block < full_groups * per_group) {
     g = block / per_group;
     r = block - g * per_group;
-    size = kHeadGroup;
+    size = group;
   } else {
     g = full_groups;
     r = block - full_groups * per_group;
-    size = bh_total - full_groups * kHeadGroup;
+    size = bh_total - full_groups * group;
   }
-  bh = g * kHeadGroup + r % size;
+  bh = g * group + r % size;
   unit = units - 1 - r / size;
 }
 
