@@ -358,7 +358,6 @@ int prepare(const fa2_fwd_params& a, int units_rows, Prepared& out, const Extent
   p.tma_o = packed ? 0 : 1;   // packed: a box would spill into the next sequence's rows
   p.bh = a.batch * a.heads;
   p.units = (int)units;
-  p.head_group = kHeadGroup;
   p.window_left = a.window_left;
   p.window_right = a.window_right;
   p.prefix = a.prefix_len;

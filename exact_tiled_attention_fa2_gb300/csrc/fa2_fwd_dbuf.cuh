@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(192, 1)
 
   DbufCtx t;
   int bh, q_tile;
-  unit_of_block((int)blockIdx.x, p.bh, p.units, bh, q_tile, p.head_group);
+  unit_of_block((int)blockIdx.x, p.bh, p.units, bh, q_tile);
   // The whole CTA leaves together, before any barrier or TMEM set-up, when
   // its sequence is malformed or shorter than this tile's rows.
   if (!seq_info(p, bh, t.seq)) return;

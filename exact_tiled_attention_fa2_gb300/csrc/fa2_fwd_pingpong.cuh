@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(384, 1)
 
   PairCtx t;
   int bh, pair;
-  unit_of_block((int)blockIdx.x, p.bh, p.units, bh, pair, p.head_group);
+  unit_of_block((int)blockIdx.x, p.bh, p.units, bh, pair);
   // The whole CTA leaves together, before any barrier or TMEM set-up, when
   // its sequence is malformed or shorter than this pair's rows.
   if (!seq_info(p, bh, t.seq)) return;

@@ -37,7 +37,6 @@ struct KernelParams {
   int tma_o;          // 1: O is staged in shared memory and written by TMA stores (unpacked batches)
   int bh;             // B * H
   int units;          // query units (tiles or tile pairs) per (b, h), from n_q
-  int head_group;     // heads per group in the order of units (see unit_of_block)
   int window_left;    // key j visible to query i iff i+off-wl <= j <= i+off+wr
   int window_right;   //   (off = N_k - N_q; -1 = unbounded on that side),
   int prefix;         //   or j < prefix (keys every query sees)
