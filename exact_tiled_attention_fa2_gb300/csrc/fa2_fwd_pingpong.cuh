@@ -27,6 +27,12 @@
 // owner and MMA issuer, warp 9 TMA producer, warps 10-11 idle.  The third
 // warpgroup gives registers to the two softmax warpgroups (setmaxnreg):
 // 2 x 128 x 200 + 128 x 104 = 384 x 168 registers at launch.
+//
+// Masks and lengths are run-time (KeyMask): each tile visits only the key
+// tiles its rows can see, and the two tiles share one stream of them (their
+// ranges overlap or touch); key tiles every row sees skip the element mask.
+// The epilogue stages O in the tile's (then free) Q buffer and writes it
+// with TMA stores (per-row stores for packed batches).
 #pragma once
 
 #include "fa2_common.cuh"

@@ -1,5 +1,6 @@
 /*
- * fa2.h -- C ABI of the GB300 (sm_103a) exact tiled attention forward pass.
+ * fa2.h -- C ABI of the GB300 (sm_103a) exact tiled attention: forward pass,
+ * its backward pass and a decoding-regime forward.
  *
  * The operation (FlashAttention V2 in depth, section 6.1 "Full forward
  * algorithm"; Flash Attention 2 page, "Standard Attention" and "Causal
@@ -14,13 +15,20 @@
  * memory.  LSE is the natural-log logsumexp that section 7.1 keeps for the
  * backward pass.
  *
- * Layouts (all contiguous, row-major):
- *   q, k, v, o : [B, H, N, d] elements of `dtype` (fp16 or bf16)
- *   lse        : [B, H, N] float32
+ * Entry points:
+ *   fa2_fwd / fa2_bwd        contiguous [B, H, N, d] tensors (fp16 or bf16),
+ *                            lse [B, H, N] float32, full or causal attention;
+ *   fa2_fwd_ex / fa2_bwd_ex  any strides, N_q != N_k, band and prefix masks,
+ *                            packed variable-length batches (fa2_fwd_params);
+ *   fa2_decode               up to FA2_DECODE_MAX_Q query rows per sequence
+ *                            against long key sequences (fa2_fwd_params);
+ *   fa2_fwd_host[_noalloc]   the forward on host buffers, end to end.
  *
- * Ownership: the caller owns every buffer.  fa2_fwd allocates no device
- * memory; the library keeps one small device status word per device for
- * reporting kernel-side wait timeouts (see fa2_get_device_status).
+ * Ownership: the caller owns every buffer.  fa2_fwd and fa2_fwd_ex allocate
+ * no device memory; fa2_bwd, fa2_bwd_ex and fa2_decode take a caller
+ * workspace.  The library keeps one small device status word per device for
+ * reporting kernel-side wait timeouts and rejected packed offsets (see
+ * fa2_get_device_status).
  *
  * No C++ exception crosses this interface: every entry point returns an
  * fa2_status code.
@@ -272,8 +280,9 @@ int fa2_get_device_status(void* stream, uint32_t* detail);
  *   other arguments  : as fa2_fwd
  *
  * dK and dV are each written once; dQ is accumulated over key tiles with
- * fp32 reduce-adds in L2 (TMA), so its last bits may vary between runs.  Outputs and
- * workspace must not overlap any input or each other.
+ * fp32 reduce-adds in L2 (TMA), so its last bits may vary between runs.
+ * Outputs and workspace must not overlap any input or each other.  This is
+ * fa2_bwd_ex for contiguous tensors and window (-1, causal ? 0 : -1).
  */
 int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
             void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
