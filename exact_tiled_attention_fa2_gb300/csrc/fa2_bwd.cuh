@@ -28,6 +28,12 @@
 //                                 into the dP^T columns; each warp copies its 32
 //                                 rows out, frees the columns, and TMA adds them
 //
+// At d = 64 the schedule is software-pipelined: S^T of tile i + 1 is issued
+// between dV_i and dK_i (into the columns dV has just read P^T from), so P^T
+// of tile i + 1 is computed while the tensor core finishes tile i, and dQ_i is
+// read out afterwards.  Q_i and dO_i are loaded into separate buffers whose
+// release follows their last reader (dK and dV respectively).
+//
 // Warp roles (384 threads): warps 0-3 and 4-7 are two elementwise warpgroups,
 // each for 64 of the tile's 128 query columns (and half of the d columns of
 // dQ, dK, dV); warp 8 owns TMEM and issues every MMA; warp 9 drives TMA.
@@ -55,16 +61,25 @@ struct BwdConfig {
   static constexpr int TMA_WARP = 9;
   static constexpr uint32_t TILE_BYTES = T * D * 2;
   static constexpr uint32_t DS_BYTES = T * T * 2;    // dS^T, keys x queries, 16-bit
-  static constexpr int QSTAGES = (D == 64) ? 2 : 1;   // Q_i / dO_i buffers (the next tile loads meanwhile)
+  // PIPELINED: S^T of query tile i + 1 is issued between dV_i and dK_i, so
+  // the elementwise warps compute its P^T while the tensor core finishes
+  // tile i.  That needs the next Q tile resident early (two Q buffers) and a
+  // whole tile's dQ staging that TMA reads out while the next tile runs
+  // (reduce-add drains shared memory slowly); both fit at d = 64 only.  At
+  // d = 128 the tile's MMAs run back to back: S^T, dP^T, dV, dK, dQ.
+  static constexpr bool PIPELINED = (D == 64);
+  static constexpr int QSTAGES = PIPELINED ? 2 : 1;    // Q_i buffers
+  static constexpr int DOSTAGES = PIPELINED ? 2 : 1;   // dO_i buffers
+  static constexpr uint32_t DQ_BOX_BYTES = 32 * 32 * 4;       // a 32 x 32 fp32 box (one TMA reduce-add)
   static constexpr uint32_t DQ_WARP_BYTES = 32 * (D / 2) * 4;  // a warp's 32 rows x d/2 fp32 dQ columns
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + TILE_BYTES;
-  static constexpr uint32_t OFF_Q = OFF_V + TILE_BYTES;            // + stage * TILE_BYTES
-  static constexpr uint32_t OFF_DO = OFF_Q + QSTAGES * TILE_BYTES;  // + stage * TILE_BYTES
-  static constexpr uint32_t OFF_DS = OFF_DO + QSTAGES * TILE_BYTES;
-  static constexpr uint32_t OFF_DQ = OFF_DS + DS_BYTES;          // + warp * DQ_WARP_BYTES, 32x32 fp32 boxes
+  static constexpr uint32_t OFF_Q = OFF_V + TILE_BYTES;             // + stage * TILE_BYTES
+  static constexpr uint32_t OFF_DO = OFF_Q + QSTAGES * TILE_BYTES;   // + stage * TILE_BYTES
+  static constexpr uint32_t OFF_DS = OFF_DO + DOSTAGES * TILE_BYTES;
+  static constexpr uint32_t OFF_DQ = OFF_DS + DS_BYTES;             // + warp * DQ_WARP_BYTES, 32x32 fp32 boxes
   static constexpr uint32_t OFF_BAR = OFF_DQ + 8 * DQ_WARP_BYTES;
-  static constexpr uint32_t NUM_BARS = 16;
+  static constexpr uint32_t NUM_BARS = 18;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
   static constexpr uint32_t TMEM_DV = 0;
@@ -85,8 +100,10 @@ enum : int {
   BB_DQEMPTY = 7,  // dQ_i read out of TMEM (8 warp arrivals)
   BB_END = 8,
   BB_EXIT = 9,
-  BB_Q = 10,       // + stage: Q_i and dO_i landed
-  BB_QEMPTY = 12,  // + stage: every MMA reading that stage finished
+  BB_Q = 10,        // + stage: Q_i landed
+  BB_QEMPTY = 12,   // + stage: the MMAs reading Q_i (S^T, dK) finished
+  BB_DO = 14,       // + stage: dO_i landed
+  BB_DOEMPTY = 16,  // + stage: the MMAs reading dO_i (dP^T, dV) finished
 };
 
 struct BwdCtx {
@@ -110,26 +127,39 @@ __device__ __forceinline__ void bwd_producer(const BwdCtx& t, const CUtensorMap*
     tma_load_rows(t.sK + kb * (C::T * 128), tm_k, t.merged, kb * 64, t.seq.row0_k + t.j0, h, b, t.hb, t.bar(BB_KV));
     tma_load_rows(t.sV + kb * (C::T * 128), tm_v, t.merged, kb * 64, t.seq.row0_k + t.j0, h, b, t.hb, t.bar(BB_KV));
   }
-  int loaded = 0;
+  // Q_i into stage i mod QSTAGES once the MMAs of tile i - QSTAGES have read
+  // it, then dO_i likewise; in this order Q runs a tile ahead of dO at d = 128
+  int loaded_q = 0, loaded_do = 0;
   for (int it = 0; it < t.niter; ++it) {
+    const int row = t.seq.row0_q + (t.i0 + it) * C::T;
     const int s = it % C::QSTAGES, u = it / C::QSTAGES;
     if (u > 0 && !wait_or_abort(t.bar(BB_QEMPTY + s), (uint32_t)(u - 1) & 1, t.abort_flag, t.status,
                                 kSiteProducerEmpty))
       break;
-    const int row = t.seq.row0_q + (t.i0 + it) * C::T;
-    mbar_arrive_expect_tx(t.bar(BB_Q + s), 2 * C::TILE_BYTES);
-    for (int kb = 0; kb < C::D / 64; ++kb) {
+    mbar_arrive_expect_tx(t.bar(BB_Q + s), C::TILE_BYTES);
+    for (int kb = 0; kb < C::D / 64; ++kb)
       tma_load_rows(t.sQ + s * C::TILE_BYTES + kb * (C::T * 128), tm_q, t.merged, kb * 64, row, h, b, t.hb,
                     t.bar(BB_Q + s));
-      tma_load_rows(t.sDO + s * C::TILE_BYTES + kb * (C::T * 128), tm_do, t.merged, kb * 64, row, h, b, t.hb,
-                    t.bar(BB_Q + s));
-    }
-    loaded = it + 1;
+    loaded_q = it + 1;
+    const int sd = it % C::DOSTAGES, ud = it / C::DOSTAGES;
+    if (ud > 0 && !wait_or_abort(t.bar(BB_DOEMPTY + sd), (uint32_t)(ud - 1) & 1, t.abort_flag, t.status,
+                                 kSiteProducerEmpty))
+      break;
+    mbar_arrive_expect_tx(t.bar(BB_DO + sd), C::TILE_BYTES);
+    for (int kb = 0; kb < C::D / 64; ++kb)
+      tma_load_rows(t.sDO + sd * C::TILE_BYTES + kb * (C::T * 128), tm_do, t.merged, kb * 64, row, h, b, t.hb,
+                    t.bar(BB_DO + sd));
+    loaded_do = it + 1;
   }
+  // every load in flight lands before the CTA can exit: the last tile of each stage
   wait_drain(t.bar(BB_KV), 0, t.status);
   for (int s = 0; s < C::QSTAGES; ++s) {
-    const int last = loaded - 1 - ((loaded - 1 - s) % C::QSTAGES + C::QSTAGES) % C::QSTAGES;   // last tile in stage s
+    const int last = loaded_q - 1 - ((loaded_q - 1 - s) % C::QSTAGES + C::QSTAGES) % C::QSTAGES;
     if (last >= 0) wait_drain(t.bar(BB_Q + s), (uint32_t)(last / C::QSTAGES) & 1, t.status);
+  }
+  for (int s = 0; s < C::DOSTAGES; ++s) {
+    const int last = loaded_do - 1 - ((loaded_do - 1 - s) % C::DOSTAGES + C::DOSTAGES) % C::DOSTAGES;
+    if (last >= 0) wait_drain(t.bar(BB_DO + s), (uint32_t)(last / C::DOSTAGES) & 1, t.status);
   }
 }
 
@@ -148,21 +178,38 @@ __device__ __forceinline__ void bwd_mma(const BwdCtx& t) {
   const uint64_t ds_mn = make_sdesc_sw128(t.sDS, C::T * 128, 1024);
   const uint32_t tS = t.tmem + C::TMEM_S, tDP = t.tmem + C::TMEM_DP;
   const uint32_t tDV = t.tmem + C::TMEM_DV, tDK = t.tmem + C::TMEM_DK;
-  bool ok = wait_or_abort(t.bar(BB_KV), 0, t.abort_flag, t.status, kSiteMmaK);
-  for (int it = 0; it < t.niter && ok; ++it) {
-    const uint32_t ph = (uint32_t)it & 1;
-    const int qs = it % C::QSTAGES;
-    const uint64_t stage_step = (uint64_t)((qs * C::TILE_BYTES) >> 4);
-    const uint64_t q_kmaj = q_kmaj0 + stage_step, do_kmaj = do_kmaj0 + stage_step;
-    const uint64_t q_mn = q_mn0 + stage_step, do_mn = do_mn0 + stage_step;
-    if (!wait_or_abort(t.bar(BB_Q + qs), (uint32_t)(it / C::QSTAGES) & 1, t.abort_flag, t.status, kSiteMmaQ)) break;
-    tc_fence_after();
+  auto issue_s = [&](int q_stage) {   // S^T = K_j Q_i^T for the Q tile in q_stage
+    const uint64_t q_kmaj = q_kmaj0 + (uint64_t)((q_stage * C::TILE_BYTES) >> 4);
 #pragma unroll
     for (int k = 0; k < C::D / 16; ++k)
       umma_ss(tS, k_kmaj + kmajor_step<C>(k, C::T), q_kmaj + kmajor_step<C>(k, C::T), idesc_s, k > 0 ? 1u : 0u);
     umma_commit(t.bar(BB_S));
+  };
+  bool ok = wait_or_abort(t.bar(BB_KV), 0, t.abort_flag, t.status, kSiteMmaK);
+  if (C::PIPELINED && ok) {
+    ok = wait_or_abort(t.bar(BB_Q), 0, t.abort_flag, t.status, kSiteMmaQ);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0);
+    }
+  }
+  // Tile i: S^T_i (pipelined: issued with tile i - 1), dP^T_i, then, once
+  // P^T_i and dS^T_i are written, dV, [pipelined: S^T of tile i + 1], dK, dQ_i
+  for (int it = 0; it < t.niter && ok; ++it) {
+    const uint32_t ph = (uint32_t)it & 1;
+    const int qs = it % C::QSTAGES, ds = it % C::DOSTAGES;
+    const uint64_t q_step = (uint64_t)((qs * C::TILE_BYTES) >> 4), do_step = (uint64_t)((ds * C::TILE_BYTES) >> 4);
+    const uint64_t do_kmaj = do_kmaj0 + do_step;
+    const uint64_t q_mn = q_mn0 + q_step, do_mn = do_mn0 + do_step;
+    if (!C::PIPELINED) {
+      if (!wait_or_abort(t.bar(BB_Q + qs), (uint32_t)(it / C::QSTAGES) & 1, t.abort_flag, t.status, kSiteMmaQ))
+        break;
+      tc_fence_after();
+      issue_s(qs);
+    }
     // dP^T reuses the columns the previous tile's dQ contribution was read from
     if (it > 0 && !wait_or_abort(t.bar(BB_DQEMPTY), ph ^ 1u, t.abort_flag, t.status, kSiteMmaO)) break;
+    if (!wait_or_abort(t.bar(BB_DO + ds), (uint32_t)(it / C::DOSTAGES) & 1, t.abort_flag, t.status, kSiteMmaQ)) break;
     tc_fence_after();
 #pragma unroll
     for (int k = 0; k < C::D / 16; ++k)
@@ -177,19 +224,30 @@ __device__ __forceinline__ void bwd_mma(const BwdCtx& t) {
       const uint32_t col = (uint32_t)((k >> 2) * 64 + (k & 3) * 8);
       umma_ts(tDV, tS + col, do_mn + (uint64_t)((k * 16 * 128) >> 4), idesc_acc, (it > 0 || k > 0) ? 1u : 0u);
     }
+    umma_commit(t.bar(BB_DOEMPTY + ds));
+    // S^T of the next tile overwrites the P^T columns dV has just read (the
+    // MMAs of one thread execute in order)
+    if (C::PIPELINED && it + 1 < t.niter) {
+      const int qn = (it + 1) % C::QSTAGES;
+      if (!wait_or_abort(t.bar(BB_Q + qn), (uint32_t)((it + 1) / C::QSTAGES) & 1, t.abort_flag, t.status,
+                         kSiteMmaQ))
+        break;
+      tc_fence_after();
+      issue_s(qn);
+    }
 #pragma unroll
     for (int k = 0; k < C::T / 16; ++k) {
       const uint32_t col = (uint32_t)((k >> 2) * 64 + (k & 3) * 8);
       umma_ts(tDK, tDP + col, q_mn + (uint64_t)((k * 16 * 128) >> 4), idesc_acc, (it > 0 || k > 0) ? 1u : 0u);
     }
-    // dQ_i = dS K_j into the dP^T columns (the dK products above read dS^T from
-    // them first: MMAs of one thread execute in order)
+    umma_commit(t.bar(BB_QEMPTY + qs));
+    // dQ_i = dS K_j into the dP^T columns (the dK products above read dS^T
+    // from them first)
 #pragma unroll
     for (int k = 0; k < C::T / 16; ++k)
       umma_ss(tDP, ds_mn + (uint64_t)((k * 16 * 128) >> 4), k_mn + (uint64_t)((k * 16 * 128) >> 4), idesc_dq,
               k > 0 ? 1u : 0u);
     umma_commit(t.bar(BB_DQ));
-    umma_commit(t.bar(BB_QEMPTY + qs));
   }
   if (ok) umma_commit(t.bar(BB_END));
   umma_commit(t.bar(BB_EXIT));
@@ -248,7 +306,7 @@ __device__ __forceinline__ void bwd_elementwise(const BwdCtx& t, const BwdParams
   const uint32_t tS = t.tmem + lane_off + C::TMEM_S + 64 * wg;
   const uint32_t tDP = t.tmem + lane_off + C::TMEM_DP + 64 * wg;
   uint8_t* ds_row = smem + C::OFF_DS + wg * (C::T * 128) + r * 128;     // this key's row of dS^T, block wg
-  uint8_t* dq_stage = smem + C::OFF_DQ + warp * C::DQ_WARP_BYTES;          // this warp's dQ boxes
+  uint8_t* dq_stage = smem + C::OFF_DQ + warp * C::DQ_WARP_BYTES;   // this warp's dQ boxes
   const int n_q = t.seq.n_q;
   const int key = t.j0 + r;
   int key_qlo, key_qhi;                    // the queries this key row is seen by
@@ -262,6 +320,51 @@ __device__ __forceinline__ void bwd_elementwise(const BwdCtx& t, const BwdParams
   const float scale = p.scale;
   const long long lse_base = (long long)t.seq.b * f.l_bs + (long long)t.seq.h * f.l_hs + t.seq.row0_q;
   const long long d_base = (long long)t.hb * f.total_q + t.seq.row0_q;
+  // dQ of query tile iq (its product runs while the next tile's P^T is
+  // computed): read out of TMEM, the columns freed, then added to the fp32
+  // accumulator by TMA from shared memory
+  auto dq_out = [&](int iq) -> bool {
+    bool w = wait_or_abort(t.bar(BB_DQ), (uint32_t)iq & 1, t.abort_flag, t.status, kSiteEpilogueO);
+    w = __all_sync(0xffffffffu, w);
+    if (!w) return false;
+    tc_fence_after();
+    // dQ_i rows: lane = query row of tile i; this warpgroup adds d/2 columns.
+    // Copy them to registers and free the TMEM columns at once, then stage
+    // them in this warp's shared-memory boxes (128-byte swizzle) and let TMA
+    // add the boxes to the fp32 accumulator asynchronously (the dQ product
+    // has read dS^T: its barrier fired).  Rows past the sequence add zeros
+    // (their dS columns are 0).
+    uint32_t dq[C::D / 2];
+#pragma unroll
+    for (int c = 0; c < C::D / 2; c += 32)
+      tmem_ld_32x32b_x32(t.tmem + lane_off + C::TMEM_DP + (C::D / 2) * wg + c, dq + c);
+#pragma unroll
+    for (int c = 0; c < C::D / 2; c += 32) tmem_ld_wait_x32(dq + c);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(t.bar(BB_DQEMPTY));
+    // the previous tile's boxes (staged one tile earlier) were read out
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
+#pragma unroll
+    for (int b = 0; b < C::D / 64; ++b) {
+      uint8_t* row = dq_stage + b * C::DQ_BOX_BYTES + lane * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) * 16)) =
+            make_uint4(dq[32 * b + 4 * c], dq[32 * b + 4 * c + 1], dq[32 * b + 4 * c + 2], dq[32 * b + 4 * c + 3]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      const int y = t.seq.row0_q + (t.i0 + iq) * C::T + quad * 32;   // rows past the tensor are clipped
+#pragma unroll
+      for (int b = 0; b < C::D / 64; ++b)
+        tma_reduce_add_3d(tm_dq, smem_u32(dq_stage + b * C::DQ_BOX_BYTES), (C::D / 2) * wg + 32 * b, y, t.hb);
+      bulk_commit_group();
+    }
+    return true;
+  };
   bool ok = true;
   for (int it = 0; it < t.niter; ++it) {
     const uint32_t ph = (uint32_t)it & 1;
@@ -306,6 +409,12 @@ __device__ __forceinline__ void bwd_elementwise(const BwdCtx& t, const BwdParams
 #pragma unroll
     for (int c = 0; c < 32; ++c) pk[c] = pack2<BF16>(pv[2 * c], pv[2 * c + 1]);
     tmem_st_32x32b_x32(tS, pk);
+    // pipelined: the previous tile's dQ, whose product ran meanwhile; dP^T
+    // of this tile goes into its columns
+    if (C::PIPELINED && it > 0 && !dq_out(it - 1)) {
+      ok = false;
+      break;
+    }
 
     ok = wait_or_abort(t.bar(BB_DP), ph, t.abort_flag, t.status, kSiteSoftmaxO);
     ok = __all_sync(0xffffffffu, ok);
@@ -337,45 +446,12 @@ __device__ __forceinline__ void bwd_elementwise(const BwdCtx& t, const BwdParams
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(t.bar(BB_P));
-
-    ok = wait_or_abort(t.bar(BB_DQ), ph, t.abort_flag, t.status, kSiteEpilogueO);
-    ok = __all_sync(0xffffffffu, ok);
-    if (!ok) break;
-    tc_fence_after();
-    // dQ_i rows: lane = query row of tile i; this warpgroup adds d/2 columns.
-    // Copy them to registers and free the TMEM columns at once, then stage
-    // them in this warp's shared-memory boxes (128-byte swizzle) and let TMA
-    // add the boxes to the fp32 accumulator asynchronously.  Rows past the
-    // sequence add zeros (their dS columns are 0).
-    uint32_t dq[C::D / 2];
-#pragma unroll
-    for (int c = 0; c < C::D / 2; c += 32)
-      tmem_ld_32x32b_x32(t.tmem + lane_off + C::TMEM_DP + (C::D / 2) * wg + c, dq + c);
-#pragma unroll
-    for (int c = 0; c < C::D / 2; c += 32) tmem_ld_wait_x32(dq + c);
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(t.bar(BB_DQEMPTY));
-    if (lane == 0) bulk_wait_read_all();   // the previous tile's boxes were read out
-    __syncwarp();
-#pragma unroll
-    for (int b = 0; b < C::D / 64; ++b) {
-      uint8_t* row = dq_stage + b * 4096 + lane * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) * 16)) =
-            make_uint4(dq[32 * b + 4 * c], dq[32 * b + 4 * c + 1], dq[32 * b + 4 * c + 2], dq[32 * b + 4 * c + 3]);
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      const int y = t.seq.row0_q + (t.i0 + it) * C::T + quad * 32;   // rows past the tensor are clipped
-#pragma unroll
-      for (int b = 0; b < C::D / 64; ++b)
-        tma_reduce_add_3d(tm_dq, smem_u32(dq_stage + b * 4096), (C::D / 2) * wg + 32 * b, y, t.hb);
-      bulk_commit_group();
+    if (!C::PIPELINED && !dq_out(it)) {
+      ok = false;
+      break;
     }
   }
+  if (C::PIPELINED && ok && t.niter > 0) ok = dq_out(t.niter - 1);
   if (lane == 0) bulk_wait_all();   // this warp's reduce-adds performed before the CTA exits
   __syncwarp();
   if (ok && t.niter > 0) {
@@ -473,6 +549,10 @@ __global__ void __launch_bounds__(384, 1)
     for (int s = 0; s < C::QSTAGES; ++s) {
       mbar_init(t.bar(BB_Q + s), 1);
       mbar_init(t.bar(BB_QEMPTY + s), 1);
+    }
+    for (int s = 0; s < C::DOSTAGES; ++s) {
+      mbar_init(t.bar(BB_DO + s), 1);
+      mbar_init(t.bar(BB_DOEMPTY + s), 1);
     }
     mbar_init(t.bar(BB_S), 1);
     mbar_init(t.bar(BB_DP), 1);
