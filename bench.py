@@ -4,7 +4,9 @@ One step = one forward pass (S = QK^T, online softmax, O = PV, LSE) over the
 whole workload, i.e. one launch of the forward kernel through the C ABI.
 Default workload: B=1, H=32, N=16384, d=128, bf16, causal -- the
 long-context batch-1 case the throughput target is set on.  Inputs (403 MB)
-exceed the 129 MB L2, so no flush is needed between steps.
+exceed the 129 MB L2, so no flush is needed between steps; a workload whose
+inputs fit in the L2 is timed launch by launch with the L2 overwritten (a
+258 MB write, outside the timed intervals) before each one.
 
 Prints one JSON line.  ``value`` is forward TFLOP/s (4*B*H*N^2*d, halved for
 causal) with inputs resident in HBM; ``e2e`` is the same metric through the
@@ -37,14 +39,18 @@ if ROOT not in sys.path:
 from exact_tiled_attention_fa2_gb300 import synthetic as sy  # noqa: E402
 
 METRIC = "forward attention TFLOP/s at 1 GB300 and % of dense FP16/BF16 tensor peak"
+L2_BYTES = 129e6          # GB300 L2
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = 4
 KERNEL_SOURCES = ["fa2_common.cuh", "fa2_fwd_pingpong.cuh", "fa2_fwd_dbuf.cuh", "sm103_ptx.cuh", "fa2_internal.h", "fa2_abi.cu"]
 
 
-def kernel_source_hash() -> str:
+BWD_KERNEL_SOURCES = KERNEL_SOURCES + ["fa2_bwd.cuh"]
+
+
+def kernel_source_hash(names=None) -> str:
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in names or KERNEL_SOURCES:
         with open(os.path.join(ROOT, "exact_tiled_attention_fa2_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -70,16 +76,19 @@ def measured_hbm():
         return 6800.0, "of fallback (6.8 TB/s)"
 
 
-def recorded_traffic(workload: int):
-    """DRAM bytes per launch from the committed ncu summary, if it matches this kernel source."""
+def recorded_traffic(workload: int, kernel: str = "fa2_fwd_pingpong_kernel"):
+    """DRAM bytes per launch of `kernel` from the committed ncu summaries, if the
+    record was taken on this kernel source (records without a kernel field are
+    the forward kernel's)."""
     path = os.path.join(ROOT, "profiles", "traffic_per_launch.txt")
     if not os.path.exists(path):
         return None
-    src = kernel_source_hash()
+    src = kernel_source_hash(BWD_KERNEL_SOURCES if kernel == "fa2_bwd_kernel" else KERNEL_SOURCES)
     with open(path) as f:
         for line in f:
             parts = dict(p.split("=", 1) for p in line.split() if "=" in p)
-            if parts.get("kernel_sha") == src and parts.get("workload") == str(workload):
+            if (parts.get("kernel_sha") == src and parts.get("workload") == str(workload)
+                    and parts.get("kernel", "fa2_fwd_pingpong_kernel") == kernel):
                 try:
                     return float(parts["bytes_per_launch"])
                 except (KeyError, ValueError):
@@ -252,17 +261,34 @@ def run_reference(args, w, gen=None):
     return 0
 
 
-def workload_config(w: sy.Workload, n_gpus: int, gen=None):
+def step_input_bytes(w: sy.Workload, gen, backward: bool) -> int:
+    """Bytes a timed step reads as input: q, k, v (backward: also o, dO and L)."""
+    if gen is not None:
+        fwd = gen["input_bytes"]
+        rows_q = w.B * gen["seqlen_q"] * w.H
+    else:
+        fwd = 3 * w.B * w.H * w.N * w.d * 2
+        rows_q = w.B * w.H * w.N
+    return fwd + (rows_q * (2 * w.d * 2 + 4) if backward else 0)
+
+
+def l2_note(in_bytes: int, flush: bool) -> str:
+    if flush:
+        return ("inputs (%.0f MB) not larger than the 129 MB L2: L2 overwritten (a %.0f MB write) before each "
+                "timed launch, launches timed one by one" % (in_bytes / 1e6, 2 * L2_BYTES / 1e6))
+    return "inputs (%.0f MB) larger than the 129 MB L2; no flush" % (in_bytes / 1e6)
+
+
+def workload_config(w: sy.Workload, n_gpus: int, gen=None, l2: str = ""):
     c = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
          "dtype": "bf16" if w.dtype == sy.BF16 else "fp16", "causal": w.causal,
          "scale": "1/sqrt(d)", "q_scale": w.q_scale,
-         "l2": "inputs (%.0f MB) larger than the 129 MB L2; no flush" % (3 * w.B * w.H * w.N * w.d * 2 / 1e6),
+         "l2": l2 or l2_note(step_input_bytes(w, gen, False), False),
          "parallelism": "replicas x%d" % n_gpus, "seed": w.seed(0)}
     if gen is not None:
         c["workload"] = w.name + " " + gen["label"]
         c["causal"] = None
         c["mask"] = {k: gen[k] for k in ("window_left", "window_right", "prefix", "seqlen_k", "layout", "varlen_seqs")}
-        c["l2"] = "inputs (%.0f MB) vs the 129 MB L2; no flush" % (gen["input_bytes"] / 1e6)
     return c
 
 
@@ -411,6 +437,8 @@ def main():
     ap.add_argument("--kernel-only", action="store_true", help="skip the end-to-end and CPU-baseline legs")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps one by one instead of replaying them from a CUDA graph")
+    ap.add_argument("--flush-l2", choices=["auto", "on", "off"], default="auto",
+                    help="overwrite the L2 before each timed launch (auto: when the inputs fit in it)")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (fa2_bwd) instead: 2.5x the forward FLOPs (five products)")
     g = ap.add_argument_group("general forward (fa2_fwd_ex); FLOPs then count 4*d per visible (query, key) pair")
@@ -488,6 +516,14 @@ def main():
     if code != fa2.FA2_OK:
         raise RuntimeError("device status %d (0x%x) after warm-up" % (code, detail))
 
+    # inputs that fit in the L2 would be timed warm: overwrite the L2 before
+    # every timed launch instead, outside the launch's own timing events
+    in_bytes = step_input_bytes(w, gen, args.backward)
+    flush = args.flush_l2 == "on" or (args.flush_l2 == "auto" and in_bytes <= L2_BYTES)
+    fbuf = None
+    if flush:
+        args.no_graph = True
+        fbuf = torch.empty(int(2 * L2_BYTES), dtype=torch.uint8, device=dev)
     graph = None
     if not args.no_graph:
         # K forward launches captured once and replayed: the timed region then
@@ -511,6 +547,8 @@ def main():
                 graph.replay()
             else:
                 for i in range(args.steps):
+                    if fbuf is not None:
+                        fbuf.zero_()
                     starts[i].record(stream)
                     step()
                     ends[i].record(stream)
@@ -522,6 +560,8 @@ def main():
         kernel_ms = [elapsed_ms / args.steps] * args.steps
     else:
         kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if fbuf is not None:
+        elapsed_ms = sum(kernel_ms)   # the flushes between launches are not the workload's time
     code, detail = fa2.fa2_get_device_status(stream)
     if code != fa2.FA2_OK:
         raise RuntimeError("device status %d (0x%x) in timed region" % (code, detail))
@@ -572,19 +612,21 @@ def main():
 
     if rank == 0:
         clk = clocks.summary()
+        kname = ("fa2_bwd_kernel" if args.backward else
+                 "fa2_fwd_pingpong_kernel" if w.d <= 128 else "fa2_fwd_dbuf_kernel")
         line = {
             "metric": METRIC if not args.backward else
             "backward attention TFLOP/s at 1 GB300 (2.5x the forward FLOPs) and % of dense FP16/BF16 tensor peak",
             "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == sy.BF16 else "fp16",
-            "data": "synthetic", "config": dict(workload_config(w, ws, gen), launch=launch_mode(args)),
+            "data": "synthetic",
+            "config": dict(workload_config(w, ws, gen, l2_note(in_bytes, flush)), launch=launch_mode(args)),
             "pct_of_peak": 100.0 * value / ws / peak,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                          "frac": achieved / peak,
-                         "traffic": recorded_traffic(args.workload) if gen is None else None,
-                         "peak_source": peak_note, "kernel": ("fa2_bwd_kernel" if args.backward else
-                                    "fa2_fwd_pingpong_kernel" if w.d <= 128 else "fa2_fwd_dbuf_kernel"),
+                         "traffic": recorded_traffic(args.workload, kname) if gen is None else None,
+                         "peak_source": peak_note, "kernel": kname,
                          "avg_launch_ms": avg_launch_ms,
                          "algorithmic_flops_per_launch": flops,
                          "algorithmic_bytes_per_launch": (w.algorithmic_bytes() if gen is None else gen["bytes"]) *
@@ -592,7 +634,7 @@ def main():
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                        "samples": clk["samples"]},
             "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": args.steps * (3 if args.backward else 1),
-            "kernel_sha": kernel_source_hash(),
+            "kernel_sha": kernel_source_hash(BWD_KERNEL_SOURCES if args.backward else KERNEL_SOURCES),
         }
         if gen is not None and gen["decode_rows"]:
             # HBM-bound: K and V read once dominate; roofline against the measured copy bandwidth
