@@ -346,7 +346,9 @@ __device__ __forceinline__ void store_staged_rows(const CUtensorMap* tm_o, const
       tma_store_rows(tm_o, merged, sO + (uint32_t)kb * (128u * 128u) + (uint32_t)quad * (32u * 128u), kb * 64,
                      s.row0_q + q0 + quad * 32, s.h, s.b, hb);
     bulk_commit_group();
-    bulk_wait_all();
+    // the staging must outlive only TMA's read of it: the writes to global
+    // memory complete with the grid
+    bulk_wait_read_all();
   }
   __syncwarp();
 }

@@ -107,20 +107,26 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 }
 
 template <class C>
+// Producer.  `first` = true issues what needs no wait -- the Q tiles and the
+// first STAGES key/value tiles -- (the kernel does this before its set-up
+// barrier, so the loads fly while TMEM is allocated); `first` = false issues
+// the rest and then waits for every load in flight to land.
 __device__ __forceinline__ void pp_producer(const PairCtx& t, const KernelParams& p, const CUtensorMap* tm_q,
-                                            const CUtensorMap* tm_k, const CUtensorMap* tm_v) {
+                                            const CUtensorMap* tm_k, const CUtensorMap* tm_v, bool first) {
   const int h = t.seq.h, b = t.seq.b, hb = b * p.heads + h;
   const bool merged = p.merged_bh != 0;
-  for (int q = 0; q < C::NQ; ++q) {
-    if (t.nkv[q] == 0) continue;
-    mbar_arrive_expect_tx(t.bar(PB_Q + q), C::Q_BYTES);
-    for (int kb = 0; kb < C::D / 64; ++kb)
-      tma_load_rows(t.sQ + q * C::Q_BYTES + kb * (C::BR * 128), tm_q, merged, kb * 64, t.seq.row0_q + t.q0[q], h, b,
-                    hb, t.bar(PB_Q + q));
+  if (first) {
+    for (int q = 0; q < C::NQ; ++q) {
+      if (t.nkv[q] == 0) continue;
+      mbar_arrive_expect_tx(t.bar(PB_Q + q), C::Q_BYTES);
+      for (int kb = 0; kb < C::D / 64; ++kb)
+        tma_load_rows(t.sQ + q * C::Q_BYTES + kb * (C::BR * 128), tm_q, merged, kb * 64, t.seq.row0_q + t.q0[q], h,
+                      b, hb, t.bar(PB_Q + q));
+    }
   }
   int last_use[C::STAGES];
-  for (int s = 0; s < C::STAGES; ++s) last_use[s] = -1;
-  for (int u = 0; u < t.nu; ++u) {
+  for (int s = 0; s < C::STAGES; ++s) last_use[s] = s < t.nu ? s / C::STAGES : -1;   // the first pass's stages
+  for (int u = first ? 0 : C::STAGES; u < (first ? min(t.nu, C::STAGES) : t.nu); ++u) {
     const int s = u % C::STAGES;
     const int w = u / C::STAGES;
     if (w > 0 && !wait_or_abort(t.bar(PB_KVEMPTY + s), (w - 1) & 1, t.abort_flag, t.status, kSiteProducerEmpty))
@@ -136,6 +142,7 @@ __device__ __forceinline__ void pp_producer(const PairCtx& t, const KernelParams
                     t.bar(PB_VFULL + s));
     last_use[s] = w;
   }
+  if (first) return;
   for (int q = 0; q < C::NQ; ++q)
     if (t.nkv[q] > 0) wait_drain(t.bar(PB_Q + q), 0, t.status);
   for (int s = 0; s < C::STAGES; ++s) {
@@ -447,7 +454,7 @@ __global__ void __launch_bounds__(384, 1)
     t.tm[q] = t.tm[q].from(t.kv0);
   }
 
-  if (threadIdx.x == 0) {
+  if (warp == C::TMA_WARP && lane == 0) {
     for (int q = 0; q < C::NQ; ++q) {
       mbar_init(t.bar(PB_Q + q), 1);
       mbar_init(t.bar(PB_S + q), 1);
@@ -464,12 +471,12 @@ __global__ void __launch_bounds__(384, 1)
     facts->seq = t.seq;
     facts->km = t.km;
     fence_mbar_init();
-  }
-  if (warp == C::TMA_WARP && lane == 0) {
+    fence_proxy_async_smem();   // the initialised barriers, before this thread's own TMA loads signal them
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_o);
+    pp_producer<C>(t, p, &tm_q, &tm_k, &tm_v, true);
   }
   if (warp == C::MMA_WARP) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -483,7 +490,7 @@ __global__ void __launch_bounds__(384, 1)
   if (warp >= 8) {
     regs_decrease<C::REGS_OTHER>();
     if (warp == C::TMA_WARP) {
-      if (lane == 0) pp_producer<C>(t, p, &tm_q, &tm_k, &tm_v);
+      if (lane == 0) pp_producer<C>(t, p, &tm_q, &tm_k, &tm_v, false);
     } else if (warp == C::MMA_WARP) {
       if (lane == 0) pp_mma<C, BF16, BAND>(t);
       __syncwarp();
