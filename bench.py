@@ -316,8 +316,11 @@ def general_mask(args, w: sy.Workload):
         label += " varlen%d" % args.varlen_seqs
     if args.decode_rows:
         label = "decode %d row%s vs %d keys " % (nq, "s" if nq > 1 else "", nk) + label
-    rows_q, rows_k = w.B * nq, w.B * nk    # per head
-    inputs = (rows_q + 2 * rows_k) * w.H * w.d * 2
+    rows_q = w.B * nq    # per head
+    # K and V rows a pass must read: the keys some query row sees (a bounded
+    # window reads only its band); packed sequences count every key
+    kv_rows = w.B * (nk if args.varlen_seqs else sy.union_visible_keys(nq, nk, wl, wr, args.prefix))
+    inputs = (rows_q + 2 * kv_rows) * w.H * w.d * 2
     return {"window_left": wl, "window_right": wr, "prefix": args.prefix, "seqlen_k": nk, "layout": args.layout,
             "varlen_seqs": args.varlen_seqs, "decode_rows": args.decode_rows, "seqlen_q": nq, "label": label,
             "input_bytes": inputs,
@@ -542,6 +545,10 @@ def main():
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
+            if graph is None:
+                # launched one by one: keep the GPU busy while the host enqueues
+                # them, so no launch waits on the host inside its own events
+                torch.cuda._sleep(int(4e5 * args.steps))
             t0.record(stream)
             if graph is not None:
                 graph.replay()

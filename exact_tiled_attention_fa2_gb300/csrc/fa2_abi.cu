@@ -127,6 +127,7 @@ struct MapCache {
 };
 thread_local MapCache t_maps;
 thread_local MapCache t_decode_maps;
+thread_local MapCache t_decode_tc_maps;
 
 // K and V maps of the decode kernel: whole rows (d columns) x
 // decode_block_rows(d) rows per box, no swizzle (rows land contiguously).
@@ -157,6 +158,31 @@ int cached_maps(LaunchArgs& a, const MapKey& key) {
     const TileGeometry g = tile_geometry(key.d);
     CUtensorMap* maps[4] = {&c.tm_q, &c.tm_k, &c.tm_v, &c.tm_o};
     const int rows[4] = {g.q_rows, g.kv_rows, g.kv_rows, 32};   // o: one warp's 32 rows per box
+    c.valid = false;
+    for (int i = 0; i < 4; ++i) {
+      if (encode_map_rows(maps[i], key.ptr[i], key.d, key.dims[i][0], key.dims[i][1], key.dims[i][2],
+                          key.strides[i], rows[i], bf16, key.merged != 0))
+        return FA2_ERR_CUDA;
+    }
+    std::memcpy(&c.key, &key, sizeof(MapKey));
+    c.valid = true;
+  }
+  a.tm_q = c.tm_q;
+  a.tm_k = c.tm_k;
+  a.tm_v = c.tm_v;
+  a.tm_o = c.tm_o;
+  return FA2_OK;
+}
+
+// Maps of the tensor-core decode path (the double-buffered kernel at d <= 128):
+// q boxes of 128 rows, k and v boxes of 64 rows, o boxes of 32 rows (o is not
+// stored through in split-key mode, but every map the kernel prefetches is valid).
+int cached_decode_tc_maps(LaunchArgs& a, const MapKey& key) {
+  MapCache& c = t_decode_tc_maps;
+  if (!(c.valid && std::memcmp(&c.key, &key, sizeof(MapKey)) == 0)) {
+    const bool bf16 = key.dtype == FA2_BF16;
+    CUtensorMap* maps[4] = {&c.tm_q, &c.tm_k, &c.tm_v, &c.tm_o};
+    const int rows[4] = {128, 64, 64, 32};
     c.valid = false;
     for (int i = 0; i < 4; ++i) {
       if (encode_map_rows(maps[i], key.ptr[i], key.d, key.dims[i][0], key.dims[i][1], key.dims[i][2],
@@ -395,9 +421,12 @@ int forward(const fa2_fwd_params& a_in, cudaStream_t stream) {
 // split shorter than kDecodeMinChunk keys, chunks a multiple of a stage.
 constexpr long long kDecodeTargetCtas = 2 * 152;
 constexpr long long kDecodeMinChunk = 256;
+// From this many query rows on (d = 64 / 128, unpacked) the chunks run on the
+// tensor cores; fewer rows stay on the CUDA-core decode kernel.
+constexpr int kDecodeTcMinRows = 2;
 
 struct DecodePlan {
-  int splits, chunk;
+  int splits, chunk, base;
   size_t ws_o_bytes, ws_ml_bytes;
 };
 
@@ -409,16 +438,27 @@ int decode_plan(const fa2_fwd_params& a, DecodePlan& out) {
   const long long bh = (long long)a.batch * a.heads;
   const long long nk = a.seqlen_k;
   const long long block = decode_block_rows(a.head_dim);
+  // Keys before the first one query row 0 sees (a bounded left window, no
+  // prefix) are seen by no row: the chunks start at that key, rounded down to
+  // a stage.  Packed sequences differ in length: their chunks start at 0.
+  long long base = 0;
+  const bool packed = a.cu_seqlens_q != nullptr;
+  if (!packed && a.window_left >= 0 && a.prefix_len <= 0) {
+    const long long first = nk - a.seqlen_q - a.window_left;
+    if (first > 0) base = (first < nk ? first : nk - 1) / block * block;
+  }
+  const long long span = nk - base;
   long long splits = kDecodeTargetCtas / bh;
-  const long long useful = (nk + kDecodeMinChunk - 1) / kDecodeMinChunk;
+  const long long useful = (span + kDecodeMinChunk - 1) / kDecodeMinChunk;
   if (splits > useful) splits = useful;
   if (splits < 1) splits = 1;
-  long long chunk = (nk + splits - 1) / splits;
+  long long chunk = (span + splits - 1) / splits;
   chunk = (chunk + block - 1) / block * block;
-  splits = (nk + chunk - 1) / chunk;
+  splits = (span + chunk - 1) / chunk;
   if (bh * splits > INT_MAX || bh * a.seqlen_q > INT_MAX) return FA2_ERR_UNSUPPORTED;
   out.splits = (int)splits;
   out.chunk = (int)chunk;
+  out.base = (int)base;
   const size_t slots = (size_t)bh * (size_t)a.seqlen_q * (size_t)splits;
   out.ws_o_bytes = align256(slots * (size_t)a.head_dim * 4);
   out.ws_ml_bytes = align256(slots * 2 * 4);
@@ -439,6 +479,27 @@ int decode(const fa2_fwd_params& a_in, void* workspace, size_t workspace_bytes, 
   rc = prepare(a, FA2_DECODE_MAX_Q, pr, &ew);
   if (rc) return rc;
   const bool packed = a.cu_seqlens_q != nullptr;
+  if (!packed && a.seqlen_q >= kDecodeTcMinRows && (a.head_dim == 64 || a.head_dim == 128)) {
+    // one query tile (N_q <= 8) per (b, h), split into the plan's key chunks
+    // (a multiple of the kernel's 64-row key tile)
+    LaunchArgs tl;
+    std::memset(&tl, 0, sizeof(tl));
+    rc = cached_decode_tc_maps(tl, pr.key);
+    if (rc) return rc;
+    tl.p = pr.p;
+    tl.p.tma_o = 0;
+    tl.p.units = plan.splits;
+    tl.p.splits = plan.splits;
+    tl.p.split_chunk = plan.chunk;
+    tl.p.split_base = plan.base;
+    tl.p.ws_o = static_cast<float*>(workspace);
+    tl.p.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.ws_o_bytes);
+    tl.bf16 = a.dtype == FA2_BF16;
+    tl.band = pr.band;
+    tl.stream = stream;
+    const int e = a.head_dim == 64 ? launch_decode_tc_d64(tl) : launch_decode_tc_d128(tl);
+    return e == 0 ? FA2_OK : FA2_ERR_CUDA;
+  }
   DecodeLaunchArgs la;
   std::memset(&la, 0, sizeof(la));
   rc = cached_decode_maps(la, pr.key);
@@ -451,6 +512,7 @@ int decode(const fa2_fwd_params& a_in, void* workspace, size_t workspace_bytes, 
   la.p.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.ws_o_bytes);
   la.p.splits = plan.splits;
   la.p.chunk = plan.chunk;
+  la.p.base = plan.base;
   la.p.f = pr.p;
   la.p.f.n_k = a.seqlen_k;   // packed: the longest sequence's key count the plan covers
   la.bf16 = a.dtype == FA2_BF16;

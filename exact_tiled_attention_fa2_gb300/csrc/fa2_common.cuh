@@ -365,6 +365,41 @@ __device__ __forceinline__ void store_empty_row(const KernelParams& p, const Seq
   p.lse[(long long)s.b * p.l_bs + (long long)s.h * p.l_hs + s.row0_q + row] = -INFINITY;
 }
 
+// Split-key mode: a row's partial over one key chunk -- O~ (unnormalised,
+// read from TMEM columns tO.. when `have`, else zeros), m (exp2 domain) and
+// l -- into workspace slot (bh * n_q + row) * splits + split, the layout the
+// decode merge kernel reads.  Every lane of the warp takes part in the TMEM
+// loads (`have` is the same for the whole warp); rows past the sequence store
+// nothing.
+template <int D>
+__device__ __forceinline__ void store_partial_row(const KernelParams& p, int bh, int split, int row, int n_q,
+                                                  uint32_t tO, float m, float l, bool have) {
+  const bool live = row < n_q;
+  const size_t slot = ((size_t)bh * (size_t)p.n_q + (size_t)row) * (size_t)p.splits + (size_t)split;
+  float4* dst = reinterpret_cast<float4*>(p.ws_o + slot * D);
+#pragma unroll 1
+  for (int c = 0; c < D; c += 32) {
+    uint32_t o[32];
+    if (have) {
+      tmem_ld_32x32b_x32(tO + c, o);
+      tmem_ld_wait_x32(o);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[i] = 0u;
+    }
+    if (live) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        dst[c / 4 + i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                                     __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+    }
+  }
+  if (live) {
+    p.ws_ml[slot * 2] = m;
+    p.ws_ml[slot * 2 + 1] = l;
+  }
+}
+
 // Order of work units over a 1-D grid of (B*H) x units blocks.  Heads go in
 // groups of `group`; inside a group the units run from the last (the one
 // with the most key tiles under a causal mask) to the first, heads

@@ -12,6 +12,9 @@
 // M = max m_c, l = sum 2^(m_c - M) l_c, O = sum 2^(m_c - M) O~_c / l (Lesson
 // 6.6, "Online softmax"; FlashAttention V2 in depth, section 3.2).  Lesson
 // 6.6 ("Common misconceptions") names this regime as needing its own kernel.
+// This CUDA-core kernel serves one query row, packed batches and d = 256; from
+// two rows on at d = 64 / 128 the tiled tensor-core kernel reduces the chunks
+// (fa2_decode_tc.cuh), since the per-key products grow with the rows.
 //
 // Per CTA: a TMA warp streams [BLOCK x d] boxes of K and V through a 3-stage
 // shared-memory ring; four compute warps each take BLOCK/4 keys of a stage.
@@ -36,6 +39,7 @@ struct DecodeParams {
   float* ws_ml;                  // [B*H][n_q][splits][2] partial (m, l), exp2 domain
   int splits;                    // key chunks per (b, h)
   int chunk;                     // keys per chunk (a multiple of the stage size)
+  int base;                      // first key of chunk 0: keys before it are seen by no row
   KernelParams f;                // outputs, offsets, sizes, mask, scale (as the tiled kernels)
 };
 
@@ -103,11 +107,12 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 
 // The chunk of keys [c0, c1) one CTA reduces, within a sequence, clipped to
 // the keys some query row sees; false if empty.
-__device__ __forceinline__ bool decode_range(const KeyMask& km, int n_q, int split, int chunk, int& c0, int& c1) {
+__device__ __forceinline__ bool decode_range(const KeyMask& km, int n_q, int split, int chunk, int base, int& c0,
+                                             int& c1) {
   int lo, end;
   if (!km.tile_range<true>(0, n_q - 1, lo, end)) return false;
-  c0 = max(lo, split * chunk);
-  c1 = min(end, min(km.n_k, (split + 1) * chunk));
+  c0 = max(lo, base + split * chunk);
+  c1 = min(end, min(km.n_k, base + (split + 1) * chunk));
   return c1 > c0;
 }
 
@@ -339,7 +344,7 @@ __global__ void __launch_bounds__(DecodeConfig<D>::THREADS, 2)
   const int split = (int)blockIdx.x - bh * dp.splits;
   SeqInfo seq;
   if (!seq_info(p, bh, seq)) return;
-  if (seq.n_k > dp.splits * dp.chunk) {   // a packed sequence longer than the split plan covers
+  if (seq.n_k > dp.base + dp.splits * dp.chunk) {   // a packed sequence longer than the split plan covers
     if (threadIdx.x == 0 && split == 0) atomicOr(p.status, kStatusBadSeqlens);
     return;
   }
@@ -347,7 +352,7 @@ __global__ void __launch_bounds__(DecodeConfig<D>::THREADS, 2)
   if (n_q == 0) return;
   const KeyMask km = key_mask(p, seq);
   int c0 = 0, c1 = 0;
-  const bool empty = !decode_range(km, n_q, split, dp.chunk, c0, c1);
+  const bool empty = !decode_range(km, n_q, split, dp.chunk, dp.base, c0, c1);
   const int nblk = empty ? 0 : (c1 - c0 + C::BLOCK - 1) / C::BLOCK;
 
   if (threadIdx.x == 0) {
@@ -413,7 +418,7 @@ __global__ void __launch_bounds__(128)
   const int r = (int)blockIdx.x - bh * p.n_q;
   SeqInfo seq;
   if (!seq_info(p, bh, seq)) return;   // the decode kernel has already reported it
-  if (r >= seq.n_q || seq.n_k > dp.splits * dp.chunk) return;
+  if (r >= seq.n_q || seq.n_k > dp.base + dp.splits * dp.chunk) return;
   const size_t slot0 = ((size_t)bh * p.n_q + r) * dp.splits;
   float M = -INFINITY;
   for (int s = 0; s < dp.splits; ++s) M = fmaxf(M, dp.ws_ml[(slot0 + s) * 2]);

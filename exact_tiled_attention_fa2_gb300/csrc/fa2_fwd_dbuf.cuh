@@ -18,6 +18,12 @@
 //
 // Warp roles (192 threads): warps 0-3 softmax + epilogue (one thread per
 // query row = TMEM lane), warp 4 TMEM owner and MMA issuer, warp 5 TMA.
+//
+// The same kernel at d = 64 / 128 (256 TMEM columns, ~100 KB of shared
+// memory: two CTAs per SM) serves decoding in split-key mode
+// (KernelParams::splits > 1): a unit is a (query tile, key chunk) pair, the
+// tile's key range is clipped to the chunk, and each row's partial (m, l, O~)
+// is written for the decode merge kernel instead of O and LSE.
 #pragma once
 
 #include "fa2_fwd_pingpong.cuh"
@@ -46,10 +52,13 @@ struct DbufConfig {
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;
   static constexpr uint32_t TMEM_S = 0;     // + 64 * buffer
   static constexpr uint32_t TMEM_O = 128;
-  static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(D == 256, "double-buffered-S kernel: head dim 256");
+  static constexpr uint32_t TMEM_COLS = (D == 256) ? 512 : 256;
+  static constexpr int CTAS_PER_SM = (D == 256) ? 1 : 2;   // TMEM and shared memory allow two below d = 256
+  static_assert(D == 64 || D == 128 || D == 256, "double-buffered-S kernel: head dim 64, 128 or 256");
   static_assert(TMEM_O + D <= TMEM_COLS, "tensor memory");
+  static_assert(CTAS_PER_SM * TMEM_COLS <= 512, "tensor memory per SM");
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+  static_assert(CTAS_PER_SM * (SMEM_BYTES + 1024) <= 233472, "shared memory per SM");
 };
 
 enum : int {
@@ -78,6 +87,7 @@ struct DbufCtx {
   int q0;    // first query row of the tile
   int kv0;   // first key tile the tile visits
   int nkv;   // key tiles it visits (0: none)
+  int bh, split;  // split-key mode: the (b, h) slice and key chunk of the partials
   TileMask tm;    // unmasked key tiles, by index counted from kv0
   bool few_keys;  // N_k <= 2 key tiles: every bf16 P is split
   __device__ __forceinline__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
@@ -206,14 +216,17 @@ __device__ __forceinline__ void db_mma(const DbufCtx& t) {
   wait_drain(t.bar(DB_EXIT), 0, t.status);
 }
 
-template <class C, bool BF16, bool BAND>
+template <class C, bool BF16, bool BAND, bool SPLIT>
 __device__ __forceinline__ void db_softmax(const DbufCtx& t, const KernelParams& p, const CtaFacts* facts, int warp,
                                            int lane, const CUtensorMap* tm_o) {
   const int quad = warp & 3;
   const int r = quad * 32 + lane;
   const int row = t.q0 + r;
   if (t.nkv == 0) {
-    store_empty_row<C::D>(p, t.seq, row);
+    if (SPLIT)
+      store_partial_row<C::D>(p, t.bh, t.split, row, t.seq.n_q, 0u, -INFINITY, 0.f, false);
+    else
+      store_empty_row<C::D>(p, t.seq, row);
     return;
   }
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
@@ -297,7 +310,9 @@ __device__ __forceinline__ void db_softmax(const DbufCtx& t, const KernelParams&
   }
   if (!ok) return;
   tc_fence_after();
-  if (p.tma_o) {
+  if (SPLIT) {
+    store_partial_row<C::D>(p, t.bh, t.split, row, t.seq.n_q, tO, m_run, l_run, true);
+  } else if (p.tma_o) {
     // the Q buffer is free: the last S product completed before DB_OLAST
     stage_row<C::D, BF16>(p, facts->seq, row, r, t.sQ, tO, m_run, l_run);
     store_staged_rows<C::D>(tm_o, p, facts->seq, t.sQ, t.q0, quad, lane);
@@ -307,9 +322,10 @@ __device__ __forceinline__ void db_softmax(const DbufCtx& t, const KernelParams&
 }
 
 // BAND: the first key a query row sees may depend on the row (a bounded left
-// window or a prefix); it selects the element mask's form.
-template <int D, bool BF16, bool BAND>
-__global__ void __launch_bounds__(192, 1)
+// window or a prefix); it selects the element mask's form.  SPLIT: split-key
+// mode (decoding; p.splits > 1), instantiated for the decode path only.
+template <int D, bool BF16, bool BAND, bool SPLIT = false>
+__global__ void __launch_bounds__(192, DbufConfig<D>::CTAS_PER_SM)
     fa2_fwd_dbuf_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                         const KernelParams p) {
@@ -326,8 +342,12 @@ __global__ void __launch_bounds__(192, 1)
   const int lane = (int)(threadIdx.x & 31);
 
   DbufCtx t;
-  int bh, q_tile;
-  unit_of_block((int)blockIdx.x, p.bh, p.units, bh, q_tile);
+  int bh, unit;
+  unit_of_block((int)blockIdx.x, p.bh, p.units, bh, unit);
+  const int splits = SPLIT ? p.splits : 1;
+  const int q_tile = unit / splits;
+  t.bh = bh;
+  t.split = unit - q_tile * splits;
   // The whole CTA leaves together, before any barrier or TMEM set-up, when
   // its sequence is malformed or shorter than this tile's rows.
   if (!seq_info(p, bh, t.seq)) return;
@@ -342,7 +362,13 @@ __global__ void __launch_bounds__(192, 1)
   t.km = key_mask(p, t.seq);
   const int last = min(t.q0 + C::BR, t.seq.n_q) - 1;
   int lo, end;
-  if (t.km.template tile_range<BAND>(t.q0, last, lo, end)) {
+  bool any = t.km.template tile_range<BAND>(t.q0, last, lo, end);
+  if (SPLIT && any) {   // the chunk's keys only (chunks are whole key tiles)
+    lo = max(lo, p.split_base + t.split * p.split_chunk);
+    end = min(end, p.split_base + (t.split + 1) * p.split_chunk);
+    any = lo < end;
+  }
+  if (any) {
     t.kv0 = lo / C::BC;
     t.nkv = (end + C::BC - 1) / C::BC - t.kv0;
   } else {
@@ -395,7 +421,7 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) db_mma<C, BF16>(t);
     __syncwarp();
   } else {
-    db_softmax<C, BF16, BAND>(t, p, facts, warp, lane, &tm_o);
+    db_softmax<C, BF16, BAND, SPLIT>(t, p, facts, warp, lane, &tm_o);
   }
   tc_fence_before();
   __syncthreads();
@@ -405,10 +431,10 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-template <int D, bool BF16, bool BAND>
+template <int D, bool BF16, bool BAND, bool SPLIT = false>
 int launch_fwd_dbuf(const LaunchArgs& a) {
   using C = DbufConfig<D>;
-  auto kern = fa2_fwd_dbuf_kernel<D, BF16, BAND>;
+  auto kern = fa2_fwd_dbuf_kernel<D, BF16, BAND, SPLIT>;
   static std::atomic<unsigned long long> configured{0};
   const int e = once_per_device(configured, [&]() -> int {
     return (int)cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);

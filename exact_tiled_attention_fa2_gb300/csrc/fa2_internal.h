@@ -41,6 +41,14 @@ struct KernelParams {
   int window_right;   //   (off = N_k - N_q; -1 = unbounded on that side),
   int prefix;         //   or j < prefix (keys every query sees)
   float scale_log2;   // scale * log2(e): scores go to the exp2 domain
+  // Split-key mode of the double-buffered kernel (decoding): a unit is a
+  // (query tile, key chunk) pair, and each row's partial (m, l, O~) goes to
+  // ws_ml / ws_o in the decode merge kernel's layout instead of O and LSE.
+  int splits;         // key chunks per (b, h); 0 or 1: whole rows
+  int split_chunk;    // keys per chunk, a multiple of the key tile
+  int split_base;     // first key of chunk 0 (a multiple of the key tile)
+  float* ws_o;        // [B*H][n_q][splits][d] partial O~
+  float* ws_ml;       // [B*H][n_q][splits][2] partial (m, l), exp2 domain
 };
 
 // Bit of the status word a forward kernel sets when a packed batch's row
@@ -126,5 +134,11 @@ struct DecodeLaunchArgs;
 int launch_decode_d64(const DecodeLaunchArgs& a);
 int launch_decode_d128(const DecodeLaunchArgs& a);
 int launch_decode_d256(const DecodeLaunchArgs& a);
+// Decoding on the tensor cores (3 or more query rows, d = 64 / 128, unpacked):
+// the double-buffered forward kernel in split-key mode, then the decode merge
+// kernel.  `a.p` carries the split fields; maps: q boxes of 128 rows, k and v
+// boxes of 64 rows.
+int launch_decode_tc_d64(const LaunchArgs& a);
+int launch_decode_tc_d128(const LaunchArgs& a);
 
 }  // namespace fa2

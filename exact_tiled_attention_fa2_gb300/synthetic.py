@@ -168,6 +168,23 @@ def visible_keys(Nq: int, Nk: int, window_left: int = -1, window_right: int = -1
     return band + pre - overlap
 
 
+def union_visible_keys(Nq: int, Nk: int, window_left: int = -1, window_right: int = -1, prefix: int = 0) -> int:
+    """Keys that at least one of the Nq query rows sees (same mask as
+    visible_keys): the keys whose K and V rows a pass must read.  Counted with
+    a difference array over the rows' bands, plus the prefix."""
+    i = np.arange(Nq, dtype=np.int64)
+    off = Nk - Nq
+    lo = np.zeros(Nq, np.int64) if window_left < 0 else np.clip(i + off - window_left, 0, Nk)
+    hi = np.full(Nq, Nk - 1, np.int64) if window_right < 0 else np.clip(i + off + window_right, -1, Nk - 1)
+    live = hi >= lo
+    diff = np.zeros(Nk + 1, np.int64)
+    np.add.at(diff, lo[live], 1)
+    np.add.at(diff, hi[live] + 1, -1)
+    seen = np.cumsum(diff[:Nk]) > 0
+    seen[:min(max(prefix, 0), Nk)] = True
+    return int(seen.sum())
+
+
 # The five synthetic workloads: a tiny single-tile case, a short-sequence d=64
 # batch, a causal d=128 batch, the long-context causal batch-1 case, and a
 # ragged d=256 case with sharpened queries.

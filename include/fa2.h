@@ -177,6 +177,9 @@ int fa2_fwd_ex(const fa2_fwd_params* params, void* stream);
  * The keys of each (batch, head) are split into chunks reduced by separate
  * CTAs to online-softmax states (m, l, O~) that a second kernel merges with
  * the rescaling step of the tiled loop (Lesson 6.6, "Online softmax").
+ * One query row (and packed batches, and d = 256) runs the chunks on CUDA
+ * cores; from two rows on, at d = 64 and 128, the tiled tensor-core kernel
+ * reduces each chunk for the whole query tile.
  *
  * Arguments as fa2_fwd_ex (same struct, masks, strides and packed batches),
  * with seqlen_q <= FA2_DECODE_MAX_Q (FA2_ERR_UNSUPPORTED otherwise; packed:
@@ -187,7 +190,8 @@ int fa2_fwd_ex(const fa2_fwd_params* params, void* stream);
  * `workspace`: device, >= fa2_decode_workspace_bytes(params) bytes, 256-byte
  * aligned, owned by the caller, overlapping no tensor; it holds fp32 partial
  * states and is written before it is read.  Asynchronous on `stream`; two
- * kernel launches.  Deterministic.
+ * kernel launches (one when the keys fit a single chunk on the tensor-core
+ * path).  Deterministic.
  */
 int fa2_decode(const fa2_fwd_params* params, void* workspace, size_t workspace_bytes, void* stream);
 

@@ -217,6 +217,17 @@ def test_decode_workspace_plan_is_device_independent(lib):
     assert lib.fa2_decode_workspace_bytes(None) == 0
 
 
+def test_decode_plan_skips_keys_no_row_sees(lib):
+    # window (4095, 0), one row vs 16384 keys: keys below 16384 - 1 - 4095 = 12288 are seen by no row,
+    # so 9 splits cover 4096 keys: ceil(4096 / 9) = 456 -> 512 (a multiple of 64), i.e. 8 chunks
+    p = _params(batch=1, heads=32, seqlen_q=1, seqlen_k=16384, head_dim=128, window_left=4095, window_right=0)
+    assert lib.fa2_decode_workspace_bytes(ctypes.byref(p)) == 32 * 8 * 128 * 4 + 32 * 8 * 2 * 4
+    # a prefix keeps every chunk from key 0 (the plan of the unwindowed call)
+    p = _params(batch=1, heads=32, seqlen_q=1, seqlen_k=16384, head_dim=128, window_left=4095, window_right=0,
+                prefix_len=16)
+    assert lib.fa2_decode_workspace_bytes(ctypes.byref(p)) == 288 * 128 * 4 + 2304
+
+
 @pytest.mark.parametrize("kw,code", [
     (dict(seqlen_q=9), fa2.FA2_ERR_UNSUPPORTED),
     (dict(seqlen_q=0), fa2.FA2_ERR_UNSUPPORTED),

@@ -159,6 +159,50 @@ def test_decode_long_caches(nk, d, dtype):
     check(o.reshape(B * H, d), lse.reshape(B * H), o_ref, l_ref, dtype, "nk=%d d=%d" % (nk, d))
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_tensor_core_path_bnhd_equals_contiguous(d):
+    """Six rows (the tensor-core split path): K/V as [B, N, H, d] views give
+    bit-identical results to contiguous caches, and both equal the oracle."""
+    B, H, nq, nk, dtype = 2, 3, 6, 5000, sy.BF16
+    q, k, v = qkv(B, H, nq, nk, d, dtype, seed=13000 + d)
+    qd, kd, vd = (to_dev(x, dtype) for x in (q, k, v))
+    o1, l1 = fa2.fa2_decode(qd, kd, vd, window_left=-1, window_right=0)
+    kb, vb = (x.transpose(1, 2).contiguous().transpose(1, 2) for x in (kd, vd))
+    o2, l2 = fa2.fa2_decode(qd, kb, vb, window_left=-1, window_right=0)
+    status_ok()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    scale = 1.0 / np.sqrt(d)
+    o_ref, lse_ref = oracle.attention_fwd_masked(q, k, v, dtype, scale, window_left=-1, window_right=0)
+    check(o1.double().cpu().numpy(), l1.double().cpu().numpy(), o_ref, lse_ref, dtype, "tensor-core path d=%d" % d)
+
+
+@pytest.mark.parametrize("nq", [3, 8])
+def test_decode_tensor_core_path_long_cache(nq):
+    """Several rows against a 65536-key cache: dozens of key chunks per
+    (b, h) on the tensor-core path, every row checked against the oracle."""
+    B, H, nk, d, dtype = 1, 8, 65536, 128, sy.BF16
+    q, k, v = qkv(B, H, nq, nk, d, dtype, seed=13100 + nq)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = run_decode(q, k, v, dtype, scale, window_left=-1, window_right=0)
+    bh = np.repeat(np.arange(B * H), nq)
+    rows = np.tile(np.arange(nq), B * H)
+    o_ref, l_ref = oracle.attention_rows_masked(q, k, v, dtype, scale, bh, rows, window_left=-1, window_right=0)
+    check(o.reshape(B * H * nq, d), lse.reshape(B * H * nq), o_ref, l_ref, dtype, "nq=%d nk=%d" % (nq, nk))
+
+
+@pytest.mark.parametrize("nq", [1, 4])
+def test_decode_window_chunks_start_at_the_band(nq):
+    """A bounded window against a long cache: the key chunks cover only the
+    band the rows see (both the CUDA-core and the tensor-core path)."""
+    B, H, nk, d, dtype = 1, 4, 20000, 128, sy.BF16
+    q, k, v = qkv(B, H, nq, nk, d, dtype, seed=13200 + nq)
+    scale = 1.0 / np.sqrt(d)
+    for wl in (1000, 4095):
+        o, lse = run_decode(q, k, v, dtype, scale, window_left=wl, window_right=0)
+        o_ref, l_ref = oracle.attention_fwd_masked(q, k, v, dtype, scale, window_left=wl, window_right=0)
+        check(o, lse, o_ref, l_ref, dtype, "nq=%d window %d" % (nq, wl))
+
+
 def test_decode_repeated_calls_bit_identical():
     q, k, v = qkv(4, 8, 4, 20000, 128, sy.BF16, seed=12900)
     qd, kd, vd = (to_dev(x, sy.BF16) for x in (q, k, v))

@@ -60,3 +60,17 @@ def test_visible_keys_matches_brute_force(Nq, Nk, wl, wr, pre):
             n += (j < pre) or band
         want.append(n)
     np.testing.assert_array_equal(sy.visible_keys(Nq, Nk, wl, wr, pre), want)
+
+
+@pytest.mark.parametrize("Nq,Nk,wl,wr,pre", [(7, 7, -1, -1, 0), (7, 7, -1, 0, 0), (5, 12, 2, 1, 0), (12, 5, -1, 0, 0),
+                                             (20, 20, 3, 0, 4), (20, 20, 0, 0, 25), (9, 30, 0, -1, 2),
+                                             (1, 64, 4, 0, 0), (3, 100, 0, 0, 0), (8, 50, 10, 2, 30), (4, 4, 0, 0, 0)])
+def test_union_visible_keys_matches_brute_force(Nq, Nk, wl, wr, pre):
+    off = Nk - Nq
+    seen = set()
+    for i in range(Nq):
+        for j in range(Nk):
+            band = (wl < 0 or j >= i + off - wl) and (wr < 0 or j <= i + off + wr)
+            if (j < pre) or band:
+                seen.add(j)
+    assert sy.union_visible_keys(Nq, Nk, wl, wr, pre) == len(seen)
