@@ -421,8 +421,8 @@ int forward(const fa2_fwd_params& a_in, cudaStream_t stream) {
 // split shorter than kDecodeMinChunk keys, chunks a multiple of a stage.
 constexpr long long kDecodeTargetCtas = 2 * 152;
 constexpr long long kDecodeMinChunk = 256;
-// From this many query rows on (d = 64 / 128, unpacked) the chunks run on the
-// tensor cores; fewer rows stay on the CUDA-core decode kernel.
+// From this many query rows on (d = 64 / 128) the chunks run on the tensor
+// cores; fewer rows stay on the CUDA-core decode kernel.
 constexpr int kDecodeTcMinRows = 2;
 
 struct DecodePlan {
@@ -479,9 +479,9 @@ int decode(const fa2_fwd_params& a_in, void* workspace, size_t workspace_bytes, 
   rc = prepare(a, FA2_DECODE_MAX_Q, pr, &ew);
   if (rc) return rc;
   const bool packed = a.cu_seqlens_q != nullptr;
-  if (!packed && a.seqlen_q >= kDecodeTcMinRows && (a.head_dim == 64 || a.head_dim == 128)) {
-    // one query tile (N_q <= 8) per (b, h), split into the plan's key chunks
-    // (a multiple of the kernel's 64-row key tile)
+  if (a.seqlen_q >= kDecodeTcMinRows && (a.head_dim == 64 || a.head_dim == 128)) {
+    // one query tile (N_q <= 8) per (b, h) or packed sequence, split into the
+    // plan's key chunks (a multiple of the kernel's 64-row key tile)
     LaunchArgs tl;
     std::memset(&tl, 0, sizeof(tl));
     rc = cached_decode_tc_maps(tl, pr.key);

@@ -351,6 +351,10 @@ __global__ void __launch_bounds__(192, DbufConfig<D>::CTAS_PER_SM)
   // The whole CTA leaves together, before any barrier or TMEM set-up, when
   // its sequence is malformed or shorter than this tile's rows.
   if (!seq_info(p, bh, t.seq)) return;
+  if (SPLIT && t.seq.n_k > p.split_base + splits * p.split_chunk) {   // a packed sequence the plan does not cover
+    if (threadIdx.x == 0 && t.split == 0) atomicOr(p.status, kStatusBadSeqlens);
+    return;
+  }
   t.q0 = q_tile * C::BR;
   if (t.q0 >= t.seq.n_q) return;
   t.bar0 = sbase + C::OFF_BAR;

@@ -131,21 +131,25 @@ def test_decode_packed_caches():
         row += nq
 
 
-def test_decode_sequence_longer_than_plan_is_reported():
+@pytest.mark.parametrize("rows", [1, 2])
+def test_decode_sequence_longer_than_plan_is_reported(rows):
+    """A packed sequence with more keys than max_seqlen_k lets the split plan
+    cover is reported and left unwritten, on both paths (one row: CUDA-core
+    kernel; two rows: tensor-core kernel)."""
     H, d, dtype = 2, 64, sy.FP16
-    q, k, v = qkv(1, H, 2, 900, d, dtype, seed=12700)
+    q, k, v = qkv(1, H, 2 * rows, 900, d, dtype, seed=12700 + rows)
     qp, kp, vp = (np.ascontiguousarray(x[0].transpose(1, 0, 2)) for x in (q, k, v))
-    cu_q = torch.tensor([0, 1, 2], dtype=torch.int32, device="cuda")
+    cu_q = torch.tensor([0, rows, 2 * rows], dtype=torch.int32, device="cuda")
     cu_k = torch.tensor([0, 300, 900], dtype=torch.int32, device="cuda")   # second sequence: 600 keys
-    o = torch.full((2, H, d), 3.0, dtype=torch.float16, device="cuda")
-    lse = torch.full((H, 2), 4.0, dtype=torch.float32, device="cuda")
+    o = torch.full((2 * rows, H, d), 3.0, dtype=torch.float16, device="cuda")
+    lse = torch.full((H, 2 * rows), 4.0, dtype=torch.float32, device="cuda")
     fa2.fa2_decode(to_dev(qp, dtype), to_dev(kp, dtype), to_dev(vp, dtype), o=o, lse=lse, cu_seqlens_q=cu_q,
-                   cu_seqlens_k=cu_k, max_seqlen_q=1, max_seqlen_k=300)
+                   cu_seqlens_k=cu_k, max_seqlen_q=rows, max_seqlen_k=300)
     torch.cuda.synchronize()
     code, _ = fa2.fa2_get_device_status()
     assert code == fa2.FA2_ERR_DEVICE_SEQLENS
-    assert torch.all(o[1] == 3.0) and torch.all(lse[:, 1] == 4.0)    # the long one is left as it was
-    assert not torch.any(o[0] == 3.0)
+    assert torch.all(o[rows:] == 3.0) and torch.all(lse[:, rows:] == 4.0)    # the long one is left as it was
+    assert not torch.any(o[:rows] == 3.0)
 
 
 @pytest.mark.parametrize("nk,d,dtype", [(131072, 128, sy.BF16), (65536, 64, sy.FP16), (32768, 256, sy.BF16)])
