@@ -42,7 +42,7 @@ METRIC = "forward attention TFLOP/s at 1 GB300 and % of dense FP16/BF16 tensor p
 L2_BYTES = 129e6          # GB300 L2
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = 4
-KERNEL_SOURCES = ["fa2_common.cuh", "fa2_fwd_pingpong.cuh", "fa2_fwd_dbuf.cuh", "sm103_ptx.cuh", "fa2_internal.h", "fa2_abi.cu"]
+KERNEL_SOURCES = ["fa2_common.cuh", "fa2_tile.cuh", "fa2_fwd_dbuf.cuh", "sm103_ptx.cuh", "fa2_internal.h", "fa2_abi.cu"]
 
 
 BWD_KERNEL_SOURCES = KERNEL_SOURCES + ["fa2_bwd.cuh"]
@@ -76,10 +76,10 @@ def measured_hbm():
         return 6800.0, "of fallback (6.8 TB/s)"
 
 
-def recorded_traffic(workload: int, kernel: str = "fa2_fwd_pingpong_kernel"):
+def recorded_traffic(workload: int, kernel: str = "fa2_fwd_dbuf_kernel"):
     """DRAM bytes per launch of `kernel` from the committed ncu summaries, if the
     record was taken on this kernel source (records without a kernel field are
-    the forward kernel's)."""
+    an earlier forward kernel's and match nothing now)."""
     path = os.path.join(ROOT, "profiles", "traffic_per_launch.txt")
     if not os.path.exists(path):
         return None
@@ -88,7 +88,7 @@ def recorded_traffic(workload: int, kernel: str = "fa2_fwd_pingpong_kernel"):
         for line in f:
             parts = dict(p.split("=", 1) for p in line.split() if "=" in p)
             if (parts.get("kernel_sha") == src and parts.get("workload") == str(workload)
-                    and parts.get("kernel", "fa2_fwd_pingpong_kernel") == kernel):
+                    and parts.get("kernel", "") == kernel):
                 try:
                     return float(parts["bytes_per_launch"])
                 except (KeyError, ValueError):
@@ -619,8 +619,7 @@ def main():
 
     if rank == 0:
         clk = clocks.summary()
-        kname = ("fa2_bwd_kernel" if args.backward else
-                 "fa2_fwd_pingpong_kernel" if w.d <= 128 else "fa2_fwd_dbuf_kernel")
+        kname = "fa2_bwd_kernel" if args.backward else "fa2_fwd_dbuf_kernel"
         line = {
             "metric": METRIC if not args.backward else
             "backward attention TFLOP/s at 1 GB300 (2.5x the forward FLOPs) and % of dense FP16/BF16 tensor peak",

@@ -23,9 +23,10 @@ __device__ uint32_t g_device_status;
 
 TileGeometry tile_geometry(int d) {
   TileGeometry g;
+  (void)d;   // the double-buffered kernel's tiles at every head dim
   g.q_rows = 128;
-  g.kv_rows = (d == 256) ? 64 : 128;
-  g.cta_rows = (d == 256) ? 128 : 256;
+  g.kv_rows = 64;
+  g.cta_rows = 128;
   return g;
 }
 
@@ -128,6 +129,7 @@ struct MapCache {
 thread_local MapCache t_maps;
 thread_local MapCache t_decode_maps;
 thread_local MapCache t_decode_tc_maps;
+thread_local MapCache t_bwd_maps;
 
 // K and V maps of the decode kernel: whole rows (d columns) x
 // decode_block_rows(d) rows per box, no swizzle (rows land contiguously).
@@ -151,13 +153,13 @@ int cached_decode_maps(DecodeLaunchArgs& a, const MapKey& key) {
   return FA2_OK;
 }
 
-int cached_maps(LaunchArgs& a, const MapKey& key) {
-  MapCache& c = t_maps;
+// q, k, v and o maps with boxes of 64 columns x rows[t] rows (128-byte
+// swizzle), cached per host thread in `c` (each cache serves one box geometry
+// per head dim).
+int cached_maps_rows(MapCache& c, LaunchArgs& a, const MapKey& key, const int rows[4]) {
   if (!(c.valid && std::memcmp(&c.key, &key, sizeof(MapKey)) == 0)) {
     const bool bf16 = key.dtype == FA2_BF16;
-    const TileGeometry g = tile_geometry(key.d);
     CUtensorMap* maps[4] = {&c.tm_q, &c.tm_k, &c.tm_v, &c.tm_o};
-    const int rows[4] = {g.q_rows, g.kv_rows, g.kv_rows, 32};   // o: one warp's 32 rows per box
     c.valid = false;
     for (int i = 0; i < 4; ++i) {
       if (encode_map_rows(maps[i], key.ptr[i], key.d, key.dims[i][0], key.dims[i][1], key.dims[i][2],
@@ -174,29 +176,25 @@ int cached_maps(LaunchArgs& a, const MapKey& key) {
   return FA2_OK;
 }
 
-// Maps of the tensor-core decode path (the double-buffered kernel at d <= 128):
-// q boxes of 128 rows, k and v boxes of 64 rows, o boxes of 32 rows (o is not
+// The forward kernel's maps: query tiles, key/value tiles (tile_geometry) and
+// o boxes of one warp's 32 rows.
+int cached_maps(LaunchArgs& a, const MapKey& key) {
+  const TileGeometry g = tile_geometry(key.d);
+  const int rows[4] = {g.q_rows, g.kv_rows, g.kv_rows, 32};
+  return cached_maps_rows(t_maps, a, key, rows);
+}
+
+// Maps of the tensor-core decode path: the forward kernel's geometry (o is not
 // stored through in split-key mode, but every map the kernel prefetches is valid).
 int cached_decode_tc_maps(LaunchArgs& a, const MapKey& key) {
-  MapCache& c = t_decode_tc_maps;
-  if (!(c.valid && std::memcmp(&c.key, &key, sizeof(MapKey)) == 0)) {
-    const bool bf16 = key.dtype == FA2_BF16;
-    CUtensorMap* maps[4] = {&c.tm_q, &c.tm_k, &c.tm_v, &c.tm_o};
-    const int rows[4] = {128, 64, 64, 32};
-    c.valid = false;
-    for (int i = 0; i < 4; ++i) {
-      if (encode_map_rows(maps[i], key.ptr[i], key.d, key.dims[i][0], key.dims[i][1], key.dims[i][2],
-                          key.strides[i], rows[i], bf16, key.merged != 0))
-        return FA2_ERR_CUDA;
-    }
-    std::memcpy(&c.key, &key, sizeof(MapKey));
-    c.valid = true;
-  }
-  a.tm_q = c.tm_q;
-  a.tm_k = c.tm_k;
-  a.tm_v = c.tm_v;
-  a.tm_o = c.tm_o;
-  return FA2_OK;
+  const int rows[4] = {128, 64, 64, 32};
+  return cached_maps_rows(t_decode_tc_maps, a, key, rows);
+}
+
+// The backward kernel's q, k and v maps: 128-row query and key tiles.
+int cached_bwd_maps(LaunchArgs& a, const MapKey& key) {
+  const int rows[4] = {128, 128, 128, 32};
+  return cached_maps_rows(t_bwd_maps, a, key, rows);
 }
 
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
@@ -893,7 +891,7 @@ int backward(const fa2_bwd_params& bp, cudaStream_t stream) {
   std::memset(&la, 0, sizeof(la));
   LaunchArgs fl;
   std::memset(&fl, 0, sizeof(fl));
-  rc = cached_maps(fl, pr.key);
+  rc = cached_bwd_maps(fl, pr.key);
   if (rc) return rc;
   la.tm_q = fl.tm_q;
   la.tm_k = fl.tm_k;

@@ -48,7 +48,7 @@
 // sees stores dK = dV = 0.
 #pragma once
 
-#include "fa2_fwd_pingpong.cuh"
+#include "fa2_tile.cuh"
 
 namespace fa2 {
 

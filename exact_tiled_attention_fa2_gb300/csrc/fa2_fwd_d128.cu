@@ -1,7 +1,7 @@
-// Forward kernel instantiations for head dim 128: two 128-row query tiles per
-// CTA sharing each 128-row key/value tile.
-#include "fa2_fwd_pingpong.cuh"
+// Forward kernel instantiations for head dim 128: one 128-row query tile per
+// CTA, 64-row key/value tiles, two S buffers in tensor memory, two CTAs per SM.
+#include "fa2_fwd_dbuf.cuh"
 
 namespace fa2 {
-int launch_fwd_d128(const LaunchArgs& a) { return launch_fwd_pingpong_dispatch<128>(a); }
+int launch_fwd_d128(const LaunchArgs& a) { return launch_fwd_dbuf_dispatch<128>(a); }
 }  // namespace fa2

@@ -1,32 +1,41 @@
-// fa2_fwd_dbuf.cuh -- forward kernel for head dim 256: one 128-row query tile
-// per CTA with two S buffers in tensor memory.
+// fa2_fwd_dbuf.cuh -- the forward kernel (head dims 64, 128, 256): one
+// 128-row query tile per CTA with two S buffers in tensor memory.
 //
-// At d = 256 the accumulator O~ alone takes 256 TMEM columns and a query tile
-// 64 KB of shared memory, so a CTA holds one query tile.  Key/value tiles of
-// B_c = 64 rows stream through separate 2-stage K and V rings (Q 64 KB +
-// 4 x 32 KB).  S alternates between two 64-column TMEM buffers, and the
+// Key/value tiles of B_c = 64 rows stream through separate 2-stage K and V
+// rings.  S alternates between two 64-column TMEM buffers, and the
 // MMA-issuing thread runs, per key tile j,
 //
 //     O~ += P(j) V_j,   S(j+2) = Q K_{j+2}^T   (into the buffer P(j) came from)
 //
-// so the softmax of tile j+1 overlaps those two products.  The PV products
-// have N = d = 256, the MMA shape that keeps the tensor pipe busiest.  A K
-// stage is released as soon as its S product completes and a V stage after
-// its PV product, so the next K tile loads while the current PV runs.
-// Online softmax as in the two-tile kernel: running max raised only past a
-// 2^8 margin, O~ rescaled in place when it is.
+// so the softmax of tile j+1 overlaps those two products.  tcgen05 MMAs
+// issued by one thread execute in order, which is what lets S(j+2) follow
+// the product reading P(j) from the same columns.  A K stage is released as
+// soon as its S product completes and a V stage after its PV product, so the
+// next K tile loads while the current PV runs.  Online softmax with the
+// rescaling margin of fa2_tile.cuh: the running max is raised only past 2^8,
+// O~ rescaled in place when it is.
+//
+// Size classes: at d <= 128 a CTA takes 256 TMEM columns (two S buffers +
+// O~) and ~100 KB of shared memory (Q 32 KB at d = 128, K and V rings), so two
+// CTAs share an SM: one CTA's set-up, first loads and epilogue overlap the
+// other's products, and the two CTAs' MMAs interleave on the tensor pipe.
+// At d = 256 O~ alone takes 256 columns and Q 64 KB: one CTA per SM, whose PV
+// products have N = 256.
 //
 // Warp roles (192 threads): warps 0-3 softmax + epilogue (one thread per
 // query row = TMEM lane), warp 4 TMEM owner and MMA issuer, warp 5 TMA.
+// Masks and lengths are run-time (KeyMask): the tile visits only the key
+// tiles its rows can see; key tiles every row sees skip the element mask.
+// The epilogue stages O in the (then free) Q buffer and writes it with TMA
+// stores (per-row stores for packed batches).
 //
-// The same kernel at d = 64 / 128 (256 TMEM columns, ~100 KB of shared
-// memory: two CTAs per SM) serves decoding in split-key mode
-// (KernelParams::splits > 1): a unit is a (query tile, key chunk) pair, the
-// tile's key range is clipped to the chunk, and each row's partial (m, l, O~)
-// is written for the decode merge kernel instead of O and LSE.
+// The same kernel at d = 64 / 128 serves decoding in split-key mode
+// (SPLIT; KernelParams::splits > 1): a unit is a (query tile, key chunk) pair,
+// the tile's key range is clipped to the chunk, and each row's partial
+// (m, l, O~) is written for the decode merge kernel instead of O and LSE.
 #pragma once
 
-#include "fa2_fwd_pingpong.cuh"
+#include "fa2_tile.cuh"
 
 namespace fa2 {
 
@@ -95,16 +104,36 @@ struct DbufCtx {
 
 // K_j is needed two products before V_j, so the K and V streams are issued
 // independently: whichever ring has a free slot gets the next load.
+// `first` = true issues what needs no wait -- Q and the first stage of each
+// ring -- (the kernel does this before its set-up barrier, so the loads fly
+// while TMEM is allocated) and returns; `first` = false issues the rest and
+// then waits for every load in flight to land.
 template <class C>
 __device__ __forceinline__ void db_producer(const DbufCtx& t, const KernelParams& p, const CUtensorMap* tm_q,
-                                            const CUtensorMap* tm_k, const CUtensorMap* tm_v) {
+                                            const CUtensorMap* tm_k, const CUtensorMap* tm_v, bool first) {
   const int h = t.seq.h, b = t.seq.b, hb = b * p.heads + h;
   const bool merged = p.merged_bh != 0;
   const int krow0 = t.seq.row0_k + t.kv0 * C::BC;
-  mbar_arrive_expect_tx(t.bar(DB_Q), C::Q_BYTES);
-  for (int kb = 0; kb < C::D / 64; ++kb)
-    tma_load_rows(t.sQ + kb * (C::BR * 128), tm_q, merged, kb * 64, t.seq.row0_q + t.q0, h, b, hb, t.bar(DB_Q));
-  int jk = 0, jv = 0;
+  const int nk0 = min(t.nkv, C::KSTAGES), nv0 = min(t.nkv, C::VSTAGES);   // loads of the first pass
+  if (first) {
+    mbar_arrive_expect_tx(t.bar(DB_Q), C::Q_BYTES);
+    for (int kb = 0; kb < C::D / 64; ++kb)
+      tma_load_rows(t.sQ + kb * (C::BR * 128), tm_q, merged, kb * 64, t.seq.row0_q + t.q0, h, b, hb, t.bar(DB_Q));
+    for (int j = 0; j < nk0; ++j) {
+      mbar_arrive_expect_tx(t.bar(DB_KFULL + j), C::KV_BYTES);
+      for (int kb = 0; kb < C::D / 64; ++kb)
+        tma_load_rows(t.sK + j * C::KV_BYTES + kb * (C::BC * 128), tm_k, merged, kb * 64, krow0 + j * C::BC, h, b,
+                      hb, t.bar(DB_KFULL + j));
+    }
+    for (int j = 0; j < nv0; ++j) {
+      mbar_arrive_expect_tx(t.bar(DB_VFULL + j), C::KV_BYTES);
+      for (int kb = 0; kb < C::D / 64; ++kb)
+        tma_load_rows(t.sV + j * C::KV_BYTES + kb * (C::BC * 128), tm_v, merged, kb * 64, krow0 + j * C::BC, h, b,
+                      hb, t.bar(DB_VFULL + j));
+    }
+    return;
+  }
+  int jk = nk0, jv = nv0;
   uint64_t idle_since = 0;
   while (jk < t.nkv || jv < t.nkv) {
     bool progressed = false;
@@ -268,10 +297,10 @@ __device__ __forceinline__ void db_softmax(const DbufCtx& t, const KernelParams&
     float2 sum0 = make_float2(0.f, 0.f), sum1 = make_float2(0.f, 0.f);
     if (split_tile<BF16>(masked, few_keys)) {
 #pragma unroll
-      for (int ch = 0; ch < C::BC / 32; ++ch) pp_p_chunk<C, BF16, true>(sr, ch, tS, scale2, neg_m2, sum0, sum1);
+      for (int ch = 0; ch < C::BC / 32; ++ch) softmax_p_chunk<C, BF16, true>(sr, ch, tS, scale2, neg_m2, sum0, sum1);
     } else {
 #pragma unroll
-      for (int ch = 0; ch < C::BC / 32; ++ch) pp_p_chunk<C, BF16, false>(sr, ch, tS, scale2, neg_m2, sum0, sum1);
+      for (int ch = 0; ch < C::BC / 32; ++ch) softmax_p_chunk<C, BF16, false>(sr, ch, tS, scale2, neg_m2, sum0, sum1);
     }
     const float2 sum2 = __fadd2_rn(sum0, sum1);
     l_run = l_run * alpha + (sum2.x + sum2.y);
@@ -382,7 +411,7 @@ __global__ void __launch_bounds__(192, DbufConfig<D>::CTAS_PER_SM)
   t.tm = tile_mask<BAND>(t.km, t.q0, last, C::BC).from(t.kv0);
   t.few_keys = t.km.n_k <= 2 * C::BC;
 
-  if (threadIdx.x == 0) {
+  if (warp == C::TMA_WARP && lane == 0) {
     mbar_init(t.bar(DB_Q), 1);
     for (int s = 0; s < C::KSTAGES; ++s) {
       mbar_init(t.bar(DB_KFULL + s), 1);
@@ -403,12 +432,12 @@ __global__ void __launch_bounds__(192, DbufConfig<D>::CTAS_PER_SM)
     facts->seq = t.seq;
     facts->km = t.km;
     fence_mbar_init();
-  }
-  if (warp == C::TMA_WARP && lane == 0) {
+    fence_proxy_async_smem();   // the initialised barriers, before this thread's own TMA loads signal them
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_o);
+    if (t.nkv > 0) db_producer<C>(t, p, &tm_q, &tm_k, &tm_v, true);
   }
   if (warp == C::MMA_WARP) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -420,7 +449,7 @@ __global__ void __launch_bounds__(192, DbufConfig<D>::CTAS_PER_SM)
   t.tmem = *tmem_slot;
 
   if (warp == C::TMA_WARP) {
-    if (lane == 0 && t.nkv > 0) db_producer<C>(t, p, &tm_q, &tm_k, &tm_v);
+    if (lane == 0 && t.nkv > 0) db_producer<C>(t, p, &tm_q, &tm_k, &tm_v, false);
   } else if (warp == C::MMA_WARP) {
     if (lane == 0) db_mma<C, BF16>(t);
     __syncwarp();
