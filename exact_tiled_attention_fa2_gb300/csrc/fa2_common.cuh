@@ -406,8 +406,10 @@ __device__ __forceinline__ void store_partial_row(const KernelParams& p, int bh,
 // interleaved.  So the CTAs resident at a time share the K/V of about
 // kHeadGroup heads in L2, and causal work is launched longest first within
 // each group, whose short tail overlaps the next group's long units.
-constexpr int kHeadGroup = 8;   // forward kernels (measured: 4 and 16 lose on the long causal workload,
-                                // a group sized to span two waves lost 10 % on B4 H16 N4096)
+// Forward kernels (128-row units, two CTAs per SM): measured against 4 and 8,
+// 16 is 0.2 % faster on B1 H32 N16384 causal and 1 % on B4 H16 N4096 causal;
+// 4 loses 7 % on the latter.
+constexpr int kHeadGroup = 16;
 
 __device__ __forceinline__ void unit_of_block(int block, int bh_total, int units, int& bh, int& unit,
                                               int group = kHeadGroup) {
