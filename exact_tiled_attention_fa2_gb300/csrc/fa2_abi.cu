@@ -419,9 +419,11 @@ int forward(const fa2_fwd_params& a_in, cudaStream_t stream) {
 // split shorter than kDecodeMinChunk keys, chunks a multiple of a stage.
 constexpr long long kDecodeTargetCtas = 2 * 152;
 constexpr long long kDecodeMinChunk = 256;
-// From this many query rows on (d = 64 / 128) the chunks run on the tensor
-// cores; fewer rows stay on the CUDA-core decode kernel.
-constexpr int kDecodeTcMinRows = 2;
+// From this many query rows on the chunks run on the tensor cores (the tiled
+// kernel in split-key mode); fewer rows, and d = 256, stay on the CUDA-core
+// decode kernel.  Measured: at d = 128 the tensor-core path is 2-8 % faster
+// already for one row; at d = 64 one row is 8 % faster on CUDA cores.
+constexpr int decode_tc_min_rows(int d) { return d == 128 ? 1 : d == 64 ? 2 : 1 << 30; }
 
 struct DecodePlan {
   int splits, chunk, base;
@@ -477,7 +479,7 @@ int decode(const fa2_fwd_params& a_in, void* workspace, size_t workspace_bytes, 
   rc = prepare(a, FA2_DECODE_MAX_Q, pr, &ew);
   if (rc) return rc;
   const bool packed = a.cu_seqlens_q != nullptr;
-  if (a.seqlen_q >= kDecodeTcMinRows && (a.head_dim == 64 || a.head_dim == 128)) {
+  if (a.seqlen_q >= decode_tc_min_rows(a.head_dim)) {
     // one query tile (N_q <= 8) per (b, h) or packed sequence, split into the
     // plan's key chunks (a multiple of the kernel's 64-row key tile)
     LaunchArgs tl;

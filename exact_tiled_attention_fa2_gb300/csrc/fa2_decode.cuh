@@ -12,8 +12,8 @@
 // M = max m_c, l = sum 2^(m_c - M) l_c, O = sum 2^(m_c - M) O~_c / l (Lesson
 // 6.6, "Online softmax"; FlashAttention V2 in depth, section 3.2).  Lesson
 // 6.6 ("Common misconceptions") names this regime as needing its own kernel.
-// This CUDA-core kernel serves one query row and d = 256; from two rows on
-// at d = 64 / 128 the tiled tensor-core kernel reduces the chunks
+// This CUDA-core kernel serves one query row at d = 64 and every row count at
+// d = 256; otherwise the tiled tensor-core kernel reduces the chunks
 // (fa2_decode_tc.cuh), since the per-key products grow with the rows.
 //
 // Per CTA: a TMA warp streams [BLOCK x d] boxes of K and V through a 3-stage

@@ -1,8 +1,9 @@
 // fa2_decode_tc.cuh -- decoding on the tensor cores: the double-buffered
 // forward kernel (fa2_fwd_dbuf.cuh) over (query tile, key chunk) units in
 // split-key mode, then the decode merge kernel (fa2_decode.cuh) over the
-// partials.  Used for two or more query rows per (b, h), where the score
-// and value products outgrow the CUDA cores of the split decode kernel.
+// partials.  Used at d = 128 for any row count and at d = 64 from two rows
+// on, where the score and value products outgrow the CUDA cores of the split
+// decode kernel.
 #pragma once
 
 #include <cstring>

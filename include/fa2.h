@@ -177,9 +177,9 @@ int fa2_fwd_ex(const fa2_fwd_params* params, void* stream);
  * The keys of each (batch, head) are split into chunks reduced by separate
  * CTAs to online-softmax states (m, l, O~) that a second kernel merges with
  * the rescaling step of the tiled loop (Lesson 6.6, "Online softmax").
- * One query row (and d = 256) runs the chunks on CUDA cores; from two rows
- * on, at d = 64 and 128, the tiled tensor-core kernel reduces each chunk for
- * the whole query tile.
+ * At d = 128 (and at d = 64 from two query rows on) the tiled tensor-core
+ * kernel reduces each chunk for the whole query tile; one row at d = 64, and
+ * d = 256, run the chunks on CUDA cores.
  *
  * Arguments as fa2_fwd_ex (same struct, masks, strides and packed batches),
  * with seqlen_q <= FA2_DECODE_MAX_Q (FA2_ERR_UNSUPPORTED otherwise; packed:
