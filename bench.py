@@ -648,7 +648,9 @@ def main():
             gbs = gen["bytes"] / (avg_launch_ms / 1e3) / 1e9
             line["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                                 "traffic": None, "peak_source": hbm_note,
-                                "kernel": "fa2_decode_kernel + fa2_decode_merge_kernel",
+                                "kernel": ("fa2_fwd_dbuf_kernel (split-key mode)"
+                                           if w.d == 128 or (w.d == 64 and gen["decode_rows"] >= 2)
+                                           else "fa2_decode_kernel") + " + fa2_decode_merge_kernel",
                                 "avg_launch_ms": avg_launch_ms, "algorithmic_bytes_per_launch": gen["bytes"],
                                 "algorithmic_flops_per_launch": flops}
             line["gpu_launches"] = 2 * args.steps
