@@ -517,12 +517,8 @@ int decode(const fa2_fwd_params& a_in, void* workspace, size_t workspace_bytes, 
   la.p.f.n_k = a.seqlen_k;   // packed: the longest sequence's key count the plan covers
   la.bf16 = a.dtype == FA2_BF16;
   la.stream = stream;
-  int e = 0;
-  switch (a.head_dim) {
-    case 64: e = launch_decode_d64(la); break;
-    case 128: e = launch_decode_d128(la); break;
-    default: e = launch_decode_d256(la); break;
-  }
+  // d = 128 always takes the tensor-core path above
+  const int e = a.head_dim == 64 ? launch_decode_d64(la) : launch_decode_d256(la);
   return e == 0 ? FA2_OK : FA2_ERR_CUDA;
 }
 

@@ -132,7 +132,6 @@ int launch_fwd_d256(const LaunchArgs& a);
 
 struct DecodeLaunchArgs;
 int launch_decode_d64(const DecodeLaunchArgs& a);
-int launch_decode_d128(const DecodeLaunchArgs& a);
 int launch_decode_d256(const DecodeLaunchArgs& a);
 // Decoding on the tensor cores (3 or more query rows, d = 64 / 128, unpacked):
 // the double-buffered forward kernel in split-key mode, then the decode merge
