@@ -36,7 +36,7 @@ struct KernelParams {
   int merged_bh;      // 1: the tensor maps are 3-D (d, rows, B*H), coordinate b*H + h; 0: 4-D
   int tma_o;          // 1: O is staged in shared memory and written by TMA stores (unpacked batches)
   int bh;             // B * H
-  int units;          // query units (tiles or tile pairs) per (b, h), from n_q
+  int units;          // work units per (b, h): query tiles (split-key mode: tiles x chunks)
   int window_left;    // key j visible to query i iff i+off-wl <= j <= i+off+wr
   int window_right;   //   (off = N_k - N_q; -1 = unbounded on that side),
   int prefix;         //   or j < prefix (keys every query sees)
