@@ -119,36 +119,54 @@ struct BwdCtx {
 };
 
 template <class C>
+// `first` = true issues what needs no wait -- K_j, V_j and the first query
+// tile's Q and dO -- (the kernel does this before its set-up barrier, so the
+// loads fly while TMEM is allocated) and returns; `first` = false issues the
+// rest and then waits for every load in flight to land.
 __device__ __forceinline__ void bwd_producer(const BwdCtx& t, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                                             const CUtensorMap* tm_v, const CUtensorMap* tm_do) {
+                                             const CUtensorMap* tm_v, const CUtensorMap* tm_do, bool first) {
   const int h = t.seq.h, b = t.seq.b;
-  mbar_arrive_expect_tx(t.bar(BB_KV), 2 * C::TILE_BYTES);
-  for (int kb = 0; kb < C::D / 64; ++kb) {
-    tma_load_rows(t.sK + kb * (C::T * 128), tm_k, t.merged, kb * 64, t.seq.row0_k + t.j0, h, b, t.hb, t.bar(BB_KV));
-    tma_load_rows(t.sV + kb * (C::T * 128), tm_v, t.merged, kb * 64, t.seq.row0_k + t.j0, h, b, t.hb, t.bar(BB_KV));
+  auto load_q = [&](int it) {
+    const int s = it % C::QSTAGES;
+    mbar_arrive_expect_tx(t.bar(BB_Q + s), C::TILE_BYTES);
+    for (int kb = 0; kb < C::D / 64; ++kb)
+      tma_load_rows(t.sQ + s * C::TILE_BYTES + kb * (C::T * 128), tm_q, t.merged, kb * 64,
+                    t.seq.row0_q + (t.i0 + it) * C::T, h, b, t.hb, t.bar(BB_Q + s));
+  };
+  auto load_do = [&](int it) {
+    const int s = it % C::DOSTAGES;
+    mbar_arrive_expect_tx(t.bar(BB_DO + s), C::TILE_BYTES);
+    for (int kb = 0; kb < C::D / 64; ++kb)
+      tma_load_rows(t.sDO + s * C::TILE_BYTES + kb * (C::T * 128), tm_do, t.merged, kb * 64,
+                    t.seq.row0_q + (t.i0 + it) * C::T, h, b, t.hb, t.bar(BB_DO + s));
+  };
+  if (first) {
+    mbar_arrive_expect_tx(t.bar(BB_KV), 2 * C::TILE_BYTES);
+    for (int kb = 0; kb < C::D / 64; ++kb) {
+      tma_load_rows(t.sK + kb * (C::T * 128), tm_k, t.merged, kb * 64, t.seq.row0_k + t.j0, h, b, t.hb,
+                    t.bar(BB_KV));
+      tma_load_rows(t.sV + kb * (C::T * 128), tm_v, t.merged, kb * 64, t.seq.row0_k + t.j0, h, b, t.hb,
+                    t.bar(BB_KV));
+    }
+    load_q(0);
+    load_do(0);
+    return;
   }
   // Q_i into stage i mod QSTAGES once the MMAs of tile i - QSTAGES have read
   // it, then dO_i likewise; in this order Q runs a tile ahead of dO at d = 128
-  int loaded_q = 0, loaded_do = 0;
-  for (int it = 0; it < t.niter; ++it) {
-    const int row = t.seq.row0_q + (t.i0 + it) * C::T;
+  int loaded_q = 1, loaded_do = 1;   // tile 0's, issued before the set-up barrier
+  for (int it = 1; it < t.niter; ++it) {
     const int s = it % C::QSTAGES, u = it / C::QSTAGES;
     if (u > 0 && !wait_or_abort(t.bar(BB_QEMPTY + s), (uint32_t)(u - 1) & 1, t.abort_flag, t.status,
                                 kSiteProducerEmpty))
       break;
-    mbar_arrive_expect_tx(t.bar(BB_Q + s), C::TILE_BYTES);
-    for (int kb = 0; kb < C::D / 64; ++kb)
-      tma_load_rows(t.sQ + s * C::TILE_BYTES + kb * (C::T * 128), tm_q, t.merged, kb * 64, row, h, b, t.hb,
-                    t.bar(BB_Q + s));
+    load_q(it);
     loaded_q = it + 1;
     const int sd = it % C::DOSTAGES, ud = it / C::DOSTAGES;
     if (ud > 0 && !wait_or_abort(t.bar(BB_DOEMPTY + sd), (uint32_t)(ud - 1) & 1, t.abort_flag, t.status,
                                  kSiteProducerEmpty))
       break;
-    mbar_arrive_expect_tx(t.bar(BB_DO + sd), C::TILE_BYTES);
-    for (int kb = 0; kb < C::D / 64; ++kb)
-      tma_load_rows(t.sDO + sd * C::TILE_BYTES + kb * (C::T * 128), tm_do, t.merged, kb * 64, row, h, b, t.hb,
-                    t.bar(BB_DO + sd));
+    load_do(it);
     loaded_do = it + 1;
   }
   // every load in flight lands before the CTA can exit: the last tile of each stage
@@ -544,7 +562,7 @@ __global__ void __launch_bounds__(384, 1)
   t.abort_flag = abort_flag;
   t.status = f.status;
 
-  if (threadIdx.x == 0) {
+  if (warp == C::TMA_WARP && lane == 0) {
     mbar_init(t.bar(BB_KV), 1);
     for (int s = 0; s < C::QSTAGES; ++s) {
       mbar_init(t.bar(BB_Q + s), 1);
@@ -563,13 +581,13 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(t.bar(BB_EXIT), 1);
     *abort_flag = 0;
     fence_mbar_init();
-  }
-  if (warp == C::TMA_WARP && lane == 0) {
+    fence_proxy_async_smem();   // the initialised barriers, before this thread's own TMA loads signal them
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
     tma_prefetch_desc(&tm_dq);
+    if (t.niter > 0) bwd_producer<C>(t, &tm_q, &tm_k, &tm_v, &tm_do, true);
   }
   if (warp == C::MMA_WARP) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -581,7 +599,7 @@ __global__ void __launch_bounds__(384, 1)
   t.tmem = *tmem_slot;
 
   if (warp == C::TMA_WARP) {
-    if (lane == 0 && t.niter > 0) bwd_producer<C>(t, &tm_q, &tm_k, &tm_v, &tm_do);
+    if (lane == 0 && t.niter > 0) bwd_producer<C>(t, &tm_q, &tm_k, &tm_v, &tm_do, false);
   } else if (warp == C::MMA_WARP) {
     if (lane == 0 && t.niter > 0) bwd_mma<C, BF16>(t);
     __syncwarp();
