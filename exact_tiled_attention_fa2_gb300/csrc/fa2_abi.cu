@@ -191,9 +191,10 @@ int cached_decode_tc_maps(LaunchArgs& a, const MapKey& key) {
   return cached_maps_rows(t_decode_tc_maps, a, key, rows);
 }
 
-// The backward kernel's q, k and v maps: 128-row query and key tiles.
+// The backward kernels' q, k and v maps: 128-row key tiles; query tiles of
+// 128 rows (d = 128) or 64 rows (d = 64).
 int cached_bwd_maps(LaunchArgs& a, const MapKey& key) {
-  const int rows[4] = {128, 128, 128, 32};
+  const int rows[4] = {key.d == 64 ? 64 : 128, 128, 128, 32};
   return cached_maps_rows(t_bwd_maps, a, key, rows);
 }
 
@@ -895,7 +896,8 @@ int backward(const fa2_bwd_params& bp, cudaStream_t stream) {
   la.tm_k = fl.tm_k;
   la.tm_v = fl.tm_v;
   const bool bf16 = a.dtype == FA2_BF16;
-  if (encode_map_rows(&la.tm_do, b.dout, d, dq_dims[2], a.heads, tb, st[3], 128, bf16, pr.key.merged != 0))
+  if (encode_map_rows(&la.tm_do, b.dout, d, dq_dims[2], a.heads, tb, st[3], d == 64 ? 64 : 128, bf16,
+                      pr.key.merged != 0))
     return FA2_ERR_CUDA;
   uint8_t* w = static_cast<uint8_t*>(b.workspace);
   if (encode_dq_accum_map(&la.tm_dq, w, plan.slices, plan.rows_q, d)) return FA2_ERR_CUDA;
