@@ -1,4 +1,6 @@
-// fa2_bwd.cuh -- backward pass of the exact attention forward (head dims 64 and 128).
+// fa2_bwd.cuh -- backward pass of the exact attention forward (head dim 128;
+// head dim 64 runs the two-CTA-per-SM variant in fa2_bwd64.cuh, which reuses
+// this file's context, helpers and preprocess / convert kernels).
 //
 // Gradients for an upstream dO (FlashAttention V2 in depth, section 7):
 //
@@ -28,11 +30,12 @@
 //                                 into the dP^T columns; each warp copies its 32
 //                                 rows out, frees the columns, and TMA adds them
 //
-// At d = 64 the schedule is software-pipelined: S^T of tile i + 1 is issued
-// between dV_i and dK_i (into the columns dV has just read P^T from), so P^T
-// of tile i + 1 is computed while the tensor core finishes tile i, and dQ_i is
-// read out afterwards.  Q_i and dO_i are loaded into separate buffers whose
-// release follows their last reader (dK and dV respectively).
+// Q_i and dO_i are loaded into separate buffers whose release follows their
+// last reader (dK and dV respectively), so the next tile's loads start before
+// dQ_i runs.  The tile's MMAs run back to back: issuing the next tile's S^T
+// ahead of dK and dQ would need a second Q buffer and a whole tile of dQ
+// staging that TMA reads out while the next tile runs (reduce-add drains
+// shared memory slowly), which do not fit beside d = 128's tiles.
 //
 // Warp roles (384 threads): warps 0-3 and 4-7 are two elementwise warpgroups,
 // each for 64 of the tile's 128 query columns (and half of the d columns of
@@ -61,15 +64,8 @@ struct BwdConfig {
   static constexpr int TMA_WARP = 9;
   static constexpr uint32_t TILE_BYTES = T * D * 2;
   static constexpr uint32_t DS_BYTES = T * T * 2;    // dS^T, keys x queries, 16-bit
-  // PIPELINED: S^T of query tile i + 1 is issued between dV_i and dK_i, so
-  // the elementwise warps compute its P^T while the tensor core finishes
-  // tile i.  That needs the next Q tile resident early (two Q buffers) and a
-  // whole tile's dQ staging that TMA reads out while the next tile runs
-  // (reduce-add drains shared memory slowly); both fit at d = 64 only.  At
-  // d = 128 the tile's MMAs run back to back: S^T, dP^T, dV, dK, dQ.
-  static constexpr bool PIPELINED = (D == 64);
-  static constexpr int QSTAGES = PIPELINED ? 2 : 1;    // Q_i buffers
-  static constexpr int DOSTAGES = PIPELINED ? 2 : 1;   // dO_i buffers
+  static constexpr int QSTAGES = 1;    // Q_i buffers
+  static constexpr int DOSTAGES = 1;   // dO_i buffers
   static constexpr uint32_t DQ_BOX_BYTES = 32 * 32 * 4;       // a 32 x 32 fp32 box (one TMA reduce-add)
   static constexpr uint32_t DQ_WARP_BYTES = 32 * (D / 2) * 4;  // a warp's 32 rows x d/2 fp32 dQ columns
   static constexpr uint32_t OFF_K = 0;
@@ -87,7 +83,7 @@ struct BwdConfig {
   static constexpr uint32_t TMEM_S = 256;       // S^T, then P^T in its first 32 columns of each half
   static constexpr uint32_t TMEM_DP = 384;      // dP^T, then dS^T, then the dQ_i contribution
   static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(D == 64 || D == 128, "backward kernel: head dim 64 or 128");
+  static_assert(D == 128, "this backward kernel: head dim 128 (d = 64: fa2_bwd64.cuh)");
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
@@ -204,27 +200,17 @@ __device__ __forceinline__ void bwd_mma(const BwdCtx& t) {
     umma_commit(t.bar(BB_S));
   };
   bool ok = wait_or_abort(t.bar(BB_KV), 0, t.abort_flag, t.status, kSiteMmaK);
-  if (C::PIPELINED && ok) {
-    ok = wait_or_abort(t.bar(BB_Q), 0, t.abort_flag, t.status, kSiteMmaQ);
-    if (ok) {
-      tc_fence_after();
-      issue_s(0);
-    }
-  }
-  // Tile i: S^T_i (pipelined: issued with tile i - 1), dP^T_i, then, once
-  // P^T_i and dS^T_i are written, dV, [pipelined: S^T of tile i + 1], dK, dQ_i
+  // Tile i: S^T_i, dP^T_i, then, once P^T_i and dS^T_i are written, dV, dK, dQ_i
   for (int it = 0; it < t.niter && ok; ++it) {
     const uint32_t ph = (uint32_t)it & 1;
     const int qs = it % C::QSTAGES, ds = it % C::DOSTAGES;
     const uint64_t q_step = (uint64_t)((qs * C::TILE_BYTES) >> 4), do_step = (uint64_t)((ds * C::TILE_BYTES) >> 4);
     const uint64_t do_kmaj = do_kmaj0 + do_step;
     const uint64_t q_mn = q_mn0 + q_step, do_mn = do_mn0 + do_step;
-    if (!C::PIPELINED) {
-      if (!wait_or_abort(t.bar(BB_Q + qs), (uint32_t)(it / C::QSTAGES) & 1, t.abort_flag, t.status, kSiteMmaQ))
-        break;
-      tc_fence_after();
-      issue_s(qs);
-    }
+    if (!wait_or_abort(t.bar(BB_Q + qs), (uint32_t)(it / C::QSTAGES) & 1, t.abort_flag, t.status, kSiteMmaQ))
+      break;
+    tc_fence_after();
+    issue_s(qs);
     // dP^T reuses the columns the previous tile's dQ contribution was read from
     if (it > 0 && !wait_or_abort(t.bar(BB_DQEMPTY), ph ^ 1u, t.abort_flag, t.status, kSiteMmaO)) break;
     if (!wait_or_abort(t.bar(BB_DO + ds), (uint32_t)(it / C::DOSTAGES) & 1, t.abort_flag, t.status, kSiteMmaQ)) break;
@@ -243,16 +229,6 @@ __device__ __forceinline__ void bwd_mma(const BwdCtx& t) {
       umma_ts(tDV, tS + col, do_mn + (uint64_t)((k * 16 * 128) >> 4), idesc_acc, (it > 0 || k > 0) ? 1u : 0u);
     }
     umma_commit(t.bar(BB_DOEMPTY + ds));
-    // S^T of the next tile overwrites the P^T columns dV has just read (the
-    // MMAs of one thread execute in order)
-    if (C::PIPELINED && it + 1 < t.niter) {
-      const int qn = (it + 1) % C::QSTAGES;
-      if (!wait_or_abort(t.bar(BB_Q + qn), (uint32_t)((it + 1) / C::QSTAGES) & 1, t.abort_flag, t.status,
-                         kSiteMmaQ))
-        break;
-      tc_fence_after();
-      issue_s(qn);
-    }
 #pragma unroll
     for (int k = 0; k < C::T / 16; ++k) {
       const uint32_t col = (uint32_t)((k >> 2) * 64 + (k & 3) * 8);
@@ -427,12 +403,6 @@ __device__ __forceinline__ void bwd_elementwise(const BwdCtx& t, const BwdParams
 #pragma unroll
     for (int c = 0; c < 32; ++c) pk[c] = pack2<BF16>(pv[2 * c], pv[2 * c + 1]);
     tmem_st_32x32b_x32(tS, pk);
-    // pipelined: the previous tile's dQ, whose product ran meanwhile; dP^T
-    // of this tile goes into its columns
-    if (C::PIPELINED && it > 0 && !dq_out(it - 1)) {
-      ok = false;
-      break;
-    }
 
     ok = wait_or_abort(t.bar(BB_DP), ph, t.abort_flag, t.status, kSiteSoftmaxO);
     ok = __all_sync(0xffffffffu, ok);
@@ -464,12 +434,11 @@ __device__ __forceinline__ void bwd_elementwise(const BwdCtx& t, const BwdParams
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(t.bar(BB_P));
-    if (!C::PIPELINED && !dq_out(it)) {
+    if (!dq_out(it)) {
       ok = false;
       break;
     }
   }
-  if (C::PIPELINED && ok && t.niter > 0) ok = dq_out(t.niter - 1);
   if (lane == 0) bulk_wait_all();   // this warp's reduce-adds performed before the CTA exits
   __syncwarp();
   if (ok && t.niter > 0) {

@@ -39,7 +39,6 @@ struct Bwd64Config {
   static constexpr int TMA_WARP = 5;
   static constexpr int QSTAGES = 2;
   static constexpr int DOSTAGES = 2;
-  static constexpr bool PIPELINED = true;
   static constexpr uint32_t KV_BYTES = T * D * 2;        // 16 KB
   static constexpr uint32_t QT_BYTES = TQ * D * 2;       // 8 KB
   static constexpr uint32_t DS_HALF = T * 128;           // 128 key rows x 64 queries, 16-bit
