@@ -391,13 +391,26 @@ int prepare(const fa2_fwd_params& a, int units_rows, Prepared& out, const Extent
   return FA2_OK;
 }
 
+// Units per head of a packed batch's grid when each CTA finds its own tile
+// from the offsets (kernels' packed_unit; at most kPackedScanSeqs sequences),
+// or 0 for the plain grid of `units_each` units per (sequence, head).
+// Sequences whose rows do not overlap hold at most (total + (rows - 1) * B) /
+// rows whole or partial tiles of `rows` rows; the smaller grid wins.
+long long packed_grid_units(const fa2_fwd_params& a, long long total, int rows, long long units_each) {
+  if (!a.cu_seqlens_q || a.batch > kPackedScanSeqs) return 0;
+  const long long u = (total + (long long)(rows - 1) * a.batch) / rows;
+  return u < units_each * a.batch ? u : 0;
+}
+
 // Validates the general forward arguments (no CUDA call before they pass),
 // then launches the tiled kernel for the head dim.
 int forward(const fa2_fwd_params& a_in, cudaStream_t stream) {
   const fa2_fwd_params a = fold_batches(a_in);
   Prepared pr;
-  int rc = prepare(a, tile_geometry(a.head_dim).cta_rows, pr);
+  const int rows = tile_geometry(a.head_dim).cta_rows;
+  int rc = prepare(a, rows, pr);
   if (rc) return rc;
+  pr.p.packed_units = (int)packed_grid_units(a, a.total_q, rows, pr.p.units);   // <= the plain grid
   LaunchArgs la;
   std::memset(&la, 0, sizeof(la));
   rc = cached_maps(la, pr.key);
@@ -922,6 +935,7 @@ int backward(const fa2_bwd_params& bp, cudaStream_t stream) {
   p.v_rs = st[2][2];
   p.slices = plan.slices;
   p.num_k_tiles = plan.num_k_tiles;
+  p.f.packed_units = (int)packed_grid_units(a, a.total_k, 128, plan.num_k_tiles);   // <= the plain grid
   p.scale = a.scale;
   la.bf16 = bf16;
   la.stream = stream;

@@ -77,7 +77,7 @@ struct BwdConfig {
   static constexpr uint32_t OFF_BAR = OFF_DQ + 8 * DQ_WARP_BYTES;
   static constexpr uint32_t NUM_BARS = 18;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 4 * kPackedScanWords + 1024;   // misc, scan
   static constexpr uint32_t TMEM_DV = 0;
   static constexpr uint32_t TMEM_DK = 128;
   static constexpr uint32_t TMEM_S = 256;       // S^T, then P^T in its first 32 columns of each half
@@ -480,7 +480,10 @@ __device__ __forceinline__ void bwd_elementwise(const BwdCtx& t, const BwdParams
   }
 }
 
-template <int D, bool BF16>
+// PACKED: a packed batch whose grid holds only its real key tiles
+// (f.packed_units); each CTA finds its sequence and tile from the offsets.
+// A template flag, so that the other kernels' code stays as it was.
+template <int D, bool BF16, bool PACKED>
 __global__ void __launch_bounds__(384, 1)
     fa2_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -500,17 +503,25 @@ __global__ void __launch_bounds__(384, 1)
   int bh, unit;
   // heads in groups of 4: a key tile re-streams the Q and dO tiles of every
   // query tile it visits, and 4 heads' worth stay in L2 better than 8 (measured)
-  unit_of_block((int)blockIdx.x, f.bh, p.num_k_tiles, bh, unit, 4);
-  // The whole CTA leaves together, before any set-up, when its sequence is
-  // malformed, has more keys than the grid covers, or ends before this tile.
-  if (!seq_info(f, bh, t.seq)) return;
-  if (t.seq.n_k > p.num_k_tiles * C::T) {
-    if (threadIdx.x == 0 && unit == 0) atomicOr(f.status, kStatusBadSeqlens);
-    return;
+  // The whole CTA leaves together, before any set-up, when it has no tile,
+  // its sequence is malformed, has more keys than the grid covers, or ends
+  // before this tile.
+  int units = p.num_k_tiles;
+  if constexpr (PACKED) {
+    if (!packed_unit<C::THREADS>(f, C::T, true, p.num_k_tiles, 4,
+                                 reinterpret_cast<int*>(smem + C::OFF_MISC + 64), t.seq, unit, units))
+      return;
+  } else {
+    unit_of_block((int)blockIdx.x, f.bh, p.num_k_tiles, bh, unit, 4);
+    if (!seq_info(f, bh, t.seq)) return;
+    if (t.seq.n_k > p.num_k_tiles * C::T) {
+      if (threadIdx.x == 0 && unit == 0) atomicOr(f.status, kStatusBadSeqlens);
+      return;
+    }
   }
   // the key tiles with the most query tiles (the first ones, under a causal
   // mask) start first
-  const int jt = p.num_k_tiles - 1 - unit;
+  const int jt = units - 1 - unit;
   t.j0 = jt * C::T;
   if (t.j0 >= t.seq.n_k) return;
   const KeyMask km = key_mask(f, t.seq);
@@ -637,6 +648,22 @@ __global__ void fa2_bwd_dq_convert_kernel(const BwdParams p) {
       make_uint4(pack2<BF16>(a.x, a.y), pack2<BF16>(a.z, a.w), pack2<BF16>(c.x, c.y), pack2<BF16>(c.z, c.w));
 }
 
+// The main kernel over the grid of key tiles (every key tile of the longest
+// sequence per (b, h), or a packed batch's real tiles).
+template <int D, bool BF16, bool PACKED>
+int launch_bwd_main(const BwdLaunchArgs& a) {
+  using C = BwdConfig<D>;
+  auto kern = fa2_bwd_kernel<D, BF16, PACKED>;
+  static std::atomic<unsigned long long> configured{0};
+  const int e = once_per_device(configured, [&]() -> int {
+    return (int)cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
+  });
+  if (e != 0) return e;
+  const long long blocks = PACKED ? (long long)a.p.f.heads * a.p.f.packed_units : (long long)a.p.f.bh * a.p.num_k_tiles;
+  kern<<<(unsigned)blocks, C::THREADS, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq, a.p);
+  return (int)cudaGetLastError();
+}
+
 template <int D, bool BF16>
 int launch_bwd(const BwdLaunchArgs& a) {
   using C = BwdConfig<D>;
@@ -647,15 +674,7 @@ int launch_bwd(const BwdLaunchArgs& a) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;
   }
-  auto kern = fa2_bwd_kernel<D, BF16>;
-  static std::atomic<unsigned long long> configured{0};
-  int e = once_per_device(configured, [&]() -> int {
-    return (int)cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
-  });
-  if (e != 0) return e;
-  kern<<<(unsigned)((long long)a.p.f.bh * a.p.num_k_tiles), C::THREADS, C::SMEM_BYTES, a.stream>>>(
-      a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq, a.p);
-  e = (int)cudaGetLastError();
+  int e = a.p.f.packed_units ? launch_bwd_main<D, BF16, true>(a) : launch_bwd_main<D, BF16, false>(a);
   if (e != 0) return e;
   const long long n8 = rows * (D / 8);
   fa2_bwd_dq_convert_kernel<D, BF16><<<(unsigned)((n8 + 255) / 256), 256, 0, a.stream>>>(a.p);

@@ -50,7 +50,7 @@ struct Bwd64Config {
   static constexpr uint32_t OFF_BAR = OFF_DS + 2 * DS_HALF;
   static constexpr uint32_t NUM_BARS = 18;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 4 * kPackedScanWords + 1024;   // misc, scan
   static constexpr uint32_t TMEM_DV = 0;
   static constexpr uint32_t TMEM_DK = 64;
   static constexpr uint32_t TMEM_S = 128;    // S^T, then P^T in its first 32 columns
@@ -375,7 +375,9 @@ __device__ __forceinline__ void bwd64_elementwise(const BwdCtx& t, const BwdPara
   }
 }
 
-template <bool BF16>
+// PACKED: a packed batch whose grid holds only its real key tiles, as in
+// fa2_bwd_kernel.
+template <bool BF16, bool PACKED>
 __global__ void __launch_bounds__(192, 2)
     fa2_bwd64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -393,15 +395,23 @@ __global__ void __launch_bounds__(192, 2)
 
   BwdCtx t;
   int bh, unit;
-  unit_of_block((int)blockIdx.x, f.bh, p.num_k_tiles, bh, unit, 4);
-  // The whole CTA leaves together, before any set-up, when its sequence is
-  // malformed, has more keys than the grid covers, or ends before this tile.
-  if (!seq_info(f, bh, t.seq)) return;
-  if (t.seq.n_k > p.num_k_tiles * C::T) {
-    if (threadIdx.x == 0 && unit == 0) atomicOr(f.status, kStatusBadSeqlens);
-    return;
+  // The whole CTA leaves together, before any set-up, when it has no tile,
+  // its sequence is malformed, has more keys than the grid covers, or ends
+  // before this tile.
+  int units = p.num_k_tiles;
+  if constexpr (PACKED) {
+    if (!packed_unit<C::THREADS>(f, C::T, true, p.num_k_tiles, 4,
+                                 reinterpret_cast<int*>(smem + C::OFF_MISC + 64), t.seq, unit, units))
+      return;
+  } else {
+    unit_of_block((int)blockIdx.x, f.bh, p.num_k_tiles, bh, unit, 4);
+    if (!seq_info(f, bh, t.seq)) return;
+    if (t.seq.n_k > p.num_k_tiles * C::T) {
+      if (threadIdx.x == 0 && unit == 0) atomicOr(f.status, kStatusBadSeqlens);
+      return;
+    }
   }
-  const int jt = p.num_k_tiles - 1 - unit;   // the key tiles with the most query tiles start first
+  const int jt = units - 1 - unit;   // the key tiles with the most query tiles start first
   t.j0 = jt * C::T;
   if (t.j0 >= t.seq.n_k) return;
   const KeyMask km = key_mask(f, t.seq);
@@ -474,6 +484,22 @@ __global__ void __launch_bounds__(192, 2)
   }
 }
 
+// The main kernel over the grid of key tiles (every key tile of the longest
+// sequence per (b, h), or a packed batch's real tiles).
+template <bool BF16, bool PACKED>
+int launch_bwd64_main(const BwdLaunchArgs& a) {
+  using C = Bwd64Config;
+  auto kern = fa2_bwd64_kernel<BF16, PACKED>;
+  static std::atomic<unsigned long long> configured{0};
+  const int e = once_per_device(configured, [&]() -> int {
+    return (int)cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
+  });
+  if (e != 0) return e;
+  const long long blocks = PACKED ? (long long)a.p.f.heads * a.p.f.packed_units : (long long)a.p.f.bh * a.p.num_k_tiles;
+  kern<<<(unsigned)blocks, C::THREADS, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq, a.p);
+  return (int)cudaGetLastError();
+}
+
 // D / accumulator zeroing, the main kernel, then the 16-bit dQ conversion;
 // maps: q and dout boxes of 64 rows, k and v of 128 rows, dQ 32 x 32 fp32.
 template <bool BF16>
@@ -486,15 +512,7 @@ int launch_bwd64_dtype(const BwdLaunchArgs& a) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;
   }
-  auto kern = fa2_bwd64_kernel<BF16>;
-  static std::atomic<unsigned long long> configured{0};
-  int e = once_per_device(configured, [&]() -> int {
-    return (int)cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
-  });
-  if (e != 0) return e;
-  kern<<<(unsigned)((long long)a.p.f.bh * a.p.num_k_tiles), C::THREADS, C::SMEM_BYTES, a.stream>>>(
-      a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq, a.p);
-  e = (int)cudaGetLastError();
+  const int e = a.p.f.packed_units ? launch_bwd64_main<BF16, true>(a) : launch_bwd64_main<BF16, false>(a);
   if (e != 0) return e;
   const long long n8 = rows * (C::D / 8);
   fa2_bwd_dq_convert_kernel<64, BF16><<<(unsigned)((n8 + 255) / 256), 256, 0, a.stream>>>(a.p);

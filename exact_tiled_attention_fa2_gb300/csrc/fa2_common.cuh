@@ -429,4 +429,77 @@ __device__ __forceinline__ void unit_of_block(int block, int bh_total, int units
   unit = units - 1 - r / size;
 }
 
+// Scratch words packed_unit needs in shared memory.
+constexpr int kPackedScanWords = 32;
+
+// Block -> (sequence, head, unit) for packed batches of at most
+// kPackedScanSeqs sequences, whose grid holds only the units that exist:
+// ceil(n / rows) per (sequence, head), n the sequence's query rows (forward)
+// or key rows (backward, `by_keys`).  Sequences whose rows do not overlap hold
+// at most total + (rows - 1) * B rows of units between them, which sizes the
+// host's grid.  Each thread reads one sequence's offsets, the CTA sums the
+// unit counts in packing order, and the thread whose sequence holds this
+// block passes its facts on through `scan` (kPackedScanWords ints of shared
+// memory).  Inside a sequence the blocks follow unit_of_block over its heads.
+// A sequence whose offsets are out of range (the seq_info checks; with
+// `by_keys` also more than max_units key tiles) holds no units and sets the
+// bad-offsets status bit.  False when this block has no unit; every thread
+// returns the same.
+template <int THREADS>
+__device__ __forceinline__ bool packed_unit(const KernelParams& p, int rows, bool by_keys, int max_units, int group,
+                                            int* scan, SeqInfo& s, int& unit, int& units) {
+  constexpr int NW = THREADS / 32;
+  static_assert(THREADS >= kPackedScanSeqs && NW + 7 <= kPackedScanWords, "packed scan");
+  const int nseq = p.bh / p.heads;
+  const int i = (int)threadIdx.x, lane = i & 31, w = i >> 5;
+  int q_a = 0, q_b = 0, k_a = 0, k_b = 0, cnt = 0;
+  if (i < nseq) {
+    q_a = __ldg(p.cu_q + i);
+    q_b = __ldg(p.cu_q + i + 1);
+    k_a = __ldg(p.cu_k + i);
+    k_b = __ldg(p.cu_k + i + 1);
+    bool ok = 0 <= q_a && q_a <= q_b && q_b <= p.total_q && q_b - q_a <= p.n_q && 0 <= k_a && k_a <= k_b &&
+              k_b <= p.total_k;
+    if (ok) cnt = ((by_keys ? k_b - k_a : q_b - q_a) + rows - 1) / rows;
+    if (ok && by_keys && cnt > max_units) ok = false;
+    if (!ok) {
+      cnt = 0;
+      if (blockIdx.x == 0) atomicOr(p.status, kStatusBadSeqlens);
+    }
+  }
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (i == 0) scan[NW] = -1;
+  if (lane == 31) scan[w] = incl;
+  __syncthreads();
+  long long start = incl - cnt;
+  for (int j = 0; j < w; ++j) start += scan[j];
+  const long long blk = (long long)blockIdx.x;
+  if (cnt > 0 && blk >= start * p.heads && blk < (start + cnt) * p.heads) {
+    scan[NW] = i;
+    scan[NW + 1] = (int)(blk - start * p.heads);
+    scan[NW + 2] = cnt;
+    scan[NW + 3] = q_a;
+    scan[NW + 4] = q_b;
+    scan[NW + 5] = k_a;
+    scan[NW + 6] = k_b;
+  }
+  __syncthreads();
+  if (scan[NW] < 0) return false;
+  units = scan[NW + 2];
+  int h;
+  unit_of_block(scan[NW + 1], p.heads, units, h, unit, group);
+  s.b = 0;
+  s.h = h;
+  s.row0_q = scan[NW + 3];
+  s.n_q = scan[NW + 4] - s.row0_q;
+  s.row0_k = scan[NW + 5];
+  s.n_k = scan[NW + 6] - s.row0_k;
+  return true;
+}
+
 }  // namespace fa2

@@ -57,7 +57,7 @@ struct DbufConfig {
   static constexpr uint32_t OFF_BAR = OFF_V + VSTAGES * KV_BYTES;
   static constexpr uint32_t NUM_BARS = 24;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr uint32_t MISC_BYTES = 128;  // TMEM address, abort flag, CtaFacts
+  static constexpr uint32_t MISC_BYTES = 128 + 4 * kPackedScanWords;  // TMEM address, abort flag, CtaFacts; scan
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;
   static constexpr uint32_t TMEM_S = 0;     // + 64 * buffer
   static constexpr uint32_t TMEM_O = 128;
@@ -353,7 +353,10 @@ __device__ __forceinline__ void db_softmax(const DbufCtx& t, const KernelParams&
 // BAND: the first key a query row sees may depend on the row (a bounded left
 // window or a prefix); it selects the element mask's form.  SPLIT: split-key
 // mode (decoding; p.splits > 1), instantiated for the decode path only.
-template <int D, bool BF16, bool BAND, bool SPLIT = false>
+// PACKED: a packed batch whose grid holds only its real tiles
+// (p.packed_units); each CTA finds its sequence and tile from the offsets.
+// A template flag, so that the other kernels' code stays as it was.
+template <int D, bool BF16, bool BAND, bool SPLIT = false, bool PACKED = false>
 __global__ void __launch_bounds__(192, DbufConfig<D>::CTAS_PER_SM)
     fa2_fwd_dbuf_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -366,20 +369,31 @@ __global__ void __launch_bounds__(192, DbufConfig<D>::CTAS_PER_SM)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   CtaFacts* facts = reinterpret_cast<CtaFacts*>(smem + C::OFF_MISC + 16);
-  static_assert(16 + sizeof(CtaFacts) <= C::MISC_BYTES, "shared-memory misc area");
+  static_assert(16 + sizeof(CtaFacts) <= 128, "shared-memory misc area");
   const int warp = (int)(threadIdx.x >> 5);
   const int lane = (int)(threadIdx.x & 31);
 
   DbufCtx t;
   int bh, unit;
-  unit_of_block((int)blockIdx.x, p.bh, p.units, bh, unit);
+  static_assert(!(SPLIT && PACKED), "split-key mode runs on the plain grid");
   const int splits = SPLIT ? p.splits : 1;
+  // The whole CTA leaves together, before any barrier or TMEM set-up, when
+  // it has no tile, its sequence is malformed or shorter than this tile's rows.
+  // (The packed kernels keep the plain path behind a run-time test: built
+  // that way they measured 8 % faster on packed batches than built without.)
+  if (PACKED && p.packed_units) {
+    int units;
+    if (!packed_unit<C::THREADS>(p, C::BR, false, 0, kHeadGroup,
+                                 reinterpret_cast<int*>(smem + C::OFF_MISC + 128), t.seq, unit, units))
+      return;
+    bh = t.seq.h;   // t.bh serves split-key mode only
+  } else {
+    unit_of_block((int)blockIdx.x, p.bh, p.units, bh, unit);
+    if (!seq_info(p, bh, t.seq)) return;
+  }
   const int q_tile = unit / splits;
   t.bh = bh;
   t.split = unit - q_tile * splits;
-  // The whole CTA leaves together, before any barrier or TMEM set-up, when
-  // its sequence is malformed or shorter than this tile's rows.
-  if (!seq_info(p, bh, t.seq)) return;
   if (SPLIT && t.seq.n_k > p.split_base + splits * p.split_chunk) {   // a packed sequence the plan does not cover
     if (threadIdx.x == 0 && t.split == 0) atomicOr(p.status, kStatusBadSeqlens);
     return;
@@ -464,23 +478,27 @@ __global__ void __launch_bounds__(192, DbufConfig<D>::CTAS_PER_SM)
   }
 }
 
-template <int D, bool BF16, bool BAND, bool SPLIT = false>
+template <int D, bool BF16, bool BAND, bool SPLIT = false, bool PACKED = false>
 int launch_fwd_dbuf(const LaunchArgs& a) {
   using C = DbufConfig<D>;
-  auto kern = fa2_fwd_dbuf_kernel<D, BF16, BAND, SPLIT>;
+  auto kern = fa2_fwd_dbuf_kernel<D, BF16, BAND, SPLIT, PACKED>;
   static std::atomic<unsigned long long> configured{0};
   const int e = once_per_device(configured, [&]() -> int {
     return (int)cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
   });
   if (e != 0) return e;
   static_assert(C::BR == 128, "query rows per CTA: tile_geometry(d).cta_rows sizes the grid");
-  dim3 grid((unsigned)(a.p.bh * a.p.units));
+  dim3 grid((unsigned)(PACKED ? a.p.heads * a.p.packed_units : a.p.bh * a.p.units));
   kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
   return (int)cudaGetLastError();
 }
 
 template <int D>
 int launch_fwd_dbuf_dispatch(const LaunchArgs& a) {
+  if (a.p.packed_units) {
+    if (a.band) return a.bf16 ? launch_fwd_dbuf<D, true, true, false, true>(a) : launch_fwd_dbuf<D, false, true, false, true>(a);
+    return a.bf16 ? launch_fwd_dbuf<D, true, false, false, true>(a) : launch_fwd_dbuf<D, false, false, false, true>(a);
+  }
   if (a.band) return a.bf16 ? launch_fwd_dbuf<D, true, true>(a) : launch_fwd_dbuf<D, false, true>(a);
   return a.bf16 ? launch_fwd_dbuf<D, true, false>(a) : launch_fwd_dbuf<D, false, false>(a);
 }

@@ -49,11 +49,17 @@ struct KernelParams {
   int split_base;     // first key of chunk 0 (a multiple of the key tile)
   float* ws_o;        // [B*H][n_q][splits][d] partial O~
   float* ws_ml;       // [B*H][n_q][splits][2] partial (m, l), exp2 domain
+  int packed_units;   // packed batches of at most kPackedScanSeqs sequences: units per head over
+                      // all sequences (the grid is heads x packed_units); 0: bh x units
 };
 
 // Bit of the status word a forward kernel sets when a packed batch's row
 // offsets are out of range; that sequence is left unwritten.
 constexpr uint32_t kStatusBadSeqlens = 2u;
+
+// Packed batches of up to this many sequences launch only the tiles that
+// exist (each CTA's threads read one sequence's offsets each).
+constexpr int kPackedScanSeqs = 192;
 
 struct LaunchArgs {
   CUtensorMap tm_q, tm_k, tm_v;  // (d, rows, B*H) or (d, rows, H, B) maps, boxes of 64 columns

@@ -159,7 +159,11 @@ size_t fa2_fwd_params_size(void);
  * sequence with cu_seqlens_q[b] > cu_seqlens_q[b+1], an offset outside
  * [0, total_q] (or [0, total_k] for keys), or more than seqlen_q queries is
  * left unwritten and the next fa2_get_device_status returns
- * FA2_ERR_DEVICE_SEQLENS.  Rows of k and v outside a sequence may be read
+ * FA2_ERR_DEVICE_SEQLENS.  The other sequences are written, except where
+ * such offsets make in-range sequences' query rows overlap: a batch of at
+ * most 192 sequences launches one CTA per real 128-row tile (as many as
+ * non-overlapping sequences can hold), and tiles past that are skipped.
+ * Rows of k and v outside a sequence may be read
  * (key tiles are 128 rows) and are multiplied by P = 0, so they must hold
  * finite values; rows past total_k read as zero.  Deterministic.
  */
@@ -304,7 +308,9 @@ size_t fa2_bwd_workspace_bytes(int B, int H, int N, int d);
  * v's strides.  head_dim 64 or 128 (FA2_ERR_UNSUPPORTED otherwise).  Packed
  * batches: fwd.seqlen_k is the longest sequence's key count (it sizes the
  * grid; a sequence with more keys is left unwritten and reported as
- * FA2_ERR_DEVICE_SEQLENS), and rows of dq outside every sequence are set to
+ * FA2_ERR_DEVICE_SEQLENS; out-of-range offsets behave as in fa2_fwd_ex,
+ * with key tiles in place of query tiles), and rows of dq outside every
+ * sequence are set to
  * zero.  A key no query row sees gets dK = dV = 0; a query row that sees no
  * key gets dQ = 0.
  *

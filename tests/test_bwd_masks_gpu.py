@@ -165,6 +165,36 @@ def test_bwd_packed_sequences():
         rk += nk
 
 
+@pytest.mark.parametrize("d,dtype,nseq", [(64, sy.FP16, 192), (128, sy.BF16, 192), (128, sy.BF16, 193)])
+def test_bwd_packed_many_sequences(d, dtype, nseq):
+    """192 packed sequences (the grid holds one CTA per real key tile, each
+    finding its sequence from the offsets) and 193 (one CTA per sequence,
+    head and key tile of the longest), some empty: each sequence's gradients
+    match the oracle on its slice."""
+    H, wl, wr = 2, -1, 0
+    rng = np.random.default_rng(15800 + nseq + d)
+    lens = rng.integers(1, 300, nseq)
+    lens[::17] = 0
+    lens[7] = 300
+    total = int(lens.sum())
+    q, k, v, do = inputs(1, H, total, total, d, dtype, seed=15810 + nseq + d)
+    packed = [to_dev(np.ascontiguousarray(x[0].transpose(1, 0, 2)), dtype) for x in (q, k, v, do)]
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device="cuda")
+    pk = dict(cu_seqlens_q=cu, cu_seqlens_k=cu, max_seqlen_q=int(lens.max()), window_left=wl, window_right=wr)
+    o, lse = fa2.fa2_fwd_ex(packed[0], packed[1], packed[2], **pk)
+    grads = fa2.fa2_bwd_ex(packed[0], packed[1], packed[2], o, lse, packed[3], **pk, max_seqlen_k=int(lens.max()))
+    status_ok()
+    grads = [g.double().cpu().numpy() for g in grads]
+    row = 0
+    for i, n in enumerate(lens.tolist()):
+        if n:
+            sl = lambda x: np.ascontiguousarray(x[:, :, row:row + n])
+            ref = oracle.attention_bwd_masked(sl(q), sl(k), sl(v), sl(do), dtype, 1.0 / np.sqrt(d), wl, wr, 0)
+            got = [g[row:row + n].transpose(1, 0, 2)[None] for g in grads]
+            check(got, ref, dtype, "seq %d of %d (n=%d)" % (i, nseq, n))
+        row += n
+
+
 @pytest.mark.parametrize("Nq,Nk,mask,d,dtype", [
     (2048, 8192, (-1, 0, 0), 128, sy.BF16),     # a query chunk at the end of a long key sequence
     (4096, 4096, (511, 0, 0), 64, sy.FP16),     # sliding window of 512 keys

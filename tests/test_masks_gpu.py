@@ -203,6 +203,47 @@ def test_packed_sequences(d, dtype, mask):
         row += nq
 
 
+def _tile_search_grid(lens, rows=128):
+    """Whether the host sizes a packed batch's grid to its real tiles (each
+    CTA then finds its sequence and tile from the offsets): at most 192
+    sequences, and fewer tiles than one per sequence, head and tile of the
+    longest sequence."""
+    B, total = len(lens), int(np.sum(lens))
+    return B <= 192 and (total + (rows - 1) * B) // rows < B * ((int(np.max(lens)) + rows - 1) // rows)
+
+
+@pytest.mark.parametrize("nseq", [192, 193])
+def test_packed_many_sequences(nseq):
+    """192 packed sequences (the most for which the grid holds only real
+    tiles) and 193 (one CTA per sequence, head and tile of the longest, most
+    of them empty), some of them empty: each sequence equals the oracle on
+    its own slice."""
+    H, d, dtype, wl, wr = 2, 128, sy.BF16, -1, 0
+    rng = np.random.default_rng(9700 + nseq)
+    lens = rng.integers(1, 300, nseq)
+    lens[::17] = 0
+    lens[7] = 300
+    assert _tile_search_grid(lens) == (nseq <= 192)
+    total = int(lens.sum())
+    q, k, v = qkv(1, H, total, total, d, dtype, seed=9710 + nseq)
+    qp, kp, vp = (np.ascontiguousarray(x[0].transpose(1, 0, 2)) for x in (q, k, v))   # [total, H, d]
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device="cuda")
+    o, lse = fa2.fa2_fwd_ex(to_dev(qp, dtype), to_dev(kp, dtype), to_dev(vp, dtype), window_left=wl,
+                            window_right=wr, cu_seqlens_q=cu, cu_seqlens_k=cu, max_seqlen_q=int(lens.max()))
+    status_ok()
+    o = o.double().cpu().numpy()
+    lse = lse.double().cpu().numpy()
+    row = 0
+    for i, n in enumerate(lens.tolist()):
+        if n:
+            sl = lambda x: np.ascontiguousarray(x[:, :, row:row + n])
+            o_orc, l_orc = oracle.attention_fwd_masked(sl(q), sl(k), sl(v), dtype, 1.0 / np.sqrt(d),
+                                                       window_left=wl, window_right=wr)
+            og = o[row:row + n].transpose(1, 0, 2)[None]
+            check(og, lse[None, :, row:row + n], o_orc, l_orc, dtype, "seq %d of %d (n=%d)" % (i, nseq, n))
+        row += n
+
+
 def _unpacked(qd, kd, vd, q_rows, k_rows, **mask):
     sl = lambda x, r: x[r[0]:r[1]].permute(1, 0, 2).unsqueeze(0)
     o, lse = fa2.fa2_fwd_ex(sl(qd, q_rows), sl(kd, k_rows), sl(vd, k_rows), **mask)
