@@ -170,6 +170,12 @@ def fa2_fwd(q, k, v, o=None, lse=None, scale=None, causal=False, stream=None):
     return o, lse
 
 
+def _same_layout(a, b) -> bool:
+    """Same shape, and the same stride wherever a dimension has more than one
+    element (a size-1 dimension's stride addresses nothing)."""
+    return a.shape == b.shape and all(sa == sb for sa, sb, n in zip(a.stride(), b.stride(), a.shape) if n > 1)
+
+
 def _general_params(q, k, v, o, lse, scale, window_left, window_right, prefix_len, cu_seqlens_q, cu_seqlens_k,
                     max_seqlen_q, max_seqlen_k):
     """Marshal tensors into an Fa2FwdParams (allocating o and lse when not given)."""
@@ -329,7 +335,7 @@ def fa2_bwd_ex(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, workspace=None,
     fp, _, _ = _general_params(q, k, v, o, lse, scale, window_left, window_right, prefix_len, cu_seqlens_q,
                                cu_seqlens_k, max_seqlen_q, max_seqlen_k)
     p.fwd = fp
-    if dout.shape != o.shape or dout.stride() != o.stride() or dout.dtype != o.dtype:
+    if not _same_layout(dout, o) or dout.dtype != o.dtype:
         raise ValueError("dout must have o's shape, strides and dtype")
     like = lambda t: torch.empty_strided(t.shape, t.stride(), dtype=t.dtype, device=t.device)
     dq = like(q) if dq is None else dq

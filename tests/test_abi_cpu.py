@@ -285,3 +285,17 @@ def test_bwd_ex_bad_arguments_rejected(lib, kw, code):
 
 def test_bwd_ex_null_params(lib):
     assert lib.fa2_bwd_ex(None, None) == fa2.FA2_ERR_INVALID_ARG
+
+
+def test_same_layout_ignores_strides_of_size_one_dimensions():
+    """dout must share o's layout; a size-1 dimension's stride addresses
+    nothing, so it may differ (numpy gives a transposed [T, 1, d] view the
+    stride of the dimension it came from)."""
+    import torch
+    from exact_tiled_attention_fa2_gb300 import _same_layout
+    a = torch.empty(5, 1, 8)
+    b = torch.empty(5 * 40).as_strided((5, 1, 8), (8, 40, 1))
+    assert a.stride() != b.stride() and _same_layout(a, b)
+    c = torch.empty(5 * 16).as_strided((5, 1, 8), (16, 8, 1))   # rows 16 apart, not 8
+    assert not _same_layout(a, c)
+    assert not _same_layout(a, torch.empty(5, 2, 8))

@@ -195,6 +195,55 @@ def test_bwd_packed_many_sequences(d, dtype, nseq):
         row += n
 
 
+@pytest.mark.parametrize("trial", range(4))
+def test_bwd_packed_random_mixes_match_unpacked(trial):
+    """Random packed batches (up to 200 sequences, skewed lengths, empty ones,
+    N_q != N_k): each sequence's dK and dV bit-equal the unpacked call on that
+    sequence alone (summed inside one CTA in a fixed order), dQ equals it to
+    rounding (fp32 reduce-adds land in run-dependent order), and dq rows
+    outside every sequence are zero."""
+    rng = np.random.default_rng(15900 + trial)
+    nseq = int(rng.choice([3, 40, 192, 200]))
+    d, dtype = [(64, sy.FP16), (128, sy.BF16)][trial % 2]
+    H = int(rng.integers(1, 3))
+    wl, wr = [(-1, 0), (-1, -1), (int(rng.integers(0, 300)), 0), (-1, 0)][trial]
+    top = 1500 if nseq <= 40 else 300
+    lq = np.minimum(rng.exponential(top / 4, nseq).astype(np.int64), top)
+    lk = np.where(rng.random(nseq) < 0.5, lq, np.minimum(rng.exponential(top / 4, nseq).astype(np.int64), top))
+    lq[rng.random(nseq) < 0.1] = 0
+    lq[0], lk[0] = max(int(lq[0]), 1), max(int(lk[0]), 1)
+    tq, tk, tail = int(lq.sum()), int(lk.sum()), 3
+    q, k, v, do = inputs(1, H, tq + tail, tk, d, dtype, seed=15910 + trial)
+    tq_, tk_, tv_, tdo_ = (to_dev(np.ascontiguousarray(x[0].transpose(1, 0, 2)), dtype) for x in (q, k, v, do))
+    cu_q = torch.tensor(np.concatenate([[0], np.cumsum(lq)]), dtype=torch.int32, device="cuda")
+    cu_k = torch.tensor(np.concatenate([[0], np.cumsum(lk)]), dtype=torch.int32, device="cuda")
+    mask = dict(window_left=wl, window_right=wr)
+    pk = dict(cu_seqlens_q=cu_q, cu_seqlens_k=cu_k, max_seqlen_q=int(lq.max()))
+    o, lse = fa2.fa2_fwd_ex(tq_, tk_, tv_, **mask, **pk)
+    dq, dk, dv = fa2.fa2_bwd_ex(tq_, tk_, tv_, o, lse, tdo_, **mask, **pk, max_seqlen_k=int(lk.max()))
+    status_ok()
+    assert torch.all(dq[tq:] == 0)
+    view = lambda x, a, n: x[a:a + n].permute(1, 0, 2).unsqueeze(0)
+    rq = rk = 0
+    for i, (nq, nk) in enumerate(zip(lq.tolist(), lk.tolist())):
+        label = "trial %d seq %d of %d (nq=%d nk=%d) d=%d" % (trial, i, nseq, nq, nk, d)
+        if nq and nk:
+            sq, sk, sv, sdo = view(tq_, rq, nq), view(tk_, rk, nk), view(tv_, rk, nk), view(tdo_, rq, nq)
+            ou, lu = fa2.fa2_fwd_ex(sq, sk, sv, **mask)
+            gu = fa2.fa2_bwd_ex(sq, sk, sv, ou, lu, torch.empty_like(ou).copy_(sdo), **mask)   # dout in o's layout
+            status_ok()
+            assert torch.equal(view(dk, rk, nk), gu[1]) and torch.equal(view(dv, rk, nk), gu[2]), label + ": dK / dV"
+            ref = gu[0].float()
+            err = float((view(dq, rq, nq).float() - ref).abs().max())
+            assert err <= 1e-2 * max(float(ref.abs().max()), 1e-6), label + ": dQ %.3e" % err
+        elif nk:
+            assert torch.all(dk[rk:rk + nk] == 0) and torch.all(dv[rk:rk + nk] == 0), label
+        elif nq:
+            assert torch.all(dq[rq:rq + nq] == 0), label
+        rq += nq
+        rk += nk
+
+
 @pytest.mark.parametrize("Nq,Nk,mask,d,dtype", [
     (2048, 8192, (-1, 0, 0), 128, sy.BF16),     # a query chunk at the end of a long key sequence
     (4096, 4096, (511, 0, 0), 64, sy.FP16),     # sliding window of 512 keys

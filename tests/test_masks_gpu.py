@@ -244,6 +244,50 @@ def test_packed_many_sequences(nseq):
         row += n
 
 
+@pytest.mark.parametrize("trial", range(8))
+def test_packed_random_mixes_bit_equal_unpacked(trial):
+    """Random packed batches (1 to 200 sequences, skewed lengths with empty
+    ones, N_q != N_k, any head count, head dim and mask): every sequence's
+    rows bit-equal the unpacked call on that sequence alone, whichever grid
+    the batch gets; rows outside every sequence stay untouched."""
+    rng = np.random.default_rng(9800 + trial)
+    nseq = int(rng.choice([1, 2, 7, 31, 64, 150, 192, 200]))
+    d, dtype = [(64, sy.FP16), (128, sy.BF16), (256, sy.FP16), (128, sy.FP16)][trial % 4]
+    H = int(rng.integers(1, 4))
+    wl, wr, pre = [(-1, 0, 0), (-1, -1, 0), (int(rng.integers(0, 300)), 0, 0), (-1, 0, int(rng.integers(1, 200)))][trial % 4]
+    scale_len = 2000 if nseq <= 31 else 400
+    lq = np.minimum(rng.exponential(scale_len / 4, nseq).astype(np.int64), scale_len)
+    lk = np.where(rng.random(nseq) < 0.5, lq, np.minimum(rng.exponential(scale_len / 4, nseq).astype(np.int64), scale_len))
+    lq[rng.random(nseq) < 0.1] = 0
+    lq[0] = max(int(lq[0]), 1)
+    lk[0] = max(int(lk[0]), 1)
+    tq, tk, tail = int(lq.sum()), int(lk.sum()), 5
+    q, k, v = qkv(1, H, tq + tail, max(tk, 1), d, dtype, seed=9810 + trial)
+    qp, kp, vp = (np.ascontiguousarray(x[0].transpose(1, 0, 2)) for x in (q, k, v))
+    qd, kd, vd = to_dev(qp, dtype), to_dev(kp, dtype), to_dev(vp, dtype)
+    cu_q = torch.tensor(np.concatenate([[0], np.cumsum(lq)]), dtype=torch.int32, device="cuda")
+    cu_k = torch.tensor(np.concatenate([[0], np.cumsum(lk)]), dtype=torch.int32, device="cuda")
+    mask = dict(window_left=wl, window_right=wr, prefix_len=pre)
+    o = torch.full(qd.shape, 3.0, dtype=qd.dtype, device="cuda")
+    lse = torch.full((H, qd.shape[0]), 4.0, dtype=torch.float32, device="cuda")
+    fa2.fa2_fwd_ex(qd, kd, vd, o=o, lse=lse, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k, max_seqlen_q=int(lq.max()), **mask)
+    status_ok()
+    assert torch.all(o[tq:] == 3.0) and torch.all(lse[:, tq:] == 4.0)
+    rq = rk = 0
+    for i, (nq, nk) in enumerate(zip(lq.tolist(), lk.tolist())):
+        if nq:
+            og = o[rq:rq + nq].permute(1, 0, 2).unsqueeze(0)
+            lg = lse[:, rq:rq + nq].unsqueeze(0)
+            label = "trial %d seq %d of %d (nq=%d nk=%d) d=%d mask=%s" % (trial, i, nseq, nq, nk, d, (wl, wr, pre))
+            if nk == 0:
+                assert torch.all(og == 0) and torch.all(torch.isneginf(lg)), label
+            else:
+                ou, lu = _unpacked(qd, kd, vd, (rq, rq + nq), (rk, rk + nk), **mask)
+                assert torch.equal(og, ou) and torch.equal(lg, lu), label + ": packed != unpacked"
+        rq += nq
+        rk += nk
+
+
 def _unpacked(qd, kd, vd, q_rows, k_rows, **mask):
     sl = lambda x, r: x[r[0]:r[1]].permute(1, 0, 2).unsqueeze(0)
     o, lse = fa2.fa2_fwd_ex(sl(qd, q_rows), sl(kd, k_rows), sl(vd, k_rows), **mask)
