@@ -76,3 +76,40 @@ def test_general_options_parse_and_count():
     assert g["seqlen_q"] == 1 and g["seqlen_k"] == w.N and g["label"].startswith("decode 1 row vs 16384 keys")
     # one causal row facing the last of N keys sees all of them: K + V read once dominate the bytes
     assert g["input_bytes"] == (1 + 2 * w.N) * w.H * w.d * 2
+
+
+def test_traffic_record_matches_kernel_source_and_workload(tmp_path, monkeypatch):
+    """`roofline.traffic` comes only from a record taken on the same kernel
+    source (hash), kernel name and workload; any other record, or one without
+    a kernel name (an earlier forward kernel's), gives null."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    hashes = {}
+
+    def fake_hash(names=None):
+        key = tuple(names or bench.KERNEL_SOURCES)
+        return hashes.setdefault(key, "h%d" % len(hashes))
+
+    monkeypatch.setattr(bench, "kernel_source_hash", fake_hash)
+    fwd, bwd = fake_hash(bench.KERNEL_SOURCES), fake_hash(bench.BWD_KERNEL_SOURCES)
+    assert fwd != bwd
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic_per_launch.txt").write_text(
+        "# comment line\n"
+        "kernel_sha=%s workload=4 bytes_per_launch=111\n" % fwd +                          # no kernel name
+        "kernel_sha=old0 workload=4 kernel=fa2_fwd_dbuf_kernel bytes_per_launch=222\n"
+        "kernel_sha=%s workload=3 kernel=fa2_fwd_dbuf_kernel bytes_per_launch=333\n" % fwd +
+        "kernel_sha=%s workload=4 kernel=fa2_fwd_dbuf_kernel bytes_per_launch=444\n" % fwd +
+        "kernel_sha=%s workload=4 kernel=fa2_bwd_kernel bytes_per_launch=555\n" % fwd +       # forward hash
+        "kernel_sha=%s workload=4 kernel=fa2_bwd_kernel bytes_per_launch=666\n" % bwd)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.recorded_traffic(4) == 444.0
+    assert bench.recorded_traffic(3) == 333.0
+    assert bench.recorded_traffic(2) is None
+    assert bench.recorded_traffic(4, "fa2_bwd_kernel") == 666.0
+    assert bench.recorded_traffic(4, "fa2_decode_kernel") is None
+    hashes[tuple(bench.KERNEL_SOURCES)] = "changed"          # a kernel source edited since the capture
+    assert bench.recorded_traffic(4) is None
+    (tmp_path / "profiles" / "traffic_per_launch.txt").unlink()
+    assert bench.recorded_traffic(4, "fa2_bwd_kernel") is None
