@@ -272,6 +272,12 @@ def step_input_bytes(w: sy.Workload, gen, backward: bool) -> int:
     return fwd + (rows_q * (2 * w.d * 2 + 4) if backward else 0)
 
 
+def flush_l2(in_bytes: int, mode: str) -> bool:
+    """Whether timed launches overwrite the L2 first: `mode` "on", or "auto"
+    with step inputs that fit in the L2 (they would otherwise be read warm)."""
+    return mode == "on" or (mode == "auto" and in_bytes <= L2_BYTES)
+
+
 def l2_note(in_bytes: int, flush: bool) -> str:
     if flush:
         return ("inputs (%.0f MB) not larger than the 129 MB L2: L2 overwritten (a %.0f MB write) before each "
@@ -522,7 +528,7 @@ def main():
     # inputs that fit in the L2 would be timed warm: overwrite the L2 before
     # every timed launch instead, outside the launch's own timing events
     in_bytes = step_input_bytes(w, gen, args.backward)
-    flush = args.flush_l2 == "on" or (args.flush_l2 == "auto" and in_bytes <= L2_BYTES)
+    flush = flush_l2(in_bytes, args.flush_l2)
     fbuf = None
     if flush:
         args.no_graph = True

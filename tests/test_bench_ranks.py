@@ -113,3 +113,19 @@ def test_traffic_record_matches_kernel_source_and_workload(tmp_path, monkeypatch
     assert bench.recorded_traffic(4) is None
     (tmp_path / "profiles" / "traffic_per_launch.txt").unlink()
     assert bench.recorded_traffic(4, "fa2_bwd_kernel") is None
+
+
+def test_l2_flush_follows_input_size():
+    """Inputs that fit in the 129 MB L2 are timed after an L2 overwrite:
+    workloads 1, 2 and 5 forward.  Workloads 3 and 4 are larger, and so is
+    workload 2's backward step, which also reads o, dO and L."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from exact_tiled_attention_fa2_gb300 import synthetic as sy
+
+    fwd = {i: bench.flush_l2(bench.step_input_bytes(sy.WORKLOADS[i], None, False), "auto") for i in range(1, 6)}
+    assert fwd == {1: True, 2: True, 3: False, 4: False, 5: True}
+    bwd = {i: bench.flush_l2(bench.step_input_bytes(sy.WORKLOADS[i], None, True), "auto") for i in range(1, 6)}
+    assert bwd == {1: True, 2: False, 3: False, 4: False, 5: True}
+    assert bench.step_input_bytes(sy.WORKLOADS[4], None, False) == 3 * 32 * 16384 * 128 * 2
+    assert bench.flush_l2(10 ** 12, "on") and not bench.flush_l2(1, "off")
