@@ -431,7 +431,7 @@ def launch_mode(args):
     return "one CUDA graph replaying the timed launches" if not args.no_graph else "one launch per step from Python"
 
 
-def main():
+def build_parser() -> argparse.ArgumentParser:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
@@ -461,6 +461,11 @@ def main():
                    help="pack the B*N query tokens as this many sequences of seeded random lengths")
     g.add_argument("--decode-rows", type=int, default=0,
                    help="time fa2_decode: this many query rows (<= 8) per (b, h) against the workload's N keys")
+    return ap
+
+
+def main():
+    ap = build_parser()
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -129,3 +129,28 @@ def test_l2_flush_follows_input_size():
     assert bwd == {1: True, 2: False, 3: False, 4: False, 5: True}
     assert bench.step_input_bytes(sy.WORKLOADS[4], None, False) == 3 * 32 * 16384 * 128 * 2
     assert bench.flush_l2(10 ** 12, "on") and not bench.flush_l2(1, "off")
+
+
+def test_profile_commands_parse():
+    """Every bench command a profile summary records parses with the bench's
+    own options (and keeps at least 3 warm-up steps)."""
+    import glob
+    import shlex
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    found = 0
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        text = open(path).read().replace("\\\n", " ")
+        for line in text.splitlines():
+            if "python bench.py" not in line:
+                continue
+            cmd = line.split("python bench.py", 1)[1]
+            for stop in ("&&", ">", "|", "`"):
+                cmd = cmd.split(stop, 1)[0]
+            argv = shlex.split(cmd)
+            args = bench.build_parser().parse_args(argv)
+            assert args.warmup >= 3, (path, argv)
+            found += 1
+    assert found >= 8
