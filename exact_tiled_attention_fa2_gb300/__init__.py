@@ -356,6 +356,25 @@ def fa2_bwd_ex(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, workspace=None,
     return dq, dk, dv
 
 
+def _check_host_tensors(q, k, v, o, lse, where):
+    """Shapes and dtypes of the host-buffer entry points' tensors, checked before
+    any pointer is passed on: the library copies B*H*N*d 16-bit elements out of
+    q, k, v and into o, and B*H*N floats into lse, so a smaller or differently
+    typed tensor would be read or written past its end.  Returns (B, H, N, d)."""
+    import torch
+    for t in (q, k, v, o, lse):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s takes contiguous host tensors" % where)
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape or o.shape != q.shape:
+        raise ValueError("%s: q, k, v and o must share one [B, H, N, d] shape" % where)
+    if q.element_size() != 2 or any(t.dtype != q.dtype for t in (k, v, o)):
+        raise ValueError("%s: q, k, v and o must share one 16-bit dtype" % where)
+    B, H, N, d = q.shape
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N):
+        raise ValueError("%s: lse must be float32 of shape [B, H, N]" % where)
+    return B, H, N, d
+
+
 def fa2_fwd_host_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
     return int(load_library().fa2_fwd_host_workspace_bytes(B, H, N, d))
 
@@ -368,13 +387,12 @@ def fa2_fwd_host(q, k, v, o, lse, workspace, scale=None, causal=False, dtype=Non
     into the given host tensors and synchronises the stream.
     """
     import torch
-    B, H, N, d = q.shape
+    B, H, N, d = _check_host_tensors(q, k, v, o, lse, "fa2_fwd_host")
     code = _dtype_code(q) if dtype is None else int(dtype)
     if scale is None:
         scale = 1.0 / float(d) ** 0.5
-    for t in (q, k, v, o, lse):
-        if t.is_cuda or not t.is_contiguous():
-            raise ValueError("fa2_fwd_host takes contiguous host tensors")
+    if not workspace.is_cuda or workspace.dtype != torch.uint8:
+        raise ValueError("fa2_fwd_host: workspace must be a CUDA uint8 tensor")
     rc = load_library().fa2_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                                      workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                      B, H, N, d, float(scale), int(bool(causal)), code,
@@ -395,13 +413,10 @@ def fa2_fwd_host_noalloc(q, k, v, o, lse, scale=None, causal=False, dtype=None, 
     race.  The first call on a device looks up the array's address there.
     """
     import torch
-    B, H, N, d = q.shape
+    B, H, N, d = _check_host_tensors(q, k, v, o, lse, "fa2_fwd_host_noalloc")
     code = _dtype_code(q) if dtype is None else int(dtype)
     if scale is None:
         scale = 1.0 / float(d) ** 0.5
-    for t in (q, k, v, o, lse):
-        if t.is_cuda or not t.is_contiguous():
-            raise ValueError("fa2_fwd_host_noalloc takes contiguous host tensors")
     rc = load_library().fa2_fwd_host_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                              lse.data_ptr(), B, H, N, d, float(scale), int(bool(causal)), code,
                                              _stream_handle(stream, torch.cuda.current_device()))

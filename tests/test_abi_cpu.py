@@ -35,7 +35,8 @@ def test_header_declares_entry_points():
     names = _declared_functions()
     for required in ("fa2_fwd", "fa2_fwd_host", "fa2_fwd_host_workspace_bytes", "fa2_get_device_status",
                      "fa2_status_string", "fa2_version", "fa2_selftest_wait_timeout", "fa2_bwd",
-                     "fa2_bwd_workspace_bytes"):
+                     "fa2_bwd_workspace_bytes", "fa2_fwd_host_noalloc", "fa2_fwd_ex", "fa2_bwd_ex",
+                     "fa2_decode"):
         assert required in names
 
 
@@ -74,8 +75,7 @@ def _call(lib, q=A, k=2 * A, v=3 * A, o=4 * A, lse=5 * A, **kw):
     (dict(causal=2), fa2.FA2_ERR_INVALID_ARG),
     (dict(scale=float("nan")), fa2.FA2_ERR_INVALID_ARG),
     (dict(scale=float("inf")), fa2.FA2_ERR_INVALID_ARG),
-    (dict(scale=0.0), fa2.FA2_ERR_INVALID_ARG),
-    (dict(scale=-0.125), fa2.FA2_ERR_INVALID_ARG),
+    (dict(scale=float("-inf")), fa2.FA2_ERR_INVALID_ARG),
     (dict(d=32), fa2.FA2_ERR_UNSUPPORTED),
     (dict(d=96), fa2.FA2_ERR_UNSUPPORTED),
     (dict(d=512), fa2.FA2_ERR_UNSUPPORTED),
@@ -113,6 +113,42 @@ def test_host_entry_point_checks(lib):
     assert f(A, A, A, A, A, 6 * A + 16, ws, 1, 2, 64, 64, 0.125, 0, 0, None) == fa2.FA2_ERR_MISALIGNED
     assert f(0, A, A, A, A, 6 * A, ws, 1, 2, 64, 64, 0.125, 0, 0, None) == fa2.FA2_ERR_INVALID_ARG
     assert f(A, A, A, A, A, 6 * A, ws, 1, 2, 64, 64, 0.125, 0, 5, None) == fa2.FA2_ERR_INVALID_ARG
+
+
+def test_noalloc_host_entry_point_checks(lib):
+    # every check runs before any CUDA call, so the stand-in pointers are never touched
+    f = lib.fa2_fwd_host_noalloc
+    assert f(A, A, A, A, 0, 1, 2, 64, 64, 0.125, 0, 0, None) == fa2.FA2_ERR_INVALID_ARG     # null lse
+    assert f(0, A, A, A, A, 1, 2, 64, 64, 0.125, 0, 0, None) == fa2.FA2_ERR_INVALID_ARG     # null q
+    assert f(A, A, A, A, A, 1, 2, 64, 96, 0.125, 0, 0, None) == fa2.FA2_ERR_UNSUPPORTED     # head dim 96
+    assert f(A, A, A, A, A, 1, 2, 64, 64, float("nan"), 0, 0, None) == fa2.FA2_ERR_INVALID_ARG
+    # B1 H16 N4096 d128 needs 64 MiB + 256 KiB of staging, beyond the 32 MiB array
+    assert fa2.fa2_fwd_host_workspace_bytes(1, 16, 4096, 128) > fa2.FA2_NOALLOC_SCRATCH_BYTES
+    assert f(A, A, A, A, A, 1, 16, 4096, 128, 0.088, 1, 0, None) == fa2.FA2_ERR_SCRATCH_LIMIT
+
+
+def test_host_wrappers_check_shapes_and_dtypes():
+    # the Python host wrappers refuse tensors the library would read or write past their ends
+    import torch
+    q = torch.zeros((1, 2, 64, 64), dtype=torch.float16)
+    lse = torch.zeros((1, 2, 64), dtype=torch.float32)
+    small = torch.zeros((1, 2, 32, 64), dtype=torch.float16)
+    bad = [
+        dict(k=small),                                          # k smaller than q
+        dict(o=small),                                          # o smaller than q
+        dict(o=torch.zeros((1, 2, 64, 64), dtype=torch.float32)),   # fp32 o
+        dict(v=q.to(torch.bfloat16)),                           # mixed dtypes
+        dict(lse=torch.zeros((1, 2, 64), dtype=torch.float16)),     # 16-bit lse
+        dict(lse=torch.zeros((1, 2, 63), dtype=torch.float32)),     # short lse
+        dict(q=torch.zeros((2, 64, 64), dtype=torch.float16)),      # not 4-D
+    ]
+    for kw in bad:
+        t = dict(q=q, k=q.clone(), v=q.clone(), o=q.clone(), lse=lse)
+        t.update(kw)
+        with pytest.raises(ValueError):
+            fa2.fa2_fwd_host_noalloc(t["q"], t["k"], t["v"], t["o"], t["lse"])
+        with pytest.raises(ValueError):
+            fa2.fa2_fwd_host(t["q"], t["k"], t["v"], t["o"], t["lse"], torch.zeros(16, dtype=torch.uint8))
 
 
 def test_selftest_limit_checked(lib):

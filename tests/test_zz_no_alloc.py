@@ -2,7 +2,8 @@
 allocate device memory (their device memory is reserved by another allocator,
 or they must not call an allocator that may synchronise the device).  It
 stages q, k, v, o and lse in the library's static device array instead of a
-caller-provided workspace, so its results must equal those of fa2_fwd_host.
+caller-provided workspace and runs the same kernel on the same inputs, so its
+results must equal fa2_fwd_host's bit for bit.
 
 Collected last on purpose (file name), and independent of every other test:
 it builds and loads the library itself.
@@ -14,6 +15,7 @@ import pytest
 import torch
 
 import exact_tiled_attention_fa2_gb300 as fa2
+import oracle
 from exact_tiled_attention_fa2_gb300 import build as fa2_build
 from exact_tiled_attention_fa2_gb300 import synthetic as sy
 
@@ -36,27 +38,59 @@ def _host(bits, dtype):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(TORCH_DT[dtype]).pin_memory()
 
 
+def _noalloc(lib, q, k, v, B, H, N, d, dtype, causal):
+    o = torch.empty((B, H, N, d), dtype=TORCH_DT[dtype]).pin_memory()
+    lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream()
+    rc = lib.fa2_fwd_host_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                  B, H, N, d, ctypes.c_float(1.0 / np.sqrt(d)), int(causal), dtype,
+                                  ctypes.c_void_p(stream.cuda_stream))
+    assert rc == fa2.FA2_OK, fa2.fa2_status_string(rc)
+    return o, lse
+
+
+def _with_workspace(q, k, v, B, H, N, d, dtype, causal):
+    o = torch.empty((B, H, N, d), dtype=TORCH_DT[dtype]).pin_memory()
+    lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    ws = torch.empty(fa2.fa2_fwd_host_workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+    fa2.fa2_fwd_host(q, k, v, o, lse, ws, scale=1.0 / np.sqrt(d), causal=causal)
+    return o, lse
+
+
+def _check_oracle(o, lse, bits, B, H, N, d, dtype, causal):
+    o_ref, lse_ref = oracle.attention_fwd(*bits, dtype, 1.0 / np.sqrt(d), causal)
+    eo = float(np.abs(o.double().numpy() - o_ref).max())
+    el = float(np.abs(lse.double().numpy() - lse_ref).max())
+    assert eo <= TOL_O[dtype] and el <= TOL_LSE, (eo, el)
+
+
 def test_noalloc_matches_workspace_entry_point_on_two_calls(lib):
-    # two different problems back to back: the second call must not see the first one's data
-    cases = [(1, 4, 1000, 128, sy.BF16, True, 9101), (2, 3, 777, 64, sy.FP16, False, 9102)]
-    for B, H, N, d, dtype, causal, seed in cases:
-        assert fa2.fa2_fwd_host_workspace_bytes(B, H, N, d) <= fa2.FA2_NOALLOC_SCRATCH_BYTES
-        q, k, v = (_host(x, dtype) for x in sy.make_qkv(B, H, N, d, dtype, seed))
-        scale = 1.0 / np.sqrt(d)
-        o_a = torch.empty((B, H, N, d), dtype=TORCH_DT[dtype]).pin_memory()
-        l_a = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-        stream = torch.cuda.current_stream()
-        rc = lib.fa2_fwd_host_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o_a.data_ptr(), l_a.data_ptr(),
-                                      B, H, N, d, ctypes.c_float(scale), int(causal), dtype,
-                                      ctypes.c_void_p(stream.cuda_stream))
-        assert rc == fa2.FA2_OK, fa2.fa2_status_string(rc)
-        o_b = torch.empty_like(o_a).pin_memory()
-        l_b = torch.empty_like(l_a).pin_memory()
-        ws = torch.empty(fa2.fa2_fwd_host_workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
-        fa2.fa2_fwd_host(q, k, v, o_b, l_b, ws, scale=scale, causal=causal)
-        assert torch.isfinite(o_a.float()).all() and torch.isfinite(l_a).all()
-        assert (o_a.double() - o_b.double()).abs().max().item() <= TOL_O[dtype]
-        assert (l_a.double() - l_b.double()).abs().max().item() <= TOL_LSE
+    # call 1: a causal bf16 problem
+    B, H, N, d, dtype, causal = 1, 4, 1000, 128, sy.BF16, True
+    assert fa2.fa2_fwd_host_workspace_bytes(B, H, N, d) <= fa2.FA2_NOALLOC_SCRATCH_BYTES
+    bits = sy.make_qkv(B, H, N, d, dtype, 9101)
+    q, k, v = (_host(x, dtype) for x in bits)
+    o_a, l_a = _noalloc(lib, q, k, v, B, H, N, d, dtype, causal)
+    o_b, l_b = _with_workspace(q, k, v, B, H, N, d, dtype, causal)
+    assert torch.equal(o_a, o_b) and torch.equal(l_a, l_b)
+    _check_oracle(o_a, l_a, bits, B, H, N, d, dtype, causal)
+
+    # the array keeps the last call's contents: fill every byte call 2 will use
+    # with NaN through a problem at least as large whose inputs are all NaN
+    nan = torch.full((B, H, N, d), float("nan"), dtype=TORCH_DT[dtype]).pin_memory()
+    _noalloc(lib, nan, nan, nan, B, H, N, d, dtype, False)
+
+    # call 2: a smaller fp16 problem must see none of that: finite, equal to the
+    # workspace entry point, and within the tolerances of the oracle
+    B, H, N, d, dtype, causal = 2, 3, 777, 64, sy.FP16, False
+    assert fa2.fa2_fwd_host_workspace_bytes(B, H, N, d) <= fa2.fa2_fwd_host_workspace_bytes(1, 4, 1000, 128)
+    bits = sy.make_qkv(B, H, N, d, dtype, 9102)
+    q, k, v = (_host(x, dtype) for x in bits)
+    o_a, l_a = _noalloc(lib, q, k, v, B, H, N, d, dtype, causal)
+    assert torch.isfinite(o_a.float()).all() and torch.isfinite(l_a).all()
+    o_b, l_b = _with_workspace(q, k, v, B, H, N, d, dtype, causal)
+    assert torch.equal(o_a, o_b) and torch.equal(l_a, l_b)
+    _check_oracle(o_a, l_a, bits, B, H, N, d, dtype, causal)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(lib):
