@@ -210,7 +210,7 @@ int check_shape(int B, int H, int N, int d, float scale, int causal, int dtype) 
   if (dtype != FA2_FP16 && dtype != FA2_BF16) return FA2_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || N < 1) return FA2_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA2_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || !(scale > 0.f)) return FA2_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA2_ERR_INVALID_ARG;
   if (d != 64 && d != 128 && d != 256) return FA2_ERR_UNSUPPORTED;
   // one block per (head, query tile) in a 1-D grid
   if ((long long)B * (long long)H * (long long)((N + 127) / 128) > INT_MAX) return FA2_ERR_UNSUPPORTED;
@@ -287,7 +287,7 @@ struct Prepared {
 int prepare(const fa2_fwd_params& a, int units_rows, Prepared& out, const Extent* scratch = nullptr) {
   if (a.dtype != FA2_FP16 && a.dtype != FA2_BF16) return FA2_ERR_INVALID_ARG;
   if (a.batch < 1 || a.heads < 1 || a.seqlen_q < 1) return FA2_ERR_INVALID_ARG;
-  if (!std::isfinite(a.scale) || !(a.scale > 0.f)) return FA2_ERR_INVALID_ARG;
+  if (!std::isfinite(a.scale)) return FA2_ERR_INVALID_ARG;
   if (a.window_left < -1 || a.window_right < -1 || a.prefix_len < 0) return FA2_ERR_INVALID_ARG;
   const int d = a.head_dim;
   if (d != 64 && d != 128 && d != 256) return FA2_ERR_UNSUPPORTED;
@@ -614,7 +614,10 @@ int check_host_args(const void* q_host, const void* k_host, const void* v_host, 
   return FA2_OK;
 }
 
-// Whole problem in one pass on `stream`: copy in, forward, copy out, synchronise.
+// Whole problem in one pass on `stream`: copy in, forward, copy out,
+// synchronise.  Every return after the first queued copy -- an error
+// included -- first synchronises `stream`, so no copy into the workspace or
+// the caller's host buffers is still in flight when the call returns.
 int host_forward_serial(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
                         void* workspace, int B, int H, int N, int d, float scale, int causal, int dtype,
                         void* stream) {
@@ -627,15 +630,19 @@ int host_forward_serial(const void* q_host, const void* k_host, const void* v_ho
   void* od = w + 3 * align256(tb);
   float* ld = reinterpret_cast<float*>(w + 4 * align256(tb));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto drained = [&](int status) {
+    cudaStreamSynchronize(s);
+    return status;
+  };
   if (cudaMemcpyAsync(qd, q_host, tb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(kd, k_host, tb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(vd, v_host, tb, cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return FA2_ERR_CUDA;
+    return drained(FA2_ERR_CUDA);
   int rc = fa2_fwd(qd, kd, vd, od, ld, B, H, N, d, scale, causal, dtype, stream);
-  if (rc) return rc;
+  if (rc) return drained(rc);
   if (cudaMemcpyAsync(o_host, od, tb, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaMemcpyAsync(lse_host, ld, lb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return FA2_ERR_CUDA;
+    return drained(FA2_ERR_CUDA);
   return fa2_get_device_status(stream, nullptr);
 }
 

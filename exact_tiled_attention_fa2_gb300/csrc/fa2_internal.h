@@ -40,7 +40,8 @@ struct KernelParams {
   int window_left;    // key j visible to query i iff i+off-wl <= j <= i+off+wr
   int window_right;   //   (off = N_k - N_q; -1 = unbounded on that side),
   int prefix;         //   or j < prefix (keys every query sees)
-  float scale_log2;   // scale * log2(e): scores go to the exp2 domain
+  float scale_log2;   // scale * log2(e), signed: scores go to the exp2 domain (the tiled kernels scale
+                      //   by its magnitude and negate the S product for a negative scale)
   // Split-key mode of the double-buffered kernel (decoding): a unit is a
   // (query tile, key chunk) pair, and each row's partial (m, l, O~) goes to
   // ws_ml / ws_o in the decode merge kernel's layout instead of O and LSE.

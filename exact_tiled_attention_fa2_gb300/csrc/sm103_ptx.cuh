@@ -198,12 +198,15 @@ __device__ __forceinline__ void tmem_st_wait() {
 
 // Instruction descriptor for tcgen05.mma kind::f16 with fp32 accumulation:
 // bits 4-5 D format (1 = f32), 7-9 A format and 10-12 B format (0 = f16,
-// 1 = bf16), 15/16 A/B major (0 = K-major, 1 = MN-major), 17-22 N >> 3,
-// 24-28 M >> 4.
+// 1 = bf16), 13 negate A, 15/16 A/B major (0 = K-major, 1 = MN-major),
+// 17-22 N >> 3, 24-28 M >> 4.
 __host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N, bool bf16, bool a_mn_major, bool b_mn_major) {
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
          ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+
+// The negate-A bit of the kind::f16 instruction descriptor: D (+)= (-A) B.
+constexpr uint32_t kIdescNegateA = 1u << 13;
 
 // Shared-memory matrix descriptor, 128-byte swizzle: bits 0-13 start address
 // >> 4, 16-29 leading-dimension byte offset >> 4, 32-45 stride-dimension byte

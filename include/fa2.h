@@ -66,7 +66,8 @@ typedef enum {
  *   B, H, N : batch, heads, sequence length (each >= 1; B*H*N*d < 2^31 elements
  *             per tensor is not required, but B*H < 2^31 and N < 2^31 are)
  *   d       : head dimension, one of 64, 128, 256 (the pages cap head dim at 256)
- *   scale   : finite and > 0; the pages use 1/sqrt(d)
+ *   scale   : any finite value (0: uniform weights over the visible keys; a
+ *             negative scale reverses the score order); the pages use 1/sqrt(d)
  *   causal  : 0 = every key visible; 1 = key j visible to query i iff j <= i
  *   dtype   : FA2_FP16 or FA2_BF16
  *   stream  : a cudaStream_t (0 = legacy default stream)
@@ -122,7 +123,7 @@ typedef struct fa2_fwd_params {
   int seqlen_k;           /* N_k >= 1 (packed: ignored) */
   int head_dim;           /* d: 64, 128 or 256 */
   int dtype;              /* FA2_FP16 or FA2_BF16 */
-  float scale;            /* finite, > 0 */
+  float scale;            /* any finite value */
   int window_left;        /* >= 0, or -1 = unbounded */
   int window_right;       /* >= 0, or -1 = unbounded */
   int prefix_len;         /* >= 0 */

@@ -249,6 +249,34 @@ def test_scale_multiplies_scores():
     np.testing.assert_allclose(l1, l2, atol=1e-12, rtol=0)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_scale_gives_uniform_weights(causal):
+    # S = 0 * Q K^T: every visible key has the same weight, so O is the mean of
+    # the visible value rows and L = ln(number of visible keys) (closed form)
+    N, d = 13, 8
+    q, k, v = _rand_bits((2, 1, N, d), oracle.BF16, 21)
+    o, lse = oracle.attention_fwd(q, k, v, oracle.BF16, 0.0, causal)
+    vf = sy.bits_to_f32(v, oracle.BF16).astype(np.float64)
+    for i in range(N):
+        n = i + 1 if causal else N
+        np.testing.assert_allclose(o[:, :, i], vf[:, :, :n].mean(axis=2), atol=1e-13, rtol=0)
+        np.testing.assert_allclose(lse[:, :, i], math.log(n), atol=1e-13, rtol=0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_negative_scale_equals_negated_queries(causal):
+    # scale * (q . k) with scale < 0 equals |scale| * ((-q) . k); negating a
+    # 16-bit value flips its sign bit, so both problems are computed exactly alike
+    q, k, v = _rand_bits((1, 2, 11, 8), oracle.FP16, 23)
+    q_neg = q ^ np.uint16(0x8000)
+    o1, l1 = oracle.attention_fwd(q, k, v, oracle.FP16, -0.7, causal)
+    o2, l2 = oracle.attention_fwd(q_neg, k, v, oracle.FP16, 0.7, causal)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    # and the order of the weights reverses: the smallest score gets the largest weight
+    o3, _ = oracle.attention_fwd(q, k, v, oracle.FP16, 0.7, causal)
+    assert not np.allclose(o1, o3)
+
+
 def test_very_negative_scores_stay_finite():
     # every score near -2000: exp without the max shift underflows to 0/0
     N, d = 5, 2
