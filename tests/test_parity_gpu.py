@@ -135,7 +135,7 @@ def test_practice_row_embedded():
     assert lse[0, 0, 0] == pytest.approx(5.0 + np.log(1.5824245), abs=1e-3)
 
 
-# ------------------------------------------------------------------ full-size workloads (sampled rows)
+# ------------------------------------------------------------------ full-size workloads
 
 def _sample_rows(w, rng, per_head=48):
     rows = set(range(min(w.N, 8)))
@@ -147,21 +147,32 @@ def _sample_rows(w, rng, per_head=48):
     return sorted(rows)
 
 
-@pytest.mark.parametrize("index", [1, 2, 3, 4, 5])
-def test_workload_parity(index):
+@pytest.mark.parametrize("index", [1, 2, 3, 5])
+def test_workload_parity_every_output(index):
+    """The workload in the benchmark's launch configuration, every element of O
+    and LSE against the oracle (which evaluates the whole problem in seconds
+    on the host's cores: 1.4e11 - 2.7e11 FLOPs)."""
     w = sy.WORKLOADS[index]
     q, k, v = w.inputs()
     o, lse = run_gpu(q, k, v, w.dtype, w.scale, w.causal)
+    o_ref, lse_ref = oracle.attention_fwd(q, k, v, w.dtype, w.scale, w.causal)
+    check(o, lse, o_ref, lse_ref, w.dtype, w.name + " (every output)")
+
+
+def test_workload_parity_every_head_sampled_rows():
+    """The long-context workload (B1 H32 N16384 d128 causal, 2.2e12 FLOPs: too
+    much for the oracle whole) on sampled rows of every head -- tile
+    boundaries, the first and last rows and random rows -- so that a tile
+    written into the wrong head or position shows up in some head; plus
+    properties that hold for every output."""
+    w = sy.WORKLOADS[4]
+    q, k, v = w.inputs()
+    o, lse = run_gpu(q, k, v, w.dtype, w.scale, w.causal)
     BH = w.B * w.H
-    if w.N * w.N * w.d * BH <= 2 ** 24:
-        o_ref, lse_ref = oracle.attention_fwd(q, k, v, w.dtype, w.scale, w.causal)
-        check(o, lse, o_ref, lse_ref, w.dtype, w.name)
-        return
-    rng = np.random.default_rng(index)
-    heads = sorted({0, BH - 1} | {int(x) for x in rng.integers(0, BH, size=3)})
+    rng = np.random.default_rng(4)
     bh_idx, row_idx = [], []
-    for bh in heads:
-        rows = _sample_rows(w, rng)
+    for bh in range(BH):
+        rows = _sample_rows(w, rng, per_head=24)
         bh_idx += [bh] * len(rows)
         row_idx += rows
     bh_idx = np.array(bh_idx)
@@ -169,11 +180,14 @@ def test_workload_parity(index):
     o_ref, lse_ref = oracle.attention_rows(q, k, v, w.dtype, w.scale, w.causal, bh_idx, row_idx)
     o_flat = o.reshape(BH, w.N, w.d)[bh_idx, row_idx]
     lse_flat = lse.reshape(BH, w.N)[bh_idx, row_idx]
-    check(o_flat, lse_flat, o_ref, lse_ref, w.dtype, w.name + " (%d sampled rows)" % len(row_idx))
+    check(o_flat, lse_flat, o_ref, lse_ref, w.dtype, w.name + " (%d sampled rows, every head)" % len(row_idx))
     # properties that hold at any size, checked on every output
     assert np.isfinite(o).all() and np.isfinite(lse).all()
     vmax = np.abs(sy.bits_to_f32(v, w.dtype)).max()
     assert np.abs(o).max() <= vmax * (1 + 1e-2)      # a convex combination of value rows
+    # causal row 0 of every head sees only key 0: O = V_0 (rounded once) and L = scale q_0 . k_0
+    v0 = sy.bits_to_f32(v, w.dtype).reshape(BH, w.N, w.d)[:, 0]
+    assert np.array_equal(o.reshape(BH, w.N, w.d)[:, 0], v0.astype(np.float64))
 
 
 # ------------------------------------------------------------------ behaviour
