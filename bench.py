@@ -251,7 +251,7 @@ def run_reference(args, w, gen=None):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(w, args.gpus, gen),
+        "data": "synthetic", "config": arm_config(args, w, gen, args.gpus),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": "%d random (head,row) rows of the workload, each step ~%.1f s of CPU work; "
                                    "flops counted 4*d per visible key" % (rows, per_step)},
@@ -285,17 +285,27 @@ def l2_note(in_bytes: int, flush: bool) -> str:
     return "inputs (%.0f MB) larger than the 129 MB L2; no flush" % (in_bytes / 1e6)
 
 
-def workload_config(w: sy.Workload, n_gpus: int, gen=None, l2: str = ""):
+def workload_config(w: sy.Workload, n_gpus: int, gen=None, l2: str = "", launch: str = ""):
     c = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
          "dtype": "bf16" if w.dtype == sy.BF16 else "fp16", "causal": w.causal,
          "scale": "1/sqrt(d)", "q_scale": w.q_scale,
          "l2": l2 or l2_note(step_input_bytes(w, gen, False), False),
          "parallelism": "replicas x%d" % n_gpus, "seed": w.seed(0)}
+    if launch:
+        c["launch"] = launch
     if gen is not None:
         c["workload"] = w.name + " " + gen["label"]
         c["causal"] = None
         c["mask"] = {k: gen[k] for k in ("window_left", "window_right", "prefix", "seqlen_k", "layout", "varlen_seqs")}
     return c
+
+
+def arm_config(args, w: sy.Workload, gen, n_gpus: int):
+    """The line's `config`, the same for both arms: the workload, the L2
+    handling and the launch mode the kernel arm times with."""
+    in_bytes = step_input_bytes(w, gen, args.backward)
+    flush = flush_l2(in_bytes, args.flush_l2)
+    return workload_config(w, n_gpus, gen, l2_note(in_bytes, flush), launch_mode(args.no_graph or flush))
 
 
 def general_mask(args, w: sy.Workload):
@@ -427,8 +437,77 @@ def general_step(fa2, torch, w: sy.Workload, gen, dev, tdt, stream, backward=Fal
     return step, flops, q_bits, k_bits, v_bits
 
 
-def launch_mode(args):
-    return "one CUDA graph replaying the timed launches" if not args.no_graph else "one launch per step from Python"
+def launch_mode(no_graph: bool) -> str:
+    return "one CUDA graph replaying the timed launches" if not no_graph else "one launch per step from Python"
+
+
+MIN_TIMED_S = 1.0       # device time the repeated K-step regions add up to, at least
+MAX_REGIONS = 2000
+
+
+def region_count(first_region_ms: float, min_total_s: float = MIN_TIMED_S, cap: int = MAX_REGIONS) -> int:
+    """How many K-step regions to time so that they add up to min_total_s of
+    device time (at least 3, at most `cap`), given the first region's time."""
+    if first_region_ms <= 0:
+        return cap
+    n = int(np.ceil(min_total_s * 1e3 / first_region_ms))
+    return max(3, min(cap, n))
+
+
+def spread(region_ms):
+    """Median and spread of the timed regions (each exactly K steps)."""
+    a = np.sort(np.asarray(region_ms, dtype=np.float64))
+    med = float(np.median(a))
+    p10, p90 = (float(x) for x in np.percentile(a, [10, 90]))
+    return {"regions": int(a.size), "median_ms": med, "min_ms": float(a[0]), "max_ms": float(a[-1]),
+            "p10_ms": p10, "p90_ms": p90, "spread_pct": 100.0 * (p90 - p10) / med if med > 0 else None,
+            "total_s": float(a.sum()) / 1e3}
+
+
+def time_regions(torch, step, stream, steps: int, flush_buf, graph, first_only: bool = False):
+    """Time K-step regions on `stream` with CUDA events: one region, or (the
+    default) as many as region_count asks for.  A graph replays the K launches
+    (region time = its events); without one, each launch has its own events
+    and, with a flush buffer, the L2 is overwritten before it, outside them
+    (region time = the sum of the K launch times).  Returns (region times in
+    ms, per-launch ms of every region)."""
+    def one():
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            if graph is None:
+                # launched one by one: keep the GPU busy while the host enqueues
+                # them, so no launch waits on the host inside its own events
+                torch.cuda._sleep(int(4e5 * steps))
+            t0.record(stream)
+            if graph is not None:
+                graph.replay()
+            else:
+                for i in range(steps):
+                    if flush_buf is not None:
+                        flush_buf.zero_()
+                    starts[i].record(stream)
+                    step()
+                    ends[i].record(stream)
+            t1.record(stream)
+        stream.synchronize()
+        if graph is not None:
+            ms = t0.elapsed_time(t1)
+            return ms, [ms / steps] * steps
+        per = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+        # with a flush, the overwrites between launches are not the workload's time
+        return (sum(per) if flush_buf is not None else t0.elapsed_time(t1)), per
+    first, per = one()
+    regions, launches = [first], list(per)
+    if not first_only:
+        for _ in range(region_count(first) - 1):
+            ms, per = one()
+            regions.append(ms)
+            launches += per
+    return regions, launches
 
 
 def build_parser() -> argparse.ArgumentParser:
@@ -535,60 +614,46 @@ def main():
     in_bytes = step_input_bytes(w, gen, args.backward)
     flush = flush_l2(in_bytes, args.flush_l2)
     fbuf = None
+    no_graph = args.no_graph or flush
     if flush:
-        args.no_graph = True
         fbuf = torch.empty(int(2 * L2_BYTES), dtype=torch.uint8, device=dev)
-    graph = None
-    if not args.no_graph:
-        # K forward launches captured once and replayed: the timed region then
-        # holds exactly the K kernels, without host launch gaps between them.
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
+
+    def capture():
+        # K launches captured once and replayed: a region then holds exactly
+        # the K kernels, without host launch gaps between them
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
             for _ in range(args.steps):
                 step()
         stream.synchronize()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        return g
+    graph = None if no_graph else capture()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
+    # K-step regions, repeated until they add up to >= 1 s of device time;
+    # the line reports the median region (every region is exactly K steps)
     with ClockSampler(local) as clocks:
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            if graph is None:
-                # launched one by one: keep the GPU busy while the host enqueues
-                # them, so no launch waits on the host inside its own events
-                torch.cuda._sleep(int(4e5 * args.steps))
-            t0.record(stream)
-            if graph is not None:
-                graph.replay()
-            else:
-                for i in range(args.steps):
-                    if fbuf is not None:
-                        fbuf.zero_()
-                    starts[i].record(stream)
-                    step()
-                    ends[i].record(stream)
-            t1.record(stream)
-        stream.synchronize()
+        regions, kernel_ms = time_regions(torch, step, stream, args.steps, fbuf, graph)
     torch.cuda.synchronize(dev)
-    elapsed_ms = t0.elapsed_time(t1)
-    if graph is not None:
-        kernel_ms = [elapsed_ms / args.steps] * args.steps
-    else:
-        kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    if fbuf is not None:
-        elapsed_ms = sum(kernel_ms)   # the flushes between launches are not the workload's time
+    timing = spread(regions)
+    elapsed_ms = timing["median_ms"]
     code, detail = fa2.fa2_get_device_status(stream)
     if code != fa2.FA2_OK:
         raise RuntimeError("device status %d (0x%x) in timed region" % (code, detail))
     max_ms = max_over_ranks(elapsed_ms, dist, dev)
     if dist is not None:
         dist.barrier()
+    unflushed = None
+    if flush and rank == 0:
+        # the same launches back to back from a CUDA graph, L2 not overwritten
+        g2 = capture()
+        r2, _ = time_regions(torch, step, stream, args.steps, None, g2)
+        unflushed = spread(r2)
+        del g2
 
     value = job_throughput(flops, args.steps, ws, max_ms)
-    avg_launch_ms = sum(kernel_ms) / len(kernel_ms)
+    avg_launch_ms = max_ms / args.steps   # the median region's K launches (flushed: their own events)
     achieved = flops / (avg_launch_ms / 1e3) / 1e12
     peak, peak_note = measured_peak()
 
@@ -638,7 +703,11 @@ def main():
             "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == sy.BF16 else "fp16",
             "data": "synthetic",
-            "config": dict(workload_config(w, ws, gen, l2_note(in_bytes, flush)), launch=launch_mode(args)),
+            "config": arm_config(args, w, gen, ws),
+            "timing": dict(timing, steps_per_region=args.steps,
+                           rule="median over regions of exactly K steps, each bracketed by a synchronize and "
+                                "timed with CUDA events on the launching stream; regions repeated until they add "
+                                "up to >= %.0f s of device time; value = max over ranks of the median" % MIN_TIMED_S),
             "pct_of_peak": 100.0 * value / ws / peak,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                          "frac": achieved / peak,
@@ -653,6 +722,25 @@ def main():
             "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": args.steps * (3 if args.backward else 1),
             "kernel_sha": kernel_source_hash(BWD_KERNEL_SOURCES if args.backward else KERNEL_SOURCES),
         }
+        # the memory side of the roofline: algorithmic bytes per launch over the launch time
+        hbm, hbm_note = measured_hbm()
+        alg_bytes = line["roofline"]["algorithmic_bytes_per_launch"]
+        gbs = alg_bytes / (avg_launch_ms / 1e3) / 1e9
+        line["hbm"] = {"achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "peak_source": hbm_note,
+                       "bytes_per_launch": alg_bytes}
+        if unflushed is not None:
+            line["latency"] = {"flushed_us_per_launch": 1e3 * avg_launch_ms,
+                               "unflushed_us_per_launch": 1e3 * unflushed["median_ms"] / args.steps,
+                               "unflushed_gbs": alg_bytes / (unflushed["median_ms"] / args.steps / 1e3) / 1e9,
+                               "unflushed_regions": unflushed["regions"],
+                               "note": "flushed: L2 overwritten before each launch (the value above); unflushed: "
+                                       "the same launches back to back from a CUDA graph"}
+        ridge = peak * 1e12 / (hbm * 1e9)   # FLOP per byte where the two measured peaks meet
+        if gen is None and not args.backward and w.flops() / w.algorithmic_bytes() < ridge:
+            # below the ridge point (the tiny single-tile workload): the memory side bounds the roofline
+            line["roofline"] = dict(line["hbm"], bound="hbm", kernel=kname, avg_launch_ms=avg_launch_ms,
+                                    algorithmic_bytes_per_launch=alg_bytes, algorithmic_flops_per_launch=flops,
+                                    traffic=None)
         if gen is not None and gen["decode_rows"]:
             # HBM-bound: K and V read once dominate; roofline against the measured copy bandwidth
             hbm, hbm_note = measured_hbm()

@@ -154,3 +154,32 @@ def test_profile_commands_parse():
             assert args.warmup >= 3, (path, argv)
             found += 1
     assert found >= 8
+
+
+def test_timing_regions_and_spread():
+    """Regions of K steps are repeated until they add up to >= 1 s of device
+    time (at least 3, at most MAX_REGIONS); the line reports their median."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert bench.region_count(31.0) == 33            # 20 launches of 1.55 ms
+    assert bench.region_count(2000.0) == 3           # long regions: still three
+    assert bench.region_count(0.01) == bench.MAX_REGIONS
+    assert bench.region_count(0.0) == bench.MAX_REGIONS
+    t = bench.spread([3.0, 1.0, 2.0, 100.0, 2.0])
+    assert t["regions"] == 5 and t["median_ms"] == 2.0 and t["min_ms"] == 1.0 and t["max_ms"] == 100.0
+    assert t["total_s"] == pytest.approx(0.108)
+
+
+def test_both_arms_report_the_same_config():
+    sys.path.insert(0, ROOT)
+    import bench
+    from exact_tiled_attention_fa2_gb300 import synthetic as sy
+
+    for wl in (1, 2, 4):
+        args = bench.build_parser().parse_args(["--workload", str(wl)])
+        w = sy.WORKLOADS[wl]
+        c = bench.arm_config(args, w, None, 1)
+        assert c["launch"] == bench.launch_mode(bench.flush_l2(bench.step_input_bytes(w, None, False), "auto"))
+        assert c == bench.arm_config(bench.build_parser().parse_args(["--workload", str(wl), "--impl", "reference"]),
+                                     w, None, 1)
