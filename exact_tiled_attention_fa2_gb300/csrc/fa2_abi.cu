@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <cfloat>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -387,6 +388,8 @@ int prepare(const fa2_fwd_params& a, int units_rows, Prepared& out, const Extent
   p.window_right = a.window_right;
   p.prefix = a.prefix_len;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.scale_log2_mag = std::fmax(std::fabs(p.scale_log2), FLT_MIN);
+  p.qk_negate = p.scale_log2 < 0.f ? kIdescNegateA : 0u;
   out.band = a.window_left >= 0 || a.prefix_len > 0;
   return FA2_OK;
 }

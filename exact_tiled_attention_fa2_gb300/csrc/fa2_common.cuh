@@ -163,22 +163,13 @@ __device__ __forceinline__ bool split_tile(bool masked, bool few_keys) {
   }
 }
 
-// Scale, in place, the scores of key tile [k0, k0 + BC) by sl2 and set to
-// -inf those of the keys query row `row` does not see.  Scaling before masking
-// keeps a zero scale exact: a hidden key's score is -inf, never -inf * 0.
-// BAND: the first visible key may depend on the row (a bounded left window or
-// a prefix); otherwise every row sees keys [0, row_hi] and one comparison per
-// score suffices.
+// Set to -inf, in place, the scores of the keys of tile [k0, k0 + BC) that
+// query row `row` does not see.  BAND: the first visible key may depend on
+// the row (a bounded left window or a prefix); otherwise every row sees keys
+// [0, row_hi] and one comparison per score suffices.
 template <int BC, bool BAND>
-__device__ __forceinline__ void mask_scores(uint32_t* sr, const KeyMask& km, int row, int k0, float sl2) {
+__device__ __forceinline__ void mask_scores(uint32_t* sr, const KeyMask& km, int row, int k0) {
   const int c_hi = km.row_hi(row) - k0;
-  const float2 sl2x2 = make_float2(sl2, sl2);
-#pragma unroll
-  for (int c = 0; c < BC; c += 2) {
-    const float2 x = __fmul2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2);
-    sr[c] = __float_as_uint(x.x);
-    sr[c + 1] = __float_as_uint(x.y);
-  }
   if constexpr (BAND) {
     const int c_pre = km.pre_end - k0;
     const int c_lo = km.row_lo(row) - k0;

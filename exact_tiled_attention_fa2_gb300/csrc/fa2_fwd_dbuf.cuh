@@ -99,7 +99,6 @@ struct DbufCtx {
   int bh, split;  // split-key mode: the (b, h) slice and key chunk of the partials
   TileMask tm;    // unmasked key tiles, by index counted from kv0
   bool few_keys;  // N_k <= 2 key tiles: every bf16 P is split
-  uint32_t neg_s; // kIdescNegateA for a negative scale (S = -Q K^T, scaled by |scale|), else 0
   __device__ __forceinline__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
 };
 
@@ -188,8 +187,9 @@ __device__ __forceinline__ void db_producer(const DbufCtx& t, const KernelParams
 }
 
 template <class C, bool BF16>
-__device__ __forceinline__ void db_mma(const DbufCtx& t) {
-  const uint32_t idesc_qk = make_idesc_f16(C::BR, C::BC, BF16, false, false) | t.neg_s;
+__device__ __forceinline__ void db_mma(const DbufCtx& t, const KernelParams& p) {
+  // S = (+-Q) K^T: a negative scale's sign goes into the product (p.qk_negate)
+  const uint32_t idesc_qk = make_idesc_f16(C::BR, C::BC, BF16, false, false) | p.qk_negate;
   constexpr uint32_t idesc_pv = make_idesc_f16(C::BR, C::D, BF16, false, true);
   const uint64_t dq0 = make_sdesc_sw128(t.sQ, 16, 1024);
   const uint64_t dk0 = make_sdesc_sw128(t.sK, 16, 1024);
@@ -261,7 +261,7 @@ __device__ __forceinline__ void db_softmax(const DbufCtx& t, const KernelParams&
   }
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
   const uint32_t tO = t.tmem + lane_off + C::TMEM_O;
-  const float sl2 = fabsf(p.scale_log2);   // a negative scale's sign is in the S product (neg_s)
+  const float sl2 = p.scale_log2_mag;
   const TileMask tmask = t.tm;
   const bool few_keys = t.few_keys;
   float m_run = -INFINITY;
@@ -279,11 +279,7 @@ __device__ __forceinline__ void db_softmax(const DbufCtx& t, const KernelParams&
 #pragma unroll
     for (int c = 0; c < C::BC; c += 32) tmem_ld_wait_x32(sr + c);
     const bool masked = !tmask.full(j);
-    float tsl = sl2;   // the scale still to apply to sr: masked tiles are scaled by the mask pass
-    if (masked) {
-      mask_scores<C::BC, BAND>(sr, facts->km, row, (t.kv0 + j) * C::BC, sl2);
-      tsl = 1.f;
-    }
+    if (masked) mask_scores<C::BC, BAND>(sr, facts->km, row, (t.kv0 + j) * C::BC);
     float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
     for (int c = 0; c < C::BC; c += 8) {
@@ -292,13 +288,13 @@ __device__ __forceinline__ void db_softmax(const DbufCtx& t, const KernelParams&
       mx2 = fmax3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
       mx3 = fmax3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
     }
-    // the largest scaled score (sl2 >= 0, so scaling keeps the maximum's place)
-    const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * tsl;
+    // the largest scaled score (sl2 > 0, so scaling keeps the maximum's place)
+    const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
     const bool raise = m_tile > m_run + kRescaleLog2;
     const float m_new = raise ? m_tile : m_run;
     const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
     const float alpha = raise ? ex2_approx(m_run - m_use) : 1.f;
-    const float2 scale2 = make_float2(tsl, tsl);
+    const float2 scale2 = make_float2(sl2, sl2);
     const float2 neg_m2 = make_float2(-m_use, -m_use);
     float2 sum0 = make_float2(0.f, 0.f), sum1 = make_float2(0.f, 0.f);
     if (split_tile<BF16>(masked, few_keys)) {
@@ -430,7 +426,6 @@ __global__ void __launch_bounds__(192, DbufConfig<D>::CTAS_PER_SM)
   }
   t.tm = tile_mask<BAND>(t.km, t.q0, last, C::BC).from(t.kv0);
   t.few_keys = t.km.n_k <= 2 * C::BC;
-  t.neg_s = p.scale_log2 < 0.f ? kIdescNegateA : 0u;
 
   if (warp == C::TMA_WARP && lane == 0) {
     mbar_init(t.bar(DB_Q), 1);
@@ -472,7 +467,7 @@ __global__ void __launch_bounds__(192, DbufConfig<D>::CTAS_PER_SM)
   if (warp == C::TMA_WARP) {
     if (lane == 0 && t.nkv > 0) db_producer<C>(t, p, &tm_q, &tm_k, &tm_v, false);
   } else if (warp == C::MMA_WARP) {
-    if (lane == 0) db_mma<C, BF16>(t);
+    if (lane == 0) db_mma<C, BF16>(t, p);
     __syncwarp();
   } else {
     db_softmax<C, BF16, BAND, SPLIT>(t, p, facts, warp, lane, &tm_o);

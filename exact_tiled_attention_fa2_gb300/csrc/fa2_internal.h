@@ -40,8 +40,16 @@ struct KernelParams {
   int window_left;    // key j visible to query i iff i+off-wl <= j <= i+off+wr
   int window_right;   //   (off = N_k - N_q; -1 = unbounded on that side),
   int prefix;         //   or j < prefix (keys every query sees)
-  float scale_log2;   // scale * log2(e), signed: scores go to the exp2 domain (the tiled kernels scale
-                      //   by its magnitude and negate the S product for a negative scale)
+  float scale_log2;   // scale * log2(e), signed: scores go to the exp2 domain
+  // The tiled forward kernel's form of the scale: it scales raw scores by
+  // scale_log2_mag = max(|scale * log2(e)|, FLT_MIN) and, for a negative
+  // scale, negates the S product (qk_negate: the negate-A bit of its
+  // instruction descriptor, else 0).  FLT_MIN in place of a zero scale rounds
+  // every scaled score to zero against the row maximum (P = 1 on every
+  // visible key, exactly as with scale 0) and keeps a hidden key's -inf from
+  // forming -inf * 0.
+  float scale_log2_mag;
+  uint32_t qk_negate;
   // Split-key mode of the double-buffered kernel (decoding): a unit is a
   // (query tile, key chunk) pair, and each row's partial (m, l, O~) goes to
   // ws_ml / ws_o in the decode merge kernel's layout instead of O and LSE.

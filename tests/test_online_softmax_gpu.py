@@ -99,7 +99,13 @@ def tile_maxima_log2(q, k, dtype, scale, causal):
 
 def ramp_inputs(B, H, N, d, dtype, step, seed, jitter):
     """q_i = e_1 + jitter * r_i e_2 and k_j = step * floor(j / 64) e_1 + jitter * u_j e_2,
-    so with scale 1 a score is step * (key tile) plus a small random term; V ~ N(0, 1)."""
+    so with scale 1 a score is step * (key tile) plus a small random term.
+
+    The softmax these ramps make is sharp: a row's weight sits on the few keys
+    of its last tile, so O comes close to single value rows.  V is uniform in
+    [-1, 1], which keeps |O| <= 1, the range in which the tolerances above
+    hold for the 16-bit output formats (bf16's half spacing is 2^-9 there; an
+    N(0, 1) value row of 4.3 would alone round by up to 2^-6)."""
     rng = np.random.default_rng(seed)
     q = np.zeros((B, H, N, d), np.float32)
     k = np.zeros((B, H, N, d), np.float32)
@@ -107,7 +113,7 @@ def ramp_inputs(B, H, N, d, dtype, step, seed, jitter):
     q[..., 1] = jitter * rng.uniform(-1, 1, size=(B, H, N))
     k[..., 0] = step * (np.arange(N) // KEY_TILE)
     k[..., 1] = jitter * rng.uniform(-1, 1, size=(B, H, N))
-    v = rng.standard_normal((B, H, N, d)).astype(np.float32)
+    v = rng.uniform(-1, 1, size=(B, H, N, d)).astype(np.float32)
     return bits(q, dtype), bits(k, dtype), bits(v, dtype)
 
 
@@ -192,7 +198,13 @@ def test_worked_example_across_three_key_tiles(dtype, N):
 
 # ------------------------------------------------------------------ scale zero and negative
 
-SCALES = {"zero": lambda d: 0.0, "negative": lambda d: -1.0 / np.sqrt(d), "negative large": lambda d: -0.5}
+SCALES = {"zero": lambda d: 0.0, "negative": lambda d: -1.0 / np.sqrt(d), "negative x2": lambda d: -2.0 / np.sqrt(d)}
+
+
+def uniform_values(v_bits, dtype, seed):
+    """Value rows uniform in [-1, 1] (|O| <= 1, see ramp_inputs) in place of the N(0, 1) draws."""
+    rng = np.random.default_rng(seed)
+    return bits(rng.uniform(-1, 1, size=v_bits.shape), dtype)
 
 
 @pytest.mark.parametrize("which", sorted(SCALES))
@@ -203,6 +215,7 @@ def test_forward_any_finite_scale(d, dtype, causal, which):
     B, H, N = 1, 2, 200
     scale = SCALES[which](d)
     q, k, v = sy.make_qkv(B, H, N, d, dtype, seed=300 + d)
+    v = uniform_values(v, dtype, 300 + d)
     o, lse = run_fwd(q, k, v, dtype, scale, causal)
     o_ref, lse_ref = oracle.attention_fwd(q, k, v, dtype, scale, causal)
     check(o, lse, o_ref, lse_ref, dtype, "scale %s d=%d causal=%d" % (which, d, causal))
