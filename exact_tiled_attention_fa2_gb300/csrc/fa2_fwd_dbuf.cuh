@@ -11,7 +11,11 @@
 // issued by one thread execute in order, which is what lets S(j+2) follow
 // the product reading P(j) from the same columns.  A K stage is released as
 // soon as its S product completes and a V stage after its PV product, so the
-// next K tile loads while the current PV runs.  Online softmax with the
+// next K tile loads while the current PV runs.  At d = 128 the MMA-issuing
+// thread waits on one barrier per key tile, P(j): besides the four softmax
+// warps, the TMA thread arrives on it once V_j and K_{j+2} have landed, so the
+// operand waits are off the MMA thread (each wait there stalls its stream of
+// products; see DbufConfig::TMA_GATES_P).  Online softmax with the
 // rescaling margin of fa2_tile.cuh: the running max is raised only past 2^8,
 // O~ rescaled in place when it is.
 //
@@ -63,6 +67,12 @@ struct DbufConfig {
   static constexpr uint32_t TMEM_O = 128;
   static constexpr uint32_t TMEM_COLS = (D == 256) ? 512 : 256;
   static constexpr int CTAS_PER_SM = (D == 256) ? 1 : 2;   // TMEM and shared memory allow two below d = 256
+  // The TMA thread, not the MMA thread, checks that V_j and K_{j+2} have landed
+  // and says so on P(j).  Measured on the same GB300: d = 128 +1.5-1.8 % (the
+  // MMA thread's stream is what limits it there); d = 64 -4.5 % and d = 256
+  // -2 %, where the softmax or the single CTA per SM sets the pace and the
+  // TMA thread's polling only delays P.
+  static constexpr bool TMA_GATES_P = (D == 128);
   static_assert(D == 64 || D == 128 || D == 256, "double-buffered-S kernel: head dim 64, 128 or 256");
   static_assert(TMEM_O + D <= TMEM_COLS, "tensor memory");
   static_assert(CTAS_PER_SM * TMEM_COLS <= 512, "tensor memory per SM");
@@ -84,6 +94,8 @@ enum : int {
                    // thread waits for P(j), so the softmax may finish P(j) and
                    // P(j+1) first; on a single barrier that would put it two
                    // phases ahead of the parity the MMA thread waits for.
+                   // Arrivals: the four softmax warps, and with TMA_GATES_P the
+                   // TMA thread (V_j and K_{j+2} in shared memory).
 };
 
 // One query tile's work, shared by the CTA's warp roles.
@@ -134,9 +146,23 @@ __device__ __forceinline__ void db_producer(const DbufCtx& t, const KernelParams
     return;
   }
   int jk = nk0, jv = nv0;
+  int jp = C::TMA_GATES_P ? 0 : t.nkv;   // next key tile whose operands the TMA thread vouches for on P(jp)
   uint64_t idle_since = 0;
-  while (jk < t.nkv || jv < t.nkv) {
+  while (jk < t.nkv || jv < t.nkv || jp < t.nkv) {
     bool progressed = false;
+    // V_jp and K_{jp+2} issued and landed: arrive on P(jp).  Their barriers are
+    // at most one phase ahead: V_{jp+2} and K_{jp+4} load only after products
+    // that need P(jp) complete.
+    if constexpr (C::TMA_GATES_P) {
+      if (jp < jv && (jp + 2 >= t.nkv || jp + 2 < jk) &&
+          mbar_try_wait(t.bar(DB_VFULL + jp % C::VSTAGES), (uint32_t)(jp / C::VSTAGES) & 1) &&
+          (jp + 2 >= t.nkv ||
+           mbar_try_wait(t.bar(DB_KFULL + (jp + 2) % C::KSTAGES), (uint32_t)((jp + 2) / C::KSTAGES) & 1))) {
+        mbar_arrive(t.bar(DB_P + (jp & 1)));
+        ++jp;
+        progressed = true;
+      }
+    }
     if (jk < t.nkv) {
       const int s = jk % C::KSTAGES, u = jk / C::KSTAGES;
       if (u == 0 || mbar_try_wait(t.bar(DB_KEMPTY + s), (u - 1) & 1)) {
@@ -195,11 +221,14 @@ __device__ __forceinline__ void db_mma(const DbufCtx& t, const KernelParams& p) 
   const uint64_t dk0 = make_sdesc_sw128(t.sK, 16, 1024);
   const uint64_t dv0 = make_sdesc_sw128(t.sV, C::BC * 128, 1024);
   bool ok = true;
+  // with TMA_GATES_P, S(j) for j >= 2 follows a P wait, which covers K_j (see DB_P)
   auto issue_s = [&](int j) -> bool {
     const int sk = j % C::KSTAGES;
-    if (!wait_or_abort(t.bar(DB_KFULL + sk), (uint32_t)(j / C::KSTAGES) & 1, t.abort_flag, t.status, kSiteMmaK))
-      return false;
-    tc_fence_after();
+    if (!C::TMA_GATES_P || j < 2) {
+      if (!wait_or_abort(t.bar(DB_KFULL + sk), (uint32_t)(j / C::KSTAGES) & 1, t.abort_flag, t.status, kSiteMmaK))
+        return false;
+      tc_fence_after();
+    }
     const uint64_t b0 = dk0 + (uint64_t)((sk * C::KV_BYTES) >> 4);
     const uint32_t tS = t.tmem + C::TMEM_S + 64 * (j & 1);
 #pragma unroll
@@ -215,8 +244,11 @@ __device__ __forceinline__ void db_mma(const DbufCtx& t, const KernelParams& p) 
     if (ok && t.nkv > 1) ok = issue_s(1);
     for (int j = 0; j < t.nkv && ok; ++j) {
       const int sv = j % C::VSTAGES;
-      ok = wait_or_abort(t.bar(DB_P + (j & 1)), (uint32_t)(j >> 1) & 1, t.abort_flag, t.status, kSiteMmaP) &&
-           wait_or_abort(t.bar(DB_VFULL + sv), (uint32_t)(j / C::VSTAGES) & 1, t.abort_flag, t.status, kSiteMmaV);
+      // with TMA_GATES_P, P(j) also stands for V_j and K_{j+2} in shared memory
+      ok = wait_or_abort(t.bar(DB_P + (j & 1)), (uint32_t)(j >> 1) & 1, t.abort_flag, t.status, kSiteMmaP);
+      if (!C::TMA_GATES_P)
+        ok = ok &&
+             wait_or_abort(t.bar(DB_VFULL + sv), (uint32_t)(j / C::VSTAGES) & 1, t.abort_flag, t.status, kSiteMmaV);
       if (!ok) break;
       tc_fence_after();
       const uint64_t b0 = dv0 + (uint64_t)((sv * C::KV_BYTES) >> 4);
@@ -439,8 +471,8 @@ __global__ void __launch_bounds__(192, DbufConfig<D>::CTAS_PER_SM)
     }
     mbar_init(t.bar(DB_S), 1);
     mbar_init(t.bar(DB_S + 1), 1);
-    mbar_init(t.bar(DB_P), 4);       // one arrival per softmax warp
-    mbar_init(t.bar(DB_P + 1), 4);
+    mbar_init(t.bar(DB_P), C::TMA_GATES_P ? 5 : 4);   // one arrival per softmax warp (and the TMA thread)
+    mbar_init(t.bar(DB_P + 1), C::TMA_GATES_P ? 5 : 4);
     mbar_init(t.bar(DB_O), 1);
     mbar_init(t.bar(DB_OLAST), 1);
     mbar_init(t.bar(DB_EXIT), 1);
