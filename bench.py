@@ -707,7 +707,8 @@ def main():
 
     if rank == 0:
         clk = clocks.summary()
-        kname = "fa2_bwd_kernel" if args.backward else "fa2_fwd_dbuf_kernel"
+        kname = ({64: "fa2_bwd64_kernel", 256: "fa2_bwd256_kernel"}.get(w.d, "fa2_bwd_kernel") if args.backward
+                 else "fa2_fwd_dbuf_kernel")
         line = {
             "metric": METRIC if not args.backward else
             "backward attention TFLOP/s at 1 GB300 (2.5x the forward FLOPs) and % of dense FP16/BF16 tensor peak",

@@ -299,7 +299,7 @@ def fa2_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
 
 def fa2_bwd(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, workspace=None, scale=None, causal=False,
             stream=None):
-    """Gradients (dq, dk, dv) of fa2_fwd for the upstream gradient dout (CUDA tensors, d = 64 or 128)."""
+    """Gradients (dq, dk, dv) of fa2_fwd for the upstream gradient dout (CUDA tensors, d = 64, 128 or 256)."""
     import torch
     for t in (q, k, v, o, dout):
         if not (t.is_cuda and t.is_contiguous() and t.dtype == q.dtype and t.shape == q.shape):
@@ -328,7 +328,7 @@ def fa2_bwd_ex(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, workspace=None,
 
     dout has o's layout; dq, dk, dv default to new tensors shaped like q, k,
     v (contiguous) and may be views.  Packed batches take ``max_seqlen_k``
-    (default: total_k), the longest sequence's key count.  head dim 64 or 128.
+    (default: total_k), the longest sequence's key count.  head dim 64, 128 or 256.
     """
     import torch
     p = Fa2BwdParams()

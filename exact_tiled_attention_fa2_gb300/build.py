@@ -19,8 +19,9 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libfa2_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 SOURCES = ["fa2_abi.cu", "fa2_fwd_d64.cu", "fa2_fwd_d128.cu", "fa2_fwd_d256.cu", "fa2_bwd_d64.cu", "fa2_bwd_d128.cu",
-           "fa2_decode_d64.cu", "fa2_decode_d128.cu", "fa2_decode_d256.cu"]
-HEADERS = ["fa2_common.cuh", "fa2_tile.cuh", "fa2_fwd_dbuf.cuh", "fa2_bwd.cuh", "fa2_bwd64.cuh", "fa2_decode.cuh", "fa2_decode_tc.cuh",
+           "fa2_bwd_d256.cu", "fa2_decode_d64.cu", "fa2_decode_d128.cu", "fa2_decode_d256.cu"]
+HEADERS = ["fa2_common.cuh", "fa2_tile.cuh", "fa2_fwd_dbuf.cuh", "fa2_bwd.cuh", "fa2_bwd64.cuh", "fa2_bwd256.cuh",
+           "fa2_decode.cuh", "fa2_decode_tc.cuh",
            "fa2_internal.h",
            "sm103_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -193,9 +193,10 @@ int cached_decode_tc_maps(LaunchArgs& a, const MapKey& key) {
 }
 
 // The backward kernels' q, k and v maps: 128-row key tiles; query tiles of
-// 128 rows (d = 128) or 64 rows (d = 64).
+// 128 rows (d = 128) or 64 rows (d = 64, 256).
+int bwd_query_rows(int d) { return d == 128 ? 128 : 64; }
 int cached_bwd_maps(LaunchArgs& a, const MapKey& key) {
-  const int rows[4] = {key.d == 64 ? 64 : 128, 128, 128, 32};
+  const int rows[4] = {bwd_query_rows(key.d), 128, 128, 32};
   return cached_maps_rows(t_bwd_maps, a, key, rows);
 }
 
@@ -852,14 +853,15 @@ struct BwdPlan {
 };
 
 int bwd_plan(const fa2_fwd_params& a, BwdPlan& out) {
-  if (a.head_dim != 64 && a.head_dim != 128) return FA2_ERR_UNSUPPORTED;
+  if (a.head_dim != 64 && a.head_dim != 128 && a.head_dim != 256) return FA2_ERR_UNSUPPORTED;
   if (a.batch < 1 || a.heads < 1 || a.seqlen_q < 1 || a.seqlen_k < 1) return FA2_ERR_INVALID_ARG;
   const bool packed = a.cu_seqlens_q != nullptr;
   if (packed && a.total_q < 1) return FA2_ERR_INVALID_ARG;
   out.slices = (long long)(packed ? 1 : a.batch) * a.heads;
   out.rows_q = packed ? a.total_q : a.seqlen_q;
   const long long tiles = ((long long)a.seqlen_k + 127) / 128;
-  if ((long long)a.batch * a.heads * tiles > INT_MAX) return FA2_ERR_UNSUPPORTED;
+  // one CTA per key tile (d = 256: per key tile and half of d) in a 1-D grid
+  if ((long long)a.batch * a.heads * tiles * (a.head_dim == 256 ? 2 : 1) > INT_MAX) return FA2_ERR_UNSUPPORTED;
   out.num_k_tiles = (int)tiles;
   const size_t rows = (size_t)out.slices * (size_t)out.rows_q;
   out.accum_bytes = align256(rows * (size_t)a.head_dim * 4);
@@ -919,7 +921,7 @@ int backward(const fa2_bwd_params& bp, cudaStream_t stream) {
   la.tm_k = fl.tm_k;
   la.tm_v = fl.tm_v;
   const bool bf16 = a.dtype == FA2_BF16;
-  if (encode_map_rows(&la.tm_do, b.dout, d, dq_dims[2], a.heads, tb, st[3], d == 64 ? 64 : 128, bf16,
+  if (encode_map_rows(&la.tm_do, b.dout, d, dq_dims[2], a.heads, tb, st[3], bwd_query_rows(d), bf16,
                       pr.key.merged != 0))
     return FA2_ERR_CUDA;
   uint8_t* w = static_cast<uint8_t*>(b.workspace);
@@ -928,6 +930,7 @@ int backward(const fa2_bwd_params& bp, cudaStream_t stream) {
   p.f = pr.p;
   p.f.n_k = a.seqlen_k;   // packed: the longest sequence's key count the grid covers
   p.q = a.q;
+  p.v = a.v;
   p.dout = b.dout;
   p.dq = b.dq;
   p.dk = b.dk;
@@ -949,7 +952,7 @@ int backward(const fa2_bwd_params& bp, cudaStream_t stream) {
   p.scale = a.scale;
   la.bf16 = bf16;
   la.stream = stream;
-  const int e = (d == 64) ? launch_bwd_d64(la) : launch_bwd_d128(la);
+  const int e = (d == 64) ? launch_bwd_d64(la) : (d == 128) ? launch_bwd_d128(la) : launch_bwd_d256(la);
   return e == 0 ? FA2_OK : FA2_ERR_CUDA;
 }
 
@@ -979,7 +982,6 @@ extern "C" int fa2_bwd(const void* q, const void* k, const void* v, const void* 
                        int d, float scale, int causal, int dtype, void* stream) {
   int rc = check_shape(B, H, N, d, scale, causal, dtype);
   if (rc) return rc;
-  if (d != 64 && d != 128) return FA2_ERR_UNSUPPORTED;
   const void* ptrs[10] = {q, k, v, o, lse, dout, dq, dk, dv, workspace};
   for (const void* ptr : ptrs)
     if (!ptr) return FA2_ERR_INVALID_ARG;

@@ -444,10 +444,11 @@ constexpr int kPackedScanWords = 32;
 // A sequence whose offsets are out of range (the seq_info checks; with
 // `by_keys` also more than max_units key tiles) holds no units and sets the
 // bad-offsets status bit.  False when this block has no unit; every thread
-// returns the same.
+// returns the same.  `block` (default: this CTA's index) is the grid position
+// to place.
 template <int THREADS>
 __device__ __forceinline__ bool packed_unit(const KernelParams& p, int rows, bool by_keys, int max_units, int group,
-                                            int* scan, SeqInfo& s, int& unit, int& units) {
+                                            int* scan, SeqInfo& s, int& unit, int& units, int block = -1) {
   constexpr int NW = THREADS / 32;
   static_assert(THREADS >= kPackedScanSeqs && NW + 7 <= kPackedScanWords, "packed scan");
   const int nseq = p.bh / p.heads;
@@ -478,7 +479,7 @@ __device__ __forceinline__ bool packed_unit(const KernelParams& p, int rows, boo
   __syncthreads();
   long long start = incl - cnt;
   for (int j = 0; j < w; ++j) start += scan[j];
-  const long long blk = (long long)blockIdx.x;
+  const long long blk = block < 0 ? (long long)blockIdx.x : (long long)block;
   if (cnt > 0 && blk >= start * p.heads && blk < (start + cnt) * p.heads) {
     scan[NW] = i;
     scan[NW + 1] = (int)(blk - start * p.heads);

@@ -86,6 +86,7 @@ struct LaunchArgs {
 struct BwdParams {
   KernelParams f;       // o and lse are the forward's outputs here (read)
   const void* q;        // read by the preprocess (nothing) and the kernels via maps
+  const void* v;        // read directly by the d = 256 kernel (V_j into tensor memory)
   const void* dout;
   void* dq;
   void* dk;
@@ -110,6 +111,7 @@ struct BwdLaunchArgs {
 
 int launch_bwd_d64(const BwdLaunchArgs& a);
 int launch_bwd_d128(const BwdLaunchArgs& a);
+int launch_bwd_d256(const BwdLaunchArgs& a);
 
 // Host-side tile geometry the launcher needs to build tensor maps and size
 // the grid: rows of Q per tile, rows of K/V per streamed tile and query rows

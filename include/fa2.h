@@ -285,7 +285,9 @@ int fa2_get_device_status(void* stream, uint32_t* detail);
  *                      256-byte aligned, owned by the caller: an fp32 dQ
  *                      accumulator [B,H,N,d] and D [B,H,N], both written
  *                      before they are read
- *   d                : 64 or 128 (FA2_ERR_UNSUPPORTED otherwise)
+ *   d                : 64, 128 or 256 (at d = 256 each 128-key tile runs as two
+ *                      CTAs, one per half of the head dimension, that both
+ *                      rebuild the tile's S and dP)
  *   other arguments  : as fa2_fwd
  *
  * dK and dV are each written once; dQ is accumulated over key tiles with
@@ -306,7 +308,7 @@ size_t fa2_bwd_workspace_bytes(int B, int H, int N, int d);
  * batches.  `fwd` holds the forward call's arguments (q, k, v; o and lse
  * are the forward's outputs and are read here); the gradients share the
  * layouts of their primal tensors: dout and dq/dk/dv use o's, q's, k's and
- * v's strides.  head_dim 64 or 128 (FA2_ERR_UNSUPPORTED otherwise).  Packed
+ * v's strides.  head_dim 64, 128 or 256 (FA2_ERR_UNSUPPORTED otherwise).  Packed
  * batches: fwd.seqlen_k is the longest sequence's key count (it sizes the
  * grid; a sequence with more keys is left unwritten and reported as
  * FA2_ERR_DEVICE_SEQLENS; out-of-range offsets behave as in fa2_fwd_ex,

@@ -297,14 +297,16 @@ def _bwd(lib, dout=6 * A, dq=7 * A, dk=8 * A, dv=9 * A, ws=10 * A, ws_bytes=1 <<
 def test_bwd_ex_workspace_plan(lib):
     # [1, 2, 64, 64]: fp32 accumulator 2 x 64 x 64 x 4 bytes + D 2 x 64 x 4 bytes (256-byte aligned)
     assert lib.fa2_bwd_ex_workspace_bytes(ctypes.byref(_params())) == 32768 + 512
-    assert lib.fa2_bwd_ex_workspace_bytes(ctypes.byref(_params(head_dim=256))) == 0
+    # d = 256: the same layout with 256 columns
+    assert lib.fa2_bwd_ex_workspace_bytes(ctypes.byref(_params(head_dim=256))) == 131072 + 512
+    assert lib.fa2_bwd_ex_workspace_bytes(ctypes.byref(_params(head_dim=96))) == 0
     assert lib.fa2_bwd_ex_workspace_bytes(None) == 0
     # the contiguous entry point asks for the same amount
     assert fa2.fa2_bwd_workspace_bytes(1, 2, 64, 64) == 32768 + 512
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(head_dim=256), fa2.FA2_ERR_UNSUPPORTED),
+    (dict(head_dim=96), fa2.FA2_ERR_UNSUPPORTED),
     (dict(dq=0), fa2.FA2_ERR_INVALID_ARG),
     (dict(dout=6 * A + 8), fa2.FA2_ERR_MISALIGNED),
     (dict(ws=10 * A + 64), fa2.FA2_ERR_MISALIGNED),

@@ -69,7 +69,7 @@ def check(got, ref, dtype, label):
 
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("dtype", [sy.FP16, sy.BF16])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("N", [1, 63, 128, 129, 300])
 def test_bwd_small(N, d, dtype, causal):
     B, H = (2, 2) if N <= 129 else (1, 2)
@@ -77,20 +77,21 @@ def test_bwd_small(N, d, dtype, causal):
     check(got, ref, dtype, "N=%d d=%d %s causal=%d" % (N, d, "bf16" if dtype else "fp16", causal))
 
 
-@pytest.mark.parametrize("d,dtype,causal", [(128, sy.BF16, True), (64, sy.FP16, False)])
+@pytest.mark.parametrize("d,dtype,causal", [(128, sy.BF16, True), (64, sy.FP16, False), (256, sy.FP16, False),
+                                            (256, sy.BF16, True)])
 def test_bwd_several_tiles(d, dtype, causal):
     got, ref = run_bwd(1, 2, 1000, d, dtype, causal, 9100 + d)
     check(got, ref, dtype, "N=1000 d=%d" % d)
 
 
 def test_bwd_rejects_unsupported_head_dim():
-    q = torch.zeros(1, 1, 64, 256, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(1, 1, 64, 96, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(fa2.Fa2Error) as e:
         fa2.fa2_bwd(q, q.clone(), q.clone(), q.clone(), torch.zeros(1, 1, 64, device="cuda"), q.clone())
     assert e.value.code == fa2.FA2_ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("index", [2, 3])
+@pytest.mark.parametrize("index", [2, 3, 5])
 def test_bwd_workload_heads(index):
     """The full workload's backward in the benchmark's launch configuration;
     two whole heads (first and last) checked against the oracle."""

@@ -91,7 +91,7 @@ SHAPES = [(1, 1), (64, 200), (200, 64), (129, 129), (300, 700), (700, 300)]
 MASKS = [(-1, -1, 0), (-1, 0, 0), (0, 0, 0), (40, 0, 0), (100, 30, 0), (200, -1, 0), (-1, 0, 70), (5, 0, 150)]
 
 
-@pytest.mark.parametrize("d,dtype", [(64, sy.FP16), (128, sy.BF16), (128, sy.FP16)])
+@pytest.mark.parametrize("d,dtype", [(64, sy.FP16), (128, sy.BF16), (128, sy.FP16), (256, sy.FP16), (256, sy.BF16)])
 @pytest.mark.parametrize("mask", MASKS)
 @pytest.mark.parametrize("Nq,Nk", SHAPES)
 def test_bwd_masks(Nq, Nk, mask, d, dtype):
@@ -103,7 +103,7 @@ def test_bwd_masks(Nq, Nk, mask, d, dtype):
     check(got, ref, dtype, "Nq=%d Nk=%d mask=%s d=%d" % (Nq, Nk, mask, d), visible(Nq, Nk, wl, wr, pre))
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_bwd_bnhd_views(d):
     """q, k, v, o, dout and the gradients as [B, N, H, d] views: dK and dV
     bit-identical to the contiguous call, dQ within fp32 reduce-add rounding."""
@@ -123,11 +123,12 @@ def test_bwd_bnhd_views(d):
     check([g.double().cpu().numpy() for g in g2], ref, dtype, "bnhd d=%d" % d)
 
 
-def test_bwd_packed_sequences():
+@pytest.mark.parametrize("d", [128, 256])
+def test_bwd_packed_sequences(d):
     """Packed sequences of mixed lengths (one without keys, one without
     queries): each sequence's gradients match the oracle on its slice; dq rows
     outside every sequence are zero."""
-    H, d, dtype = 2, 128, sy.BF16
+    H, dtype = 2, sy.BF16
     lens_q = [1, 129, 0, 300, 64, 200]
     lens_k = [1, 200, 5, 300, 0, 513]
     mask = dict(window_left=-1, window_right=0)
@@ -165,7 +166,8 @@ def test_bwd_packed_sequences():
         rk += nk
 
 
-@pytest.mark.parametrize("d,dtype,nseq", [(64, sy.FP16, 192), (128, sy.BF16, 192), (128, sy.BF16, 193)])
+@pytest.mark.parametrize("d,dtype,nseq", [(64, sy.FP16, 192), (128, sy.BF16, 192), (128, sy.BF16, 193),
+                                          (256, sy.FP16, 192), (256, sy.BF16, 193)])
 def test_bwd_packed_many_sequences(d, dtype, nseq):
     """192 packed sequences (the grid holds one CTA per real key tile, each
     finding its sequence from the offsets) and 193 (one CTA per sequence,
@@ -248,6 +250,7 @@ def test_bwd_packed_random_mixes_match_unpacked(trial):
     (2048, 8192, (-1, 0, 0), 128, sy.BF16),     # a query chunk at the end of a long key sequence
     (4096, 4096, (511, 0, 0), 64, sy.FP16),     # sliding window of 512 keys
     (3000, 3000, (-1, 0, 1000), 128, sy.BF16),  # prefix-LM
+    (1500, 3000, (-1, 0, 0), 256, sy.FP16),     # d = 256: a query chunk after a key prefix
 ])
 def test_bwd_masks_larger(Nq, Nk, mask, d, dtype):
     wl, wr, pre = mask
