@@ -46,6 +46,9 @@ KERNEL_SOURCES = ["fa2_common.cuh", "fa2_tile.cuh", "fa2_fwd_dbuf.cuh", "sm103_p
 
 
 BWD_KERNEL_SOURCES = KERNEL_SOURCES + ["fa2_bwd.cuh"]
+# per backward main kernel: the sources its code comes from
+BWD_SOURCES = {"fa2_bwd_kernel": BWD_KERNEL_SOURCES, "fa2_bwd64_kernel": BWD_KERNEL_SOURCES + ["fa2_bwd64.cuh"],
+               "fa2_bwd256_kernel": BWD_KERNEL_SOURCES + ["fa2_bwd256.cuh"]}
 
 
 def kernel_source_hash(names=None) -> str:
@@ -88,7 +91,7 @@ def recorded_traffic(workload: int, kernel: str = "fa2_fwd_dbuf_kernel"):
     path = os.path.join(ROOT, "profiles", "traffic_per_launch.txt")
     if not os.path.exists(path):
         return None
-    src = kernel_source_hash(BWD_KERNEL_SOURCES if kernel == "fa2_bwd_kernel" else KERNEL_SOURCES)
+    src = kernel_source_hash(BWD_SOURCES.get(kernel, KERNEL_SOURCES))
     with open(path) as f:
         for line in f:
             parts = dict(p.split("=", 1) for p in line.split() if "=" in p)
@@ -471,7 +474,8 @@ def spread(region_ms):
             "total_s": float(a.sum()) / 1e3}
 
 
-def time_regions(torch, step, stream, steps: int, flush_buf, graph, first_only: bool = False):
+def time_regions(torch, step, stream, steps: int, flush_buf, graph, first_only: bool = False,
+                 min_total_s: float = MIN_TIMED_S):
     """Time K-step regions on `stream` with CUDA events: one region, or (the
     default) as many as region_count asks for.  A graph replays the K launches
     (region time = its events); without one, each launch has its own events
@@ -510,7 +514,7 @@ def time_regions(torch, step, stream, steps: int, flush_buf, graph, first_only: 
     first, per = one()
     regions, launches = [first], list(per)
     if not first_only:
-        for _ in range(region_count(first) - 1):
+        for _ in range(region_count(first, min_total_s) - 1):
             ms, per = one()
             regions.append(ms)
             launches += per
@@ -530,6 +534,9 @@ def build_parser() -> argparse.ArgumentParser:
     ap.add_argument("--heads", type=int, default=0,
                     help="override H (a smaller case of the same kernel, e.g. for an ncu capture)")
     ap.add_argument("--kernel-only", action="store_true", help="skip the end-to-end and CPU-baseline legs")
+    ap.add_argument("--min-seconds", type=float, default=MIN_TIMED_S,
+                    help="repeat the K-step region until the regions add up to this much device time "
+                         "(at least 3 regions; 0 for a profiler run)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps one by one instead of replaying them from a CUDA graph")
     ap.add_argument("--flush-l2", choices=["auto", "on", "off"], default="auto",
@@ -641,7 +648,7 @@ def main():
     # K-step regions, repeated until they add up to >= 1 s of device time;
     # the line reports the median region (every region is exactly K steps)
     with ClockSampler(local) as clocks:
-        regions, kernel_ms = time_regions(torch, step, stream, args.steps, fbuf, graph)
+        regions, kernel_ms = time_regions(torch, step, stream, args.steps, fbuf, graph, min_total_s=args.min_seconds)
     torch.cuda.synchronize(dev)
     timing = spread(regions)
     elapsed_ms = timing["median_ms"]
@@ -655,7 +662,7 @@ def main():
     if flush and rank == 0:
         # the same launches back to back from a CUDA graph, L2 not overwritten
         g2 = capture()
-        r2, _ = time_regions(torch, step, stream, args.steps, None, g2)
+        r2, _ = time_regions(torch, step, stream, args.steps, None, g2, min_total_s=args.min_seconds)
         unflushed = spread(r2)
         del g2
 
@@ -720,7 +727,7 @@ def main():
             "timing": dict(timing, steps_per_region=args.steps,
                            rule="median over regions of exactly K steps, each bracketed by a synchronize and "
                                 "timed with CUDA events on the launching stream; regions repeated until they add "
-                                "up to >= %.0f s of device time; value = max over ranks of the median" % MIN_TIMED_S),
+                                "up to >= %g s of device time; value = max over ranks of the median" % args.min_seconds),
             "pct_of_peak": 100.0 * value / ws / peak,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                          "frac": achieved / peak,
@@ -735,7 +742,7 @@ def main():
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                        "samples": clk["samples"]},
             "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": args.steps * (3 if args.backward else 1),
-            "kernel_sha": kernel_source_hash(BWD_KERNEL_SOURCES if args.backward else KERNEL_SOURCES),
+            "kernel_sha": kernel_source_hash(BWD_SOURCES.get(kname, KERNEL_SOURCES)),
         }
         # the memory side of the roofline: algorithmic bytes per launch over the launch time
         hbm, hbm_note = measured_hbm()
