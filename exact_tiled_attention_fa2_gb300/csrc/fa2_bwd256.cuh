@@ -126,7 +126,7 @@ __device__ __forceinline__ void bwd256_producer(const BwdCtx& t, const CUtensorM
 }
 
 template <class C, bool BF16>
-__device__ __forceinline__ void bwd256_mma(const BwdCtx& t, int half) {
+__device__ __forceinline__ void bwd256_mma(const BwdCtx& t, int dhalf) {
   constexpr uint32_t idesc_s = make_idesc_f16(128, C::TQ, BF16, false, false);    // S^T, dP^T (N = 64 queries)
   constexpr uint32_t idesc_acc = make_idesc_f16(128, C::DH, BF16, false, true);   // dV, dK: A in TMEM, B MN-major
   constexpr uint32_t idesc_dq = make_idesc_f16(128, C::DH, BF16, true, true);     // dQ: A, B MN-major
@@ -134,9 +134,9 @@ __device__ __forceinline__ void bwd256_mma(const BwdCtx& t, int half) {
   const uint64_t q_kmaj0 = make_sdesc_sw128(t.sQ, 16, 1024);
   const uint64_t do_kmaj0 = make_sdesc_sw128(t.sDO, 16, 1024);
   // half c of Q_t / dO_t / K_j: its two 64-column blocks, N-adjacent at the block stride
-  const uint64_t q_mn0 = make_sdesc_sw128(t.sQ + 2 * half * C::QBLK, C::QBLK, 1024);
-  const uint64_t do_mn0 = make_sdesc_sw128(t.sDO + 2 * half * C::QBLK, C::QBLK, 1024);
-  const uint64_t k_mn = make_sdesc_sw128(t.sK + 2 * half * C::KBLK, C::KBLK, 1024);
+  const uint64_t q_mn0 = make_sdesc_sw128(t.sQ + 2 * dhalf * C::QBLK, C::QBLK, 1024);
+  const uint64_t do_mn0 = make_sdesc_sw128(t.sDO + 2 * dhalf * C::QBLK, C::QBLK, 1024);
+  const uint64_t k_mn = make_sdesc_sw128(t.sK + 2 * dhalf * C::KBLK, C::KBLK, 1024);
   const uint64_t ds_mn = make_sdesc_sw128(t.sDS, C::DS_HALF, 1024);   // the pair's 128 queries: 2 halves
   const uint32_t tS = t.tmem + C::TMEM_S, tDP = t.tmem + C::TMEM_DP, tV = t.tmem + C::TMEM_V;
   const uint32_t tDV = t.tmem + C::TMEM_DV, tDK = t.tmem + C::TMEM_DK;
@@ -212,7 +212,7 @@ __device__ __forceinline__ void bwd256_mma(const BwdCtx& t, int half) {
 
 template <class C, bool BF16>
 __device__ __forceinline__ void bwd256_elementwise(const BwdCtx& t, const BwdParams& p, const KeyMask& km,
-                                                   uint8_t* smem, int warp, int lane, int half,
+                                                   uint8_t* smem, int warp, int lane, int dhalf,
                                                    const CUtensorMap* tm_dq) {
   const KernelParams& f = p.f;
   const int quad = warp & 3;
@@ -299,7 +299,7 @@ __device__ __forceinline__ void bwd256_elementwise(const BwdCtx& t, const BwdPar
 #pragma unroll
         for (int b = 0; b < 2; ++b)
           tma_reduce_add_3d(tm_dq, smem_u32(smem + C::OFF_DS + b * C::DS_HALF + quad * 4096),
-                            C::DH * half + 64 * round + 32 * b, y, t.hb);
+                            C::DH * dhalf + 64 * round + 32 * b, y, t.hb);
         bulk_commit_group();
       }
     }
@@ -406,7 +406,7 @@ __device__ __forceinline__ void bwd256_elementwise(const BwdCtx& t, const BwdPar
                                      (long long)(t.seq.row0_k + key) * p.k_rs
                                : (long long)t.seq.b * p.v_bs + (long long)t.seq.h * p.v_hs +
                                      (long long)(t.seq.row0_k + key) * p.v_rs) +
-                        (long long)C::DH * half);
+                        (long long)C::DH * dhalf);
 #pragma unroll 1
     for (int c = 0; c < C::DH; c += 32) {
       uint32_t pk16[16];
@@ -429,7 +429,7 @@ __device__ __forceinline__ void bwd256_elementwise(const BwdCtx& t, const BwdPar
   }
 }
 
-// One CTA per (key tile, half of d); blocks 2u and 2u + 1 are the two halves
+// One CTA per (key tile, half dhalf of d); blocks 2u and 2u + 1 are the two halves
 // of the key tile the forward kernels' unit order gives block u.  PACKED: a
 // packed batch whose grid holds only its real key tiles, as in fa2_bwd_kernel.
 template <bool BF16, bool PACKED>
@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(192, 1)
   const int warp = (int)(threadIdx.x >> 5);
   const int lane = (int)(threadIdx.x & 31);
   const KernelParams& f = p.f;
-  const int half = (int)(blockIdx.x & 1u);
+  const int dhalf = (int)(blockIdx.x & 1u);
   const int block = (int)(blockIdx.x >> 1);
 
   BwdCtx t;
@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(192, 1)
     unit_of_block(block, f.bh, p.num_k_tiles, bh, unit, 4);
     if (!seq_info(f, bh, t.seq)) return;
     if (t.seq.n_k > p.num_k_tiles * C::T) {
-      if (threadIdx.x == 0 && unit == 0 && half == 0) atomicOr(f.status, kStatusBadSeqlens);
+      if (threadIdx.x == 0 && unit == 0 && dhalf == 0) atomicOr(f.status, kStatusBadSeqlens);
       return;
     }
   }
@@ -525,10 +525,10 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == C::TMA_WARP) {
     if (lane == 0 && t.niter > 0) bwd256_producer<C>(t, &tm_q, &tm_k, &tm_do, false);
   } else if (warp == C::MMA_WARP) {
-    if (lane == 0 && t.niter > 0) bwd256_mma<C, BF16>(t, half);
+    if (lane == 0 && t.niter > 0) bwd256_mma<C, BF16>(t, dhalf);
     __syncwarp();
   } else {
-    bwd256_elementwise<C, BF16>(t, p, km, smem, warp, lane, half, &tm_dq);
+    bwd256_elementwise<C, BF16>(t, p, km, smem, warp, lane, dhalf, &tm_dq);
   }
   tc_fence_before();
   __syncthreads();
