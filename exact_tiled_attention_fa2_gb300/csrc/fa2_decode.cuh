@@ -99,12 +99,6 @@ __device__ __forceinline__ void unpack8(const uint4& u, float* x) {
   }
 }
 
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-
 // The chunk of keys [c0, c1) one CTA reduces, within a sequence, clipped to
 // the keys some query row sees; false if empty.
 __device__ __forceinline__ bool decode_range(const KeyMask& km, int n_q, int split, int chunk, int base, int& c0,

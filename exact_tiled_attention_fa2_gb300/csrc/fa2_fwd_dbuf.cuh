@@ -20,11 +20,12 @@
 // O~ rescaled in place when it is.
 //
 // Size classes: at d <= 128 a CTA takes 256 TMEM columns (two S buffers +
-// O~) and ~100 KB of shared memory (Q 32 KB at d = 128, K and V rings), so two
-// CTAs share an SM: one CTA's set-up, first loads and epilogue overlap the
-// other's products, and the two CTAs' MMAs interleave on the tensor pipe.
-// At d = 256 O~ alone takes 256 columns and Q 64 KB: one CTA per SM, whose PV
-// products have N = 256.
+// O~, and at d = 64 a copy of Q_i) and ~100 KB of shared memory (Q 32 KB at
+// d = 128, K and V rings), so two CTAs share an SM: one CTA's set-up, first
+// loads and epilogue overlap the other's products, and the two CTAs' MMAs
+// interleave on the tensor pipe.  At d = 256 O~ alone takes 256 columns and Q
+// 64 KB: one CTA per SM, whose PV products have N = 256.  At d = 64 and 256
+// the S products read Q_i from tensor memory (DbufConfig::Q_IN_TMEM).
 //
 // Warp roles (192 threads): warps 0-3 softmax + epilogue (one thread per
 // query row = TMEM lane), warp 4 TMEM owner and MMA issuer, warp 5 TMA.
@@ -63,8 +64,16 @@ struct DbufConfig {
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t MISC_BYTES = 128 + 4 * kPackedScanWords;  // TMEM address, abort flag, CtaFacts; scan
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;
+  // Where the columns allow it (d = 64: 224 of 256; d = 256: all 512), the
+  // softmax warps copy Q_i once into tensor memory and the S products take it
+  // from there as their A operand, reading only K_j from shared memory.
+  // Measured on the same GB300: +1.8 % at d = 64 (B8 H16 N2048) and +1.9 % at
+  // d = 256 (B2 H8 N3000), same results bit for bit.  At d = 128 two CTAs per
+  // SM fill the tensor memory without it.
+  static constexpr bool Q_IN_TMEM = (D == 64 || D == 256);
   static constexpr uint32_t TMEM_S = 0;     // + 64 * buffer
-  static constexpr uint32_t TMEM_O = 128;
+  static constexpr uint32_t TMEM_Q = 128;   // Q_i as 16-bit pairs (Q_IN_TMEM)
+  static constexpr uint32_t TMEM_O = Q_IN_TMEM ? TMEM_Q + D / 2 : 128;
   static constexpr uint32_t TMEM_COLS = (D == 256) ? 512 : 256;
   static constexpr int CTAS_PER_SM = (D == 256) ? 1 : 2;   // TMEM and shared memory allow two below d = 256
   // The TMA thread, not the MMA thread, checks that V_j and K_{j+2} have landed
@@ -96,6 +105,7 @@ enum : int {
                    // phases ahead of the parity the MMA thread waits for.
                    // Arrivals: the four softmax warps, and with TMA_GATES_P the
                    // TMA thread (V_j and K_{j+2} in shared memory).
+  DB_QT = 17,      // Q_IN_TMEM: Q_i copied into tensor memory (four softmax warps)
 };
 
 // One query tile's work, shared by the CTA's warp roles.
@@ -231,14 +241,20 @@ __device__ __forceinline__ void db_mma(const DbufCtx& t, const KernelParams& p) 
     }
     const uint64_t b0 = dk0 + (uint64_t)((sk * C::KV_BYTES) >> 4);
     const uint32_t tS = t.tmem + C::TMEM_S + 64 * (j & 1);
+    if constexpr (C::Q_IN_TMEM) {
 #pragma unroll
-    for (int k = 0; k < C::D / 16; ++k)
-      umma_ss(tS, dq0 + kmajor_step<C>(k, C::BR), b0 + kmajor_step<C>(k, C::BC), idesc_qk, k > 0 ? 1u : 0u);
+      for (int k = 0; k < C::D / 16; ++k)   // 16 elements of the head dim = 8 columns of Q_i
+        umma_ts(tS, t.tmem + C::TMEM_Q + k * 8, b0 + kmajor_step<C>(k, C::BC), idesc_qk, k > 0 ? 1u : 0u);
+    } else {
+#pragma unroll
+      for (int k = 0; k < C::D / 16; ++k)
+        umma_ss(tS, dq0 + kmajor_step<C>(k, C::BR), b0 + kmajor_step<C>(k, C::BC), idesc_qk, k > 0 ? 1u : 0u);
+    }
     umma_commit(t.bar(DB_S + (j & 1)));
     umma_commit(t.bar(DB_KEMPTY + sk));
     return true;
   };
-  if (t.nkv > 0 && wait_or_abort(t.bar(DB_Q), 0, t.abort_flag, t.status, kSiteMmaQ)) {
+  if (t.nkv > 0 && wait_or_abort(t.bar(C::Q_IN_TMEM ? DB_QT : DB_Q), 0, t.abort_flag, t.status, kSiteMmaQ)) {
     tc_fence_after();
     ok = issue_s(0);
     if (ok && t.nkv > 1) ok = issue_s(1);
@@ -299,7 +315,34 @@ __device__ __forceinline__ void db_softmax(const DbufCtx& t, const KernelParams&
   float m_run = -INFINITY;
   float l_run = 0.f;
   bool ok = true;
-  for (int j = 0; j < t.nkv; ++j) {
+  if constexpr (C::Q_IN_TMEM) {
+    // Row r of Q_i from its 128-byte-swizzled shared-memory blocks (16-byte
+    // chunk c of a row stored at chunk c ^ (r & 7)) into TMEM lane r, 64
+    // elements = 32 columns per block.  TMA has zero-filled rows past N.
+    ok = wait_or_abort(t.bar(DB_Q), 0, t.abort_flag, t.status, kSiteMmaQ);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+#pragma unroll 1
+      for (int kb = 0; kb < C::D / 64; ++kb) {
+        const uint32_t src = t.sQ + kb * (C::BR * 128) + r * 128;
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 x = lds128(src + ((c ^ (r & 7)) << 4));
+          w[4 * c] = x.x;
+          w[4 * c + 1] = x.y;
+          w[4 * c + 2] = x.z;
+          w[4 * c + 3] = x.w;
+        }
+        tmem_st_32x32b_x32(t.tmem + lane_off + C::TMEM_Q + kb * 32, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(t.bar(DB_QT));
+    }
+  }
+  for (int j = 0; ok && j < t.nkv; ++j) {
     const uint32_t tS = t.tmem + lane_off + C::TMEM_S + 64 * (j & 1);
     ok = wait_or_abort(t.bar(DB_S + (j & 1)), (uint32_t)(j >> 1) & 1, t.abort_flag, t.status, kSiteSoftmaxS);
     ok = __all_sync(0xffffffffu, ok);
@@ -476,6 +519,7 @@ __global__ void __launch_bounds__(192, DbufConfig<D>::CTAS_PER_SM)
     mbar_init(t.bar(DB_O), 1);
     mbar_init(t.bar(DB_OLAST), 1);
     mbar_init(t.bar(DB_EXIT), 1);
+    if (C::Q_IN_TMEM) mbar_init(t.bar(DB_QT), 4);
     *abort_flag = 0;
     facts->seq = t.seq;
     facts->km = t.km;
