@@ -65,6 +65,14 @@ def _load():
         lib.oracle_attention_bwd.argtypes = [p16, p16, p16, p16, ctypes.c_int, i64, i64, i64, i64, ctypes.c_double,
                                              ctypes.c_int, pd, pd, pd, pd, ctypes.c_int]
         lib.oracle_attention_bwd.restype = ctypes.c_int
+        lib.oracle_attention_bwd_rows.argtypes = [p16, p16, p16, p16, ctypes.c_int, i64, i64, i64, i64,
+                                                  ctypes.c_double, ctypes.c_int, pi64, pi64, i64, pd, pd,
+                                                  ctypes.c_int]
+        lib.oracle_attention_bwd_rows.restype = ctypes.c_int
+        lib.oracle_attention_bwd_keys.argtypes = [p16, p16, p16, p16, ctypes.c_int, i64, i64, i64, i64,
+                                                  ctypes.c_double, ctypes.c_int, i64, pi64, i64, pd, pd,
+                                                  ctypes.c_int]
+        lib.oracle_attention_bwd_keys.restype = ctypes.c_int
         lib.oracle_attention_fwd_masked.argtypes = [p16, p16, p16, ctypes.c_int, i64, i64, i64, i64, i64,
                                                     ctypes.c_double, i64, i64, i64, pd, pd, ctypes.c_int]
         lib.oracle_attention_fwd_masked.restype = ctypes.c_int
@@ -196,6 +204,49 @@ def attention_bwd(q, k, v, dout, dtype: int, scale: float, causal: bool, threads
     if rc:
         raise ValueError("oracle_attention_bwd failed (%d)" % rc)
     return dq, dk, dv, delta
+
+
+def attention_bwd_rows(q, k, v, dout, dtype: int, scale: float, causal: bool, bh_idx, row_idx, threads: int = 0):
+    """dQ rows [count, d] and D [count] of the backward at the sampled (bh, row)
+    pairs, from 16-bit bit patterns [B,H,N,d], float64: the rows pass of
+    attention_bwd for those rows only."""
+    q, k, v, dout = _bits(q), _bits(k), _bits(v), _bits(dout)
+    B, H, N, d = q.shape
+    bh_idx = np.ascontiguousarray(bh_idx, dtype=np.int64)
+    row_idx = np.ascontiguousarray(row_idx, dtype=np.int64)
+    count = bh_idx.size
+    if row_idx.size != count:
+        raise ValueError("bh_idx and row_idx must have one length")
+    dq = np.empty((count, d))
+    delta = np.empty((count,))
+    rc = _load().oracle_attention_bwd_rows(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
+                                           _ptr(v, ctypes.c_uint16), _ptr(dout, ctypes.c_uint16), int(dtype), B, H,
+                                           N, d, float(scale), int(bool(causal)), _ptr(bh_idx, ctypes.c_int64),
+                                           _ptr(row_idx, ctypes.c_int64), count, _ptr(dq, ctypes.c_double),
+                                           _ptr(delta, ctypes.c_double), int(threads))
+    if rc:
+        raise ValueError("oracle_attention_bwd_rows failed (%d)" % rc)
+    return dq, delta
+
+
+def attention_bwd_keys(q, k, v, dout, dtype: int, scale: float, causal: bool, bh: int, key_idx, threads: int = 0):
+    """dK and dV rows [count, d] of the backward at the sampled keys of slice
+    bh (= b * H + h), from 16-bit bit patterns [B,H,N,d], float64: the keys
+    pass of attention_bwd for those keys, over every row that sees them."""
+    q, k, v, dout = _bits(q), _bits(k), _bits(v), _bits(dout)
+    B, H, N, d = q.shape
+    key_idx = np.ascontiguousarray(key_idx, dtype=np.int64)
+    count = key_idx.size
+    dk = np.empty((count, d))
+    dv = np.empty((count, d))
+    rc = _load().oracle_attention_bwd_keys(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
+                                           _ptr(v, ctypes.c_uint16), _ptr(dout, ctypes.c_uint16), int(dtype), B, H,
+                                           N, d, float(scale), int(bool(causal)), int(bh),
+                                           _ptr(key_idx, ctypes.c_int64), count, _ptr(dk, ctypes.c_double),
+                                           _ptr(dv, ctypes.c_double), int(threads))
+    if rc:
+        raise ValueError("oracle_attention_bwd_keys failed (%d)" % rc)
+    return dk, dv
 
 
 def _masked_shapes(q, k, v):

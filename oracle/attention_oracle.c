@@ -254,6 +254,62 @@ int oracle_attention_fwd_f64(const double* q, const double* k, const double* v, 
 
 /* Backward of one (b,h) slice: q, k, v, dout are N x d; writes dq, dk, dv
  * (N x d) and delta (N). */
+/* Row i of the backward: P_i, dP_i, D_i, dS_i and dQ_i (dq_i, d values),
+ * with the row statistics m_i, l_i.  p and dp are N-long scratch rows. */
+static void bwd_row(const double* q, const double* k, const double* v, const double* dout, int64_t N, int64_t d,
+                    double scale, int causal, int64_t i, double* p, double* dp, double* dq_i, double* m_i,
+                    double* l_i, double* delta_i) {
+  const int64_t nvis = causal ? (i + 1 < N ? i + 1 : N) : N;
+  const double* qi = q + i * d;
+  const double* doi = dout + i * d;
+  double mi = -INFINITY;
+  for (int64_t j = 0; j < nvis; ++j) {
+    double acc = 0.0;
+    for (int64_t c = 0; c < d; ++c) acc += qi[c] * k[j * d + c];
+    p[j] = scale * acc;
+    if (p[j] > mi) mi = p[j];
+  }
+  double li = 0.0;
+  for (int64_t j = 0; j < nvis; ++j) { p[j] = exp(p[j] - mi); li += p[j]; }
+  for (int64_t j = 0; j < nvis; ++j) p[j] /= li;
+  double di = 0.0;
+  for (int64_t j = 0; j < nvis; ++j) {
+    double acc = 0.0;
+    for (int64_t c = 0; c < d; ++c) acc += doi[c] * v[j * d + c];
+    dp[j] = acc;
+    di += p[j] * dp[j];
+  }
+  for (int64_t c = 0; c < d; ++c) dq_i[c] = 0.0;
+  for (int64_t j = 0; j < nvis; ++j) {
+    const double ds = p[j] * (dp[j] - di);
+    for (int64_t c = 0; c < d; ++c) dq_i[c] += scale * ds * k[j * d + c];
+  }
+  *m_i = mi;
+  *l_i = li;
+  *delta_i = di;
+}
+
+/* Key j of the backward: dK_j and dV_j summed over the rows i that see key j,
+ * P_ij and dS_ij rebuilt from the rows' statistics m, l and delta. */
+static void bwd_key(const double* q, const double* k, const double* v, const double* dout, int64_t N, int64_t d,
+                    double scale, int causal, int64_t j, const double* m, const double* l, const double* delta,
+                    double* dk_j, double* dv_j) {
+  for (int64_t c = 0; c < d; ++c) { dk_j[c] = 0.0; dv_j[c] = 0.0; }
+  for (int64_t i = causal ? j : 0; i < N; ++i) {
+    double s = 0.0, dpij = 0.0;
+    for (int64_t c = 0; c < d; ++c) {
+      s += q[i * d + c] * k[j * d + c];
+      dpij += dout[i * d + c] * v[j * d + c];
+    }
+    const double pij = exp(scale * s - m[i]) / l[i];
+    const double ds = pij * (dpij - delta[i]);
+    for (int64_t c = 0; c < d; ++c) {
+      dv_j[c] += pij * dout[i * d + c];
+      dk_j[c] += scale * ds * q[i * d + c];
+    }
+  }
+}
+
 static int attention_bwd_slice(const double* q, const double* k, const double* v, const double* dout, int64_t N,
                                int64_t d, double scale, int causal, double* dq, double* dk, double* dv,
                                double* delta) {
@@ -270,36 +326,8 @@ static int attention_bwd_slice(const double* q, const double* k, const double* v
       nomem = 1;
     } else {
 #pragma omp for schedule(dynamic, 4)
-      for (int64_t i = 0; i < N; ++i) {
-        const int64_t nvis = causal ? (i + 1 < N ? i + 1 : N) : N;
-        const double* qi = q + i * d;
-        const double* doi = dout + i * d;
-        double mi = -INFINITY;
-        for (int64_t j = 0; j < nvis; ++j) {
-          double acc = 0.0;
-          for (int64_t c = 0; c < d; ++c) acc += qi[c] * k[j * d + c];
-          p[j] = scale * acc;
-          if (p[j] > mi) mi = p[j];
-        }
-        double li = 0.0;
-        for (int64_t j = 0; j < nvis; ++j) { p[j] = exp(p[j] - mi); li += p[j]; }
-        for (int64_t j = 0; j < nvis; ++j) p[j] /= li;
-        double di = 0.0;
-        for (int64_t j = 0; j < nvis; ++j) {
-          double acc = 0.0;
-          for (int64_t c = 0; c < d; ++c) acc += doi[c] * v[j * d + c];
-          dp[j] = acc;
-          di += p[j] * dp[j];
-        }
-        for (int64_t c = 0; c < d; ++c) dq[i * d + c] = 0.0;
-        for (int64_t j = 0; j < nvis; ++j) {
-          const double ds = p[j] * (dp[j] - di);
-          for (int64_t c = 0; c < d; ++c) dq[i * d + c] += scale * ds * k[j * d + c];
-        }
-        m[i] = mi;
-        l[i] = li;
-        delta[i] = di;
-      }
+      for (int64_t i = 0; i < N; ++i)
+        bwd_row(q, k, v, dout, N, d, scale, causal, i, p, dp, dq + i * d, m + i, l + i, delta + i);
     }
     free(p);
     free(dp);
@@ -307,22 +335,7 @@ static int attention_bwd_slice(const double* q, const double* k, const double* v
   if (nomem) { free(m); free(l); return ORACLE_ERR_NOMEM; }
   /* keys: dK_j, dV_j over the rows that see key j */
 #pragma omp parallel for schedule(dynamic, 4)
-  for (int64_t j = 0; j < N; ++j) {
-    for (int64_t c = 0; c < d; ++c) { dk[j * d + c] = 0.0; dv[j * d + c] = 0.0; }
-    for (int64_t i = causal ? j : 0; i < N; ++i) {
-      double s = 0.0, dpij = 0.0;
-      for (int64_t c = 0; c < d; ++c) {
-        s += q[i * d + c] * k[j * d + c];
-        dpij += dout[i * d + c] * v[j * d + c];
-      }
-      const double pij = exp(scale * s - m[i]) / l[i];
-      const double ds = pij * (dpij - delta[i]);
-      for (int64_t c = 0; c < d; ++c) {
-        dv[j * d + c] += pij * dout[i * d + c];
-        dk[j * d + c] += scale * ds * q[i * d + c];
-      }
-    }
-  }
+  for (int64_t j = 0; j < N; ++j) bwd_key(q, k, v, dout, N, d, scale, causal, j, m, l, delta, dk + j * d, dv + j * d);
   free(m);
   free(l);
   return ORACLE_OK;
@@ -368,6 +381,111 @@ int oracle_attention_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v
                                 delta, threads);
   free(buf);
   return rc;
+}
+
+/* dQ rows and D_i of the backward at sampled (bh, row) pairs, on 16-bit
+ * inputs (widened exactly first): the rows pass of the backward above, for
+ * the listed rows only.  dq [count, d], delta [count]. */
+int oracle_attention_bwd_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout,
+                              int dtype, int64_t B, int64_t H, int64_t N, int64_t d, double scale, int causal,
+                              const int64_t* bh_idx, const int64_t* row_idx, int64_t count, double* dq,
+                              double* delta, int threads) {
+  int rc = check_args(q, k, v, dtype, B, H, N, d, scale);
+  if (rc) return rc;
+  if (!dout || !bh_idx || !row_idx || count < 0 || !dq || !delta) return ORACLE_ERR_ARG;
+  for (int64_t s = 0; s < count; ++s)
+    if (bh_idx[s] < 0 || bh_idx[s] >= B * H || row_idx[s] < 0 || row_idx[s] >= N) return ORACLE_ERR_ARG;
+#ifdef _OPENMP
+  if (threads > 0) omp_set_num_threads(threads);
+#else
+  (void)threads;
+#endif
+  const int64_t slice = N * d;
+  int nomem = 0;
+#pragma omp parallel reduction(| : nomem)
+  {
+    double* buf = (double*)malloc(sizeof(double) * (size_t)(4 * slice + 2 * N));
+    if (!buf) {
+      nomem = 1;
+    } else {
+      int64_t have = -1;   /* the (b, h) slice widened in buf */
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t s = 0; s < count; ++s) {
+        const int64_t bh = bh_idx[s];
+        if (bh != have) {
+          const int64_t off = bh * slice;
+          for (int64_t x = 0; x < slice; ++x) {
+            buf[x] = widen(q[off + x], dtype);
+            buf[slice + x] = widen(k[off + x], dtype);
+            buf[2 * slice + x] = widen(v[off + x], dtype);
+            buf[3 * slice + x] = widen(dout[off + x], dtype);
+          }
+          have = bh;
+        }
+        double m_i, l_i;
+        bwd_row(buf, buf + slice, buf + 2 * slice, buf + 3 * slice, N, d, scale, causal, row_idx[s],
+                buf + 4 * slice, buf + 4 * slice + N, dq + s * d, &m_i, &l_i, delta + s);
+      }
+    }
+    free(buf);
+  }
+  return nomem ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+/* dK and dV rows of the backward at sampled keys of one (b, h) slice bh, on
+ * 16-bit inputs: the rows pass for every row that sees one of the keys (with
+ * causal masking the rows from the smallest key on), then the keys pass for
+ * the listed keys.  dk, dv [count, d]. */
+int oracle_attention_bwd_keys(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout,
+                              int dtype, int64_t B, int64_t H, int64_t N, int64_t d, double scale, int causal,
+                              int64_t bh, const int64_t* key_idx, int64_t count, double* dk, double* dv,
+                              int threads) {
+  int rc = check_args(q, k, v, dtype, B, H, N, d, scale);
+  if (rc) return rc;
+  if (!dout || !key_idx || count < 0 || !dk || !dv || bh < 0 || bh >= B * H) return ORACLE_ERR_ARG;
+  int64_t first = N;
+  for (int64_t s = 0; s < count; ++s) {
+    if (key_idx[s] < 0 || key_idx[s] >= N) return ORACLE_ERR_ARG;
+    if (key_idx[s] < first) first = key_idx[s];
+  }
+  const int64_t i0 = causal ? first : 0;   /* rows before i0 see none of the keys */
+#ifdef _OPENMP
+  if (threads > 0) omp_set_num_threads(threads);
+#else
+  (void)threads;
+#endif
+  const int64_t slice = N * d, off = bh * slice;
+  double* buf = (double*)malloc(sizeof(double) * (size_t)(4 * slice + 3 * N));
+  if (!buf) return ORACLE_ERR_NOMEM;
+  double *qd = buf, *kd = buf + slice, *vd = buf + 2 * slice, *dod = buf + 3 * slice;
+  double *m = buf + 4 * slice, *l = m + N, *delta = l + N;
+  for (int64_t x = 0; x < slice; ++x) {
+    qd[x] = widen(q[off + x], dtype);
+    kd[x] = widen(k[off + x], dtype);
+    vd[x] = widen(v[off + x], dtype);
+    dod[x] = widen(dout[off + x], dtype);
+  }
+  int nomem = 0;
+#pragma omp parallel reduction(| : nomem)
+  {
+    double* scratch = (double*)malloc(sizeof(double) * (size_t)(2 * N + d));
+    if (!scratch) {
+      nomem = 1;
+    } else {
+#pragma omp for schedule(dynamic, 4)
+      for (int64_t i = i0; i < N; ++i)
+        bwd_row(qd, kd, vd, dod, N, d, scale, causal, i, scratch, scratch + N, scratch + 2 * N, m + i, l + i,
+                delta + i);
+    }
+    free(scratch);
+  }
+  if (!nomem) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t s = 0; s < count; ++s)
+      bwd_key(qd, kd, vd, dod, N, d, scale, causal, key_idx[s], m, l, delta, dk + s * d, dv + s * d);
+  }
+  free(buf);
+  return nomem ? ORACLE_ERR_NOMEM : ORACLE_OK;
 }
 
 /* ------------------------------------------------------------------ masks and N_q != N_k */

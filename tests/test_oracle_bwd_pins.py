@@ -93,3 +93,51 @@ def test_16bit_entry_equals_widened_f64_entry():
     g64 = oracle.attention_bwd_f64(*(oracle.widen(x, sy.BF16) for x in (q, k, v, dout)), 0.35, True)
     for a, b in zip(g16, g64):
         np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_sampled_rows_equal_the_full_backward(causal):
+    # the sampled-row entry point runs the rows pass of the full backward for
+    # the listed rows: dQ rows and D_i equal the full function's, bit for bit
+    B, H, N, d = 2, 3, 37, 16
+    q, k, v = sy.make_qkv(B, H, N, d, sy.FP16, 41)
+    dout = sy.make_qkv(B, H, N, d, sy.FP16, 42)[0]
+    dq, _, _, delta = oracle.attention_bwd(q, k, v, dout, sy.FP16, 0.25, causal)
+    rng = np.random.default_rng(43)
+    bh_idx = np.sort(rng.integers(0, B * H, size=40))
+    row_idx = rng.integers(0, N, size=40)
+    dq_rows, delta_rows = oracle.attention_bwd_rows(q, k, v, dout, sy.FP16, 0.25, causal, bh_idx, row_idx)
+    np.testing.assert_array_equal(dq_rows, dq.reshape(B * H, N, d)[bh_idx, row_idx])
+    np.testing.assert_array_equal(delta_rows, delta.reshape(B * H, N)[bh_idx, row_idx])
+
+
+def test_sampled_rows_reject_out_of_range_indices():
+    q, k, v = sy.make_qkv(1, 1, 8, 4, sy.FP16, 44)
+    with pytest.raises(ValueError):
+        oracle.attention_bwd_rows(q, k, v, q, sy.FP16, 0.5, False, np.array([1]), np.array([0]))
+    with pytest.raises(ValueError):
+        oracle.attention_bwd_rows(q, k, v, q, sy.FP16, 0.5, False, np.array([0]), np.array([8]))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_sampled_keys_equal_the_full_backward(causal):
+    # the sampled-key entry point runs the keys pass of the full backward for
+    # the listed keys (over the rows that see them): dK and dV rows equal the
+    # full function's, bit for bit
+    B, H, N, d = 1, 3, 45, 16
+    q, k, v = sy.make_qkv(B, H, N, d, sy.BF16, 51)
+    dout = sy.make_qkv(B, H, N, d, sy.BF16, 52)[0]
+    _, dk, dv, _ = oracle.attention_bwd(q, k, v, dout, sy.BF16, 0.3, causal)
+    keys = np.array([44, 40, 31, 3, 0, 44])
+    for bh in range(B * H):
+        dk_rows, dv_rows = oracle.attention_bwd_keys(q, k, v, dout, sy.BF16, 0.3, causal, bh, keys)
+        np.testing.assert_array_equal(dk_rows, dk.reshape(B * H, N, d)[bh, keys])
+        np.testing.assert_array_equal(dv_rows, dv.reshape(B * H, N, d)[bh, keys])
+
+
+def test_sampled_keys_reject_out_of_range_indices():
+    q, k, v = sy.make_qkv(1, 1, 8, 4, sy.FP16, 53)
+    with pytest.raises(ValueError):
+        oracle.attention_bwd_keys(q, k, v, q, sy.FP16, 0.5, True, 1, np.array([0]))
+    with pytest.raises(ValueError):
+        oracle.attention_bwd_keys(q, k, v, q, sy.FP16, 0.5, True, 0, np.array([8]))
