@@ -333,6 +333,7 @@ __global__ void __launch_bounds__(DecodeConfig<D>::THREADS, 2)
   const int warp = (int)(threadIdx.x >> 5);
   const int lane = (int)(threadIdx.x & 31);
   const KernelParams& p = dp.f;
+  grid_launch_dependents();   // the merge kernel may be scheduled now; it waits for this grid's partials
 
   const int bh = (int)blockIdx.x / dp.splits;
   const int split = (int)blockIdx.x - bh * dp.splits;
@@ -404,9 +405,13 @@ __global__ void __launch_bounds__(DecodeConfig<D>::THREADS, 2)
 }
 
 // One block per (b*h, query row): merge the row's partials, store O and LSE.
+// Launched right behind the split kernel with programmatic stream
+// serialization (launch_decode_merge), so its launch overlaps that kernel's
+// last CTAs.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(128)
     fa2_decode_merge_kernel(const DecodeParams dp) {
+  grid_dependency_wait();   // the split kernel's partials are complete and visible
   const KernelParams& p = dp.f;
   const int bh = (int)blockIdx.x / p.n_q;
   const int r = (int)blockIdx.x - bh * p.n_q;
@@ -446,6 +451,23 @@ __global__ void __launch_bounds__(128)
         empty ? -INFINITY : (M + log2f(L)) * 0.6931471805599453f;
 }
 
+// The merge behind a split kernel on the same stream, as a programmatic
+// dependent launch (its blocks wait in grid_dependency_wait for the partials).
+template <int D, bool BF16>
+int launch_decode_merge(const DecodeParams& dp, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((long long)dp.f.bh * dp.f.n_q));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return (int)cudaLaunchKernelEx(&cfg, fa2_decode_merge_kernel<D, BF16>, dp);
+}
+
 template <int D, bool BF16, int NQ>
 int launch_decode_nq(const DecodeLaunchArgs& a) {
   using C = DecodeConfig<D>;
@@ -459,8 +481,7 @@ int launch_decode_nq(const DecodeLaunchArgs& a) {
   kern<<<(unsigned)blocks, C::THREADS, C::SMEM_BYTES, a.stream>>>(a.tm_k, a.tm_v, a.p);
   cudaError_t r = cudaGetLastError();
   if (r != cudaSuccess) return (int)r;
-  fa2_decode_merge_kernel<D, BF16><<<(unsigned)((long long)a.p.f.bh * a.p.f.n_q), 128, 0, a.stream>>>(a.p);
-  return (int)cudaGetLastError();
+  return launch_decode_merge<D, BF16>(a.p, a.stream);
 }
 
 template <int D, bool BF16>

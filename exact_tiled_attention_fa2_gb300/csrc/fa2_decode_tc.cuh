@@ -26,8 +26,7 @@ int launch_decode_tc_kernels(const LaunchArgs& a) {
   dp.splits = a.p.splits;
   dp.chunk = a.p.split_chunk;
   dp.base = a.p.split_base;
-  fa2_decode_merge_kernel<D, BF16><<<(unsigned)((long long)a.p.bh * a.p.n_q), 128, 0, a.stream>>>(dp);
-  return (int)cudaGetLastError();
+  return launch_decode_merge<D, BF16>(dp, a.stream);
 }
 
 template <int D>

@@ -454,6 +454,7 @@ __global__ void __launch_bounds__(192, DbufConfig<D>::CTAS_PER_SM)
   int bh, unit;
   static_assert(!(SPLIT && PACKED), "split-key mode runs on the plain grid");
   const int splits = SPLIT ? p.splits : 1;
+  if (SPLIT) grid_launch_dependents();   // the decode merge may be scheduled now; it waits for the partials
   // The whole CTA leaves together, before any barrier or TMEM set-up, when
   // it has no tile, its sequence is malformed or shorter than this tile's rows.
   // (The packed kernels keep the plain path behind a run-time test: built

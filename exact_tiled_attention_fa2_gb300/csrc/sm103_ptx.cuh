@@ -70,6 +70,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Programmatic dependent launch (a kernel launched with programmatic stream
+// serialization after another on the same stream): launch_dependents lets
+// the next kernel's CTAs be scheduled before this grid ends; the next kernel
+// calls grid_dependency_wait before it reads what this grid wrote, which
+// returns once this grid has completed and its memory operations are
+// visible.  Both are no-ops without such a launch.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // 16 bytes from shared memory (shared-window address).
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
